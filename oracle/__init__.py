@@ -1,0 +1,173 @@
+"""Float64 CPU oracle for the finite-automaton constrained denoising step.
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the CPU-baseline
+leg of the benchmark use it; the product path never imports it.  It shares no
+code with the CUDA path.
+
+`oracle.c` holds the chain forward-backward, forward-filter/backward-sample
+sampler, acceptor, commit rule and Philox4x32-10; `brute.py` enumerates every
+string for tiny cases.  Citations are in the C file's header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+OR_OK, OR_INVALID, OR_NOMEM, OR_EMPTY = 0, 1, 2, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain gcc, no target-specific flags)."""
+    src = os.path.join(_HERE, "oracle.c")
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
+        tmp = _SO + ".%d.tmp" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, src, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_SO)
+    P = ctypes.c_void_p
+    i32, i64 = ctypes.c_int32, ctypes.c_int64
+    lib.or_fa_new.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, P, P, P, P,
+                              ctypes.c_int, ctypes.POINTER(P)]
+    lib.or_fa_new.restype = ctypes.c_int
+    lib.or_fa_free.argtypes = [P]
+    lib.or_fa_sizes.argtypes = [P, P, P, P, P]
+    lib.or_fa_export.argtypes = [P] * 10
+    lib.or_transition_matrix.argtypes = [P, P, i32, P]
+    lib.or_transition_matrix.restype = ctypes.c_int
+    lib.or_posterior.argtypes = [P, ctypes.c_int, P, P, P, P, P, P, P, P, P]
+    lib.or_posterior.restype = ctypes.c_int
+    lib.or_sample.argtypes = [P, ctypes.c_int, P, P, ctypes.c_uint64, ctypes.c_int, P]
+    lib.or_sample.restype = ctypes.c_int
+    lib.or_path_count.argtypes = [P, ctypes.c_int, P]
+    lib.or_path_count.restype = ctypes.c_double
+    lib.or_topk.argtypes = [ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+    lib.or_philox4x32_10.argtypes = [P, P, P]
+    _lib = lib
+    return lib
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class OracleFA:
+    """The oracle's own compiled view of an automaton (see synth.Automaton for the fields)."""
+
+    def __init__(self, fa):
+        lib = _load()
+        self._keep = [np.ascontiguousarray(fa.accept, np.int32), np.ascontiguousarray(fa.edge_src, np.int32),
+                      np.ascontiguousarray(fa.edge_dst, np.int32), np.ascontiguousarray(fa.label_offsets, np.int64),
+                      np.ascontiguousarray(fa.label_tokens, np.int32)]
+        acc, src, dst, off, tok = self._keep
+        h = ctypes.c_void_p()
+        rc = lib.or_fa_new(fa.n_states, fa.start, _p(acc), acc.shape[0], src.shape[0], _p(src), _p(dst),
+                           _p(off), _p(tok), fa.vocab, ctypes.byref(h))
+        if rc != OR_OK:
+            raise ValueError("oracle rejected the automaton (code %d)" % rc)
+        self.h = h
+        self.S, self.V = fa.n_states, fa.vocab
+        e, i, d, na = np.zeros(1, np.int64), np.zeros(1, np.int64), np.zeros(1, np.int32), np.zeros(1, np.int32)
+        lib.or_fa_sizes(h, _p(e), _p(i), _p(d), _p(na))
+        self.E, self.I, self.is_dfa, self.n_accept = int(e[0]), int(i[0]), bool(d[0]), int(na[0])
+
+    def __del__(self):
+        if getattr(self, "h", None) and _lib is not None:
+            _lib.or_fa_free(self.h)
+            self.h = None
+
+    def canonical(self) -> dict:
+        """The canonical compiled arrays (label CSR, by-src, by-dst, token->edge)."""
+        E, I, S, V = self.E, self.I, self.S, self.V
+        out = dict(lab_off=np.zeros(E + 1, np.int64), lab_tok=np.zeros(max(I, 1), np.int32),
+                   src_off=np.zeros(S + 1, np.int32), src_edges=np.zeros(max(E, 1), np.int32),
+                   dst_off=np.zeros(S + 1, np.int32), dst_edges=np.zeros(max(E, 1), np.int32),
+                   tok_off=np.zeros(V + 1, np.int64), tok_edges=np.zeros(max(I, 1), np.int32),
+                   accept=np.zeros(max(self.n_accept, 1), np.int32))
+        _lib.or_fa_export(self.h, *[_p(out[k]) for k in ("lab_off", "lab_tok", "src_off", "src_edges", "dst_off",
+                                                          "dst_edges", "tok_off", "tok_edges", "accept")])
+        out["lab_tok"] = out["lab_tok"][:I]
+        out["tok_edges"] = out["tok_edges"][:I]
+        out["src_edges"] = out["src_edges"][:E]
+        out["dst_edges"] = out["dst_edges"][:E]
+        out["accept"] = out["accept"][:self.n_accept]
+        return out
+
+    def transition_matrix(self, probs_row: np.ndarray, committed_token: int = -1) -> np.ndarray:
+        row = np.ascontiguousarray(probs_row, np.float32)
+        M = np.zeros((self.S, self.S), np.float64)
+        rc = _lib.or_transition_matrix(self.h, _p(row), int(committed_token), _p(M))
+        assert rc == OR_OK
+        return M
+
+    def posterior(self, probs: np.ndarray, committed: Optional[np.ndarray] = None,
+                  tokens: Optional[np.ndarray] = None, want_all: bool = False,
+                  want_states: bool = False, want_messages: bool = False) -> dict:
+        """One sequence (probs [L, V]): logZ and the requested marginals / messages."""
+        probs = np.ascontiguousarray(probs, np.float32)
+        L = probs.shape[0]
+        com = None if committed is None else np.ascontiguousarray(committed, np.int32)
+        tok = None if tokens is None else np.ascontiguousarray(tokens, np.int32)
+        lz = np.zeros(1, np.float64)
+        mt = np.zeros(L, np.float64) if tok is not None else None
+        ma = np.zeros((L, self.V), np.float64) if want_all else None
+        sp = np.zeros((L + 1, self.S), np.float64) if want_states else None
+        la = np.zeros((L + 1, self.S), np.float64) if want_messages else None
+        lb = np.zeros((L + 1, self.S), np.float64) if want_messages else None
+        rc = _lib.or_posterior(self.h, L, _p(probs), _p(com), _p(tok), _p(lz), _p(mt), _p(ma), _p(sp),
+                               _p(la), _p(lb))
+        if rc not in (OR_OK, OR_EMPTY):
+            raise MemoryError("oracle out of memory")
+        return dict(logZ=float(lz[0]), empty=(rc == OR_EMPTY), marg_tokens=mt, marg_all=ma,
+                    state_post=sp, log_alpha=la, log_beta=lb)
+
+    def sample(self, probs: np.ndarray, committed: Optional[np.ndarray], n: int, seed: int) -> np.ndarray:
+        probs = np.ascontiguousarray(probs, np.float32)
+        L = probs.shape[0]
+        com = None if committed is None else np.ascontiguousarray(committed, np.int32)
+        out = np.zeros((n, L), np.int32)
+        rc = _lib.or_sample(self.h, L, _p(probs), _p(com), ctypes.c_uint64(seed), n, _p(out))
+        if rc == OR_EMPTY:
+            raise ValueError("empty constrained distribution")
+        assert rc == OR_OK
+        return out
+
+    def path_count(self, tokens: np.ndarray) -> float:
+        tok = np.ascontiguousarray(tokens, np.int32)
+        return float(_lib.or_path_count(self.h, tok.shape[0], _p(tok)))
+
+    def accepts(self, tokens: np.ndarray) -> bool:
+        return self.path_count(tokens) > 0.0
+
+
+def topk(marg: np.ndarray, committed: np.ndarray, k: int, lo: int, hi: int) -> np.ndarray:
+    lib = _load()
+    m = np.ascontiguousarray(marg, np.float64)
+    c = np.ascontiguousarray(committed, np.int32)
+    out = np.zeros(max(k, 1), np.int32)
+    lib.or_topk(m.shape[0], _p(m), _p(c), k, lo, hi, _p(out))
+    return out[:k]
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(ctr, np.uint32)
+    k = np.asarray(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    lib.or_philox4x32_10(_p(c), _p(k), _p(out))
+    return out
