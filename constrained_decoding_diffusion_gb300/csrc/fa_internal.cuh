@@ -1,0 +1,156 @@
+// Internal definitions shared by the compile and step translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/fa.h"
+
+// ----------------------------------------------------------------------------- host side
+
+// A compiled automaton: the canonical arrays (exported bit-exact by fa_export_csr) plus
+// the kernel-facing "cell" layout.  A cell is a distinct (src, dst) pair; its token list is
+// the sorted multiset union of the label sets of all edges src -> dst, so the cell's sum of
+// token weights is exactly M_t(src, dst) (parallel edges add, as NFA path counting needs).
+struct fa_automaton {
+    int32_t S = 0, V = 0, E = 0, start = 0, n_accept = 0, is_dfa = 0, device = 0;
+    int64_t I = 0;
+    int32_t n_cells = 0;
+    int32_t max_cell_len = 0;
+    // canonical arrays (device)
+    int64_t *lab_off = nullptr;
+    int32_t *lab_tok = nullptr;
+    int32_t *src_off = nullptr, *src_edges = nullptr;
+    int32_t *dst_off = nullptr, *dst_edges = nullptr;
+    int64_t *tok_off = nullptr;
+    int32_t *tok_edges = nullptr;
+    int32_t *accept = nullptr;       // [n_accept] ascending
+    int32_t *accept_mask = nullptr;  // [S] 0/1
+    int32_t *edge_src = nullptr, *edge_dst = nullptr;
+    // cells (device), sorted by (src, dst)
+    int32_t *row_cell_off = nullptr;  // [S+1]
+    int32_t *cell_dst = nullptr;      // [n_cells]
+    int32_t *cell_src = nullptr;      // [n_cells]
+    int64_t *cell_off = nullptr;      // [n_cells+1]
+    int32_t *cell_tok = nullptr;      // [I]
+    // row blocks for the reweight grid: for nrb = 2^p (p = 0..n_rb_levels-1), the bounds of
+    // nrb contiguous row ranges with balanced token counts, at rb_bounds + (2^p - 1) + p.
+    int32_t *rb_bounds = nullptr;
+    int32_t n_rb_levels = 0;
+    std::vector<int32_t> h_rb_bounds;
+    void *blob = nullptr;  // one device allocation holding every array above
+    size_t blob_bytes = 0;
+};
+
+void fa_set_error(const std::string &msg);
+
+// ----------------------------------------------------------------------------- device side
+
+#define FA_INT_NONE (-2147483647 - 1)
+
+// floor(log2 x) of a positive normal float from its exponent field (subnormals give -127).
+__device__ __forceinline__ int fa_exponent(float x) {
+    return ((__float_as_int(x) >> 23) & 0xff) - 127;
+}
+
+// x * 2^d exactly (up to flush of results below the fp32 subnormal range).
+__device__ __forceinline__ float fa_scale_pow2(float x, int d) {
+    if (d < -300) return 0.0f;
+    if (d > 254) d = 254;
+    return ldexpf(x, d);
+}
+
+// Split x > 0 into m in [1, 2) and integer e with x = m * 2^e (normal or subnormal x).
+__device__ __forceinline__ void fa_split(float x, float &m, int &e) {
+    int bits = __float_as_int(x);
+    int ex = (bits >> 23) & 0xff;
+    if (ex == 0) {  // subnormal: renormalise
+        x *= 16777216.0f;  // 2^24
+        bits = __float_as_int(x);
+        ex = ((bits >> 23) & 0xff) - 24;
+    }
+    e = ex - 127;
+    m = __int_as_float((bits & 0x807fffff) | 0x3f800000);
+}
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): a counter-based generator; one call
+// maps (counter, key) to four independent 32-bit words.
+struct fa_u4 { uint32_t x, y, z, w; };
+
+__device__ __forceinline__ fa_u4 fa_philox(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                           uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    }
+    return fa_u4{c0, c1, c2, c3};
+}
+
+// Uniform in [0, 1) with 24 random bits for draw `idx` of sequence b and purpose p.
+// The counter is (idx, b, offset<<2 | p, offset>>30): distinct for every draw of one step and
+// for every offset below 2^62.
+enum { FA_RNG_ROOT = 0, FA_RNG_MID = 1, FA_RNG_LEAF = 2 };
+
+__device__ __forceinline__ float fa_uniform(uint64_t seed, uint64_t offset, uint32_t idx, uint32_t b,
+                                            uint32_t purpose) {
+    fa_u4 r = fa_philox(idx, b, (uint32_t)(offset << 2) | purpose, (uint32_t)(offset >> 30),
+                        (uint32_t)seed, (uint32_t)(seed >> 32));
+    return (float)(r.x >> 8) * (1.0f / 16777216.0f);
+}
+
+__device__ __forceinline__ float fa_warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int fa_warp_max_int(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// An extended-range non-negative number acc * 2^E accumulated term by term (acc is kept
+// near [1, 2^24) so no term below the fp32 range of the running maximum is lost).
+struct fa_xacc {
+    float acc;
+    int E;
+    __device__ __forceinline__ void init() { acc = 0.0f; E = FA_INT_NONE; }
+    // add m * 2^e with m in [0.5, 4)
+    __device__ __forceinline__ void add(float m, int e) {
+        if (m <= 0.0f) return;
+        if (E == FA_INT_NONE) { acc = m; E = e; return; }
+        if (e > E) { acc = fa_scale_pow2(acc, E - e) + m; E = e; }
+        else acc += fa_scale_pow2(m, e - E);
+    }
+    __device__ __forceinline__ void merge(float m2, int e2) {
+        if (e2 == FA_INT_NONE || m2 <= 0.0f) return;
+        if (E == FA_INT_NONE) { acc = m2; E = e2; return; }
+        if (e2 > E) { acc = fa_scale_pow2(acc, E - e2) + m2; E = e2; }
+        else acc += fa_scale_pow2(m2, e2 - E);
+    }
+    __device__ __forceinline__ void warp_reduce() {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            float m2 = __shfl_xor_sync(0xffffffffu, acc, o);
+            int e2 = __shfl_xor_sync(0xffffffffu, E, o);
+            merge(m2, e2);
+        }
+    }
+    // normalise to mantissa in [1, 2) (or 0 with exponent 0)
+    __device__ __forceinline__ void normalised(float &m, int &e) const {
+        if (E == FA_INT_NONE || acc <= 0.0f) { m = 0.0f; e = 0; return; }
+        int ee;
+        float mm;
+        fa_split(acc, mm, ee);
+        m = mm;
+        e = E + ee;
+    }
+};

@@ -1,0 +1,744 @@
+// The constrained denoising step on one GPU: emission reweighting, the span-matrix up-sweep,
+// top-down midpoint sampling, prefix/suffix messages, leaf tokens and marginals, and the
+// top-k commit.  Method: "Constrained Decoding for Diffusion Language Models via Efficient
+// Inference over Finite Automata" (paperfeed.app summary, sections "The insight" and "The
+// scan trick"; papernotes.org notes, key designs 1-3).
+//
+// Span number format.  A span matrix A[l, r) = M_{l+1} ... M_r is stored as an fp32
+// mantissa matrix Ã and one power-of-two exponent per row: A[i, j] = Ã[i, j] * 2^rho[i].
+// rmax[i] holds the bit pattern of max_j Ã[i, j] (0 for an all-zero row).  Products of
+// hundreds of probabilities leave the fp32 range long before a sequence ends, and rows of one
+// span differ by far more than 2^254 once committed tokens pin the path, so a single
+// exponent per matrix would flush whole rows; per-row exponents keep every row at full
+// relative precision.  Only entries more than ~2^-126 below their own row's maximum are lost.
+#include <cfloat>
+#include <cmath>
+#include <string>
+#include <vector>
+
+#include "fa_internal.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// ----------------------------------------------------------------------------- workspace plan
+
+struct Plan {
+    int B = 0, L = 0, S = 0, V = 0, K = 0, Lp = 1;
+    int nk[18] = {0};
+    size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, mu[18] = {0};
+    size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, zsum = 0, zexp = 0;
+    size_t total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Plan make_plan(const fa_automaton *a, int B, int L) {
+    Plan p;
+    p.B = B; p.L = L; p.S = a->S; p.V = a->V;
+    p.Lp = 1; p.K = 0;
+    while (p.Lp < L) { p.Lp <<= 1; p.K++; }
+    size_t off = 0;
+    const size_t S = (size_t)a->S;
+    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + (bytes ? bytes : 1)); return o; };
+    for (int k = 0; k <= p.K; ++k) {
+        p.nk[k] = (L + (1 << k) - 1) >> k;
+        size_t nodes = (size_t)B * (size_t)p.nk[k];
+        p.mant[k] = take(nodes * S * S * sizeof(float));
+        p.rho[k] = take(nodes * S * sizeof(int32_t));
+        p.rmax[k] = take(nodes * S * sizeof(int32_t));
+        p.mu[k] = take(k ? nodes * S * sizeof(int32_t) : 0);
+    }
+    size_t bnd = (size_t)B * (size_t)(L + 1);
+    p.z = take(bnd * sizeof(int32_t));
+    p.am = take(bnd * S * sizeof(float));
+    p.ae = take(bnd * S * sizeof(int32_t));
+    p.bm = take(bnd * S * sizeof(float));
+    p.be = take(bnd * S * sizeof(int32_t));
+    p.zsum = take((size_t)B * sizeof(float));
+    p.zexp = take((size_t)B * sizeof(int32_t));
+    p.total = off;
+    return p;
+}
+
+// Device view of the compiled automaton.
+struct DevFA {
+    int S, V, start, n_accept;
+    const int32_t *accept, *accept_mask, *edge_src, *edge_dst;
+    const int64_t *tok_off;
+    const int32_t *tok_edges;
+    const int32_t *row_cell_off, *cell_dst, *cell_src;
+    const int64_t *cell_off;
+    const int32_t *cell_tok;
+};
+
+DevFA dev_view(const fa_automaton *a) {
+    DevFA d;
+    d.S = a->S; d.V = a->V; d.start = a->start; d.n_accept = a->n_accept;
+    d.accept = a->accept; d.accept_mask = a->accept_mask; d.edge_src = a->edge_src; d.edge_dst = a->edge_dst;
+    d.tok_off = a->tok_off; d.tok_edges = a->tok_edges;
+    d.row_cell_off = a->row_cell_off; d.cell_dst = a->cell_dst; d.cell_src = a->cell_src;
+    d.cell_off = a->cell_off; d.cell_tok = a->cell_tok;
+    return d;
+}
+
+// ----------------------------------------------------------------------------- block helpers
+
+// Inverse-CDF draw over n weights given by w(i) >= 0: the first i whose running sum exceeds
+// u * total (total from the same loop order), clamped to the last positive weight.  Returns
+// -1 when every weight is zero.  Executed by one full warp; all lanes get the result.
+template <class WF>
+__device__ int warp_categorical(int n, float u, WF w) {
+    const int lane = threadIdx.x & 31;
+    float total = 0.0f;
+    for (int base = 0; base < n; base += 32) {
+        int i = base + lane;
+        float x = (i < n) ? w(i) : 0.0f;
+        total += fa_warp_sum(x);
+    }
+    if (!(total > 0.0f)) return -1;
+    const float target = u * total;
+    float run = 0.0f;
+    int last_pos = -1;
+    for (int base = 0; base < n; base += 32) {
+        int i = base + lane;
+        float x = (i < n) ? w(i) : 0.0f;
+        float incl = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        unsigned hit = __ballot_sync(0xffffffffu, x > 0.0f && run + incl > target);
+        if (hit) return base + __ffs(hit) - 1;
+        unsigned pos = __ballot_sync(0xffffffffu, x > 0.0f);
+        if (pos) last_pos = base + 31 - __clz(pos);
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return last_pos;
+}
+
+// ----------------------------------------------------------------------------- 1. reweight
+
+// One block per (position, row block): M_t(s, s') for rows s in [r0, r1) as a dense fp32 row
+// segment with row exponent 0.  A masked position sums its probabilities over each cell's
+// tokens (papernotes.org key design 1: g(x=v | z=e) = 1[v in label(e)] p_t(v), aggregated
+// over edges s -> s'); a committed position counts the edges s -> s' that carry its token.
+__global__ void __launch_bounds__(kThreads) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
+                                                     const int32_t *__restrict__ committed,
+                                                     const int32_t *__restrict__ rb, int nrb, float *mant,
+                                                     int32_t *rho, int32_t *rmax) {
+    __shared__ int smax[FA_MAX_STATES];
+    const int S = fa.S;
+    const int t = blockIdx.x / nrb, r = blockIdx.x % nrb, b = blockIdx.y;
+    const int r0 = rb[r], r1 = rb[r + 1];
+    if (r0 >= r1) return;
+    const size_t pos = (size_t)b * L + t;
+    float *M = mant + pos * (size_t)S * S;
+    for (size_t i = (size_t)r0 * S + threadIdx.x; i < (size_t)r1 * S; i += kThreads) M[i] = 0.0f;
+    for (int i = threadIdx.x; i < r1 - r0; i += kThreads) smax[i] = 0;
+    __syncthreads();
+    const int c = committed[pos];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (c < 0) {
+        const float *prow = probs + pos * (size_t)fa.V;
+        const int cb = fa.row_cell_off[r0], ce = fa.row_cell_off[r1];
+        for (int cell = cb + warp; cell < ce; cell += kWarps) {
+            const int64_t a0 = fa.cell_off[cell], a1 = fa.cell_off[cell + 1];
+            float acc = 0.0f;
+            for (int64_t j = a0 + lane; j < a1; j += 32) acc += __ldg(prow + fa.cell_tok[j]);
+            acc = fa_warp_sum(acc);
+            if (lane == 0) {
+                const int s = fa.cell_src[cell];
+                M[(size_t)s * S + fa.cell_dst[cell]] = acc;
+                atomicMax(&smax[s - r0], __float_as_int(acc));
+            }
+        }
+    } else if (c < fa.V) {
+        const int64_t a0 = fa.tok_off[c], a1 = fa.tok_off[c + 1];
+        for (int64_t j = a0 + threadIdx.x; j < a1; j += kThreads) {
+            const int e = fa.tok_edges[j];
+            const int s = fa.edge_src[e];
+            if (s >= r0 && s < r1) atomicAdd(&M[(size_t)s * S + fa.edge_dst[e]], 1.0f);
+        }
+        __syncthreads();
+        for (int64_t j = a0 + threadIdx.x; j < a1; j += kThreads) {
+            const int e = fa.tok_edges[j];
+            const int s = fa.edge_src[e];
+            if (s >= r0 && s < r1) atomicMax(&smax[s - r0], __float_as_int(M[(size_t)s * S + fa.edge_dst[e]]));
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < r1 - r0; i += kThreads) {
+        rho[pos * S + r0 + i] = 0;
+        if (rmax) rmax[pos * S + r0 + i] = smax[i];
+    }
+}
+
+// ----------------------------------------------------------------------------- 2. up-sweep
+
+// Row shift for the product C = A_left * A_right at tree level k (paperfeed.app, "The scan
+// trick": 2^k-step transitions from two 2^(k-1)-step ones).  For row i,
+//   C[i, :] = 2^rhoL[i] * sum_m Ã_L[i, m] 2^rhoR[m] Ã_R[m, :]
+// and mu[i] = max over m with Ã_L[i, m] > 0 and a nonzero right row m of
+// rhoR[m] + e(rmaxR[m]) + e(Ã_L[i, m]), so the prescaled left row
+// Ã_L[i, m] 2^(rhoR[m] - mu[i]) keeps its largest contribution near 1.  Also clears rmax of
+// the product.  One warp per row.
+__global__ void __launch_bounds__(kThreads) k_rowshift(int S, int L, int k, int nk, const float *__restrict__ mant_c,
+                                                     const int32_t *__restrict__ rho_c,
+                                                     const int32_t *__restrict__ rmax_c, int nc, int32_t *mu,
+                                                     int32_t *rmax_p) {
+    const int b = blockIdx.z, j = blockIdx.y;
+    const int i = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (i >= S) return;
+    const size_t pnode = (size_t)b * nk + j;
+    if (lane == 0) rmax_p[pnode * S + i] = 0;
+    const bool has_right = ((2 * j + 1) << (k - 1)) < L;
+    if (!has_right) return;
+    const size_t lnode = (size_t)b * nc + 2 * j, rnode = lnode + 1;
+    const float *Lrow = mant_c + lnode * (size_t)S * S + (size_t)i * S;
+    const int32_t *rhoR = rho_c + rnode * S;
+    const int32_t *rmaxR = rmax_c + rnode * S;
+    int best = FA_INT_NONE;
+    for (int m = lane; m < S; m += 32) {
+        const float x = Lrow[m];
+        const int rr = rmaxR[m];
+        if (x > 0.0f && rr > 0) best = max(best, rhoR[m] + fa_exponent(__int_as_float(rr)) + fa_exponent(x));
+    }
+    best = fa_warp_max_int(best);
+    if (lane == 0) mu[pnode * S + i] = best;
+}
+
+constexpr int GBM = 64, GBN = 64, GBK = 16;
+
+// C̃ = (Ã_L prescaled per (row, m)) x Ã_R in fp32 FMA, 64x64 tiles, 4x4 per thread.  A
+// product whose right child lies wholly in the padding beyond L is a copy of the left child.
+__global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int nk, const float *__restrict__ mant_c,
+                                                      const int32_t *__restrict__ rho_c,
+                                                      const int32_t *__restrict__ rmax_c, int nc,
+                                                      const int32_t *__restrict__ mu, float *mant_p, int32_t *rho_p,
+                                                      int32_t *rmax_p) {
+    __shared__ float As[GBK][GBM + 4];
+    __shared__ float Bs[GBK][GBN + 4];
+    __shared__ int mu_s[GBM];
+    const int tiles = (S + GBN - 1) / GBN;
+    const long flat = blockIdx.x;                       // ((b * nk + node) * tiles + ti) * tiles + tj
+    const int tj = (int)(flat % tiles), ti = (int)((flat / tiles) % tiles);
+    const long bn = flat / ((long)tiles * tiles);
+    const int node = (int)(bn % nk), b = (int)(bn / nk);
+    const int i0 = ti * GBM, j0 = tj * GBN;
+    const int tid = threadIdx.x;
+    const size_t pnode = (size_t)b * nk + node;
+    const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
+    const float *A = mant_c + lnode * (size_t)S * S;
+    float *C = mant_p + pnode * (size_t)S * S;
+    const bool has_right = ((2 * node + 1) << (k - 1)) < L;
+    if (!has_right) {
+        for (int q = tid; q < GBM * GBN; q += kThreads) {
+            const int r = q / GBN, c = q % GBN;
+            if (i0 + r < S && j0 + c < S) C[(size_t)(i0 + r) * S + j0 + c] = A[(size_t)(i0 + r) * S + j0 + c];
+        }
+        if (tj == 0)
+            for (int r = tid; r < GBM; r += kThreads)
+                if (i0 + r < S) {
+                    rho_p[pnode * S + i0 + r] = rho_c[lnode * S + i0 + r];
+                    rmax_p[pnode * S + i0 + r] = rmax_c[lnode * S + i0 + r];
+                }
+        return;
+    }
+    const float *Bm = mant_c + rnode * (size_t)S * S;
+    const int32_t *rhoR = rho_c + rnode * S;
+    const int32_t *rmaxR = rmax_c + rnode * S;
+    for (int r = tid; r < GBM; r += kThreads) mu_s[r] = (i0 + r < S) ? mu[pnode * S + i0 + r] : FA_INT_NONE;
+    __syncthreads();
+    const int tx = tid & 15, ty = tid >> 4;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < S; k0 += GBK) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * kThreads;
+            const int r = idx / GBK, kk = idx % GBK;
+            const int i = i0 + r, m = k0 + kk;
+            float v = 0.0f;
+            if (i < S && m < S) {
+                const float x = A[(size_t)i * S + m];
+                const int mr = mu_s[r];
+                if (x > 0.0f && mr != FA_INT_NONE && rmaxR[m] > 0) v = fa_scale_pow2(x, rhoR[m] - mr);
+            }
+            As[kk][r] = v;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * kThreads;
+            const int kk = idx / GBN, c = idx % GBN;
+            const int m = k0 + kk, j = j0 + c;
+            Bs[kk][c] = (m < S && j < S) ? Bm[(size_t)m * S + j] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < GBK; ++kk) {
+            float a[4], bb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) { a[q] = As[kk][ty * 4 + q]; bb[q] = Bs[kk][tx * 4 + q]; }
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(a[p], bb[q], acc[p][q]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int i = i0 + ty * 4 + p;
+        float mx = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = j0 + tx * 4 + q;
+            if (i < S && j < S) {
+                C[(size_t)i * S + j] = acc[p][q];
+                mx = fmaxf(mx, acc[p][q]);
+            }
+        }
+#pragma unroll
+        for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (tx == 0 && i < S) {
+            if (mx > 0.0f) atomicMax(&rmax_p[pnode * S + i], __float_as_int(mx));
+            if (tj == 0) {
+                const int mr = mu_s[ty * 4 + p];
+                rho_p[pnode * S + i] = (mr == FA_INT_NONE) ? 0 : rho_c[lnode * S + i] + mr;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------- 3. root
+
+// Z = e_{s0}^T A_root 1_F, the end state z_L ~ A_root[s0, f] over f in F, and the boundary
+// messages alpha_0 = e_{s0}, beta_L = 1_F (papernotes.org key design 2: sample the boundary
+// states from the joint marginal; the start is pinned to s0).
+__global__ void __launch_bounds__(kThreads) k_root(DevFA fa, int L, int K, int nK, const float *__restrict__ mant_root,
+                                                 const int32_t *__restrict__ rho_root, uint64_t seed, uint64_t offset,
+                                                 int32_t *z, float *am, int32_t *ae, float *bm, int32_t *be,
+                                                 float *zsum_ws, int32_t *zexp_ws, double *logZ, int32_t *status) {
+    const int b = blockIdx.x, S = fa.S, s0 = fa.start;
+    const float *row = mant_root + (size_t)b * nK * S * S + (size_t)s0 * S;
+    const size_t bnd0 = (size_t)b * (L + 1);
+    for (int s = threadIdx.x; s < S; s += kThreads) {
+        am[bnd0 * S + s] = (s == s0) ? 1.0f : 0.0f;
+        ae[bnd0 * S + s] = 0;
+        bm[(bnd0 + L) * S + s] = fa.accept_mask[s] ? 1.0f : 0.0f;
+        be[(bnd0 + L) * S + s] = 0;
+    }
+    if (threadIdx.x >= 32) return;
+    const float u = fa_uniform(seed, offset, 0u, (uint32_t)b, FA_RNG_ROOT);
+    const int pick = warp_categorical(fa.n_accept, u, [&](int i) { return row[fa.accept[i]]; });
+    float tot = 0.0f;
+    for (int i = threadIdx.x; i < fa.n_accept; i += 32) tot += row[fa.accept[i]];
+    tot = fa_warp_sum(tot);
+    if (threadIdx.x == 0) {
+        z[bnd0] = s0;
+        if (pick < 0 || !(tot > 0.0f)) {
+            status[b] = FA_ROW_EMPTY;
+            logZ[b] = -INFINITY;
+            z[bnd0 + L] = s0;
+            zsum_ws[b] = 0.0f;
+            zexp_ws[b] = 0;
+        } else {
+            status[b] = FA_ROW_OK;
+            const int rr = rho_root[(size_t)b * nK * S + s0];
+            logZ[b] = (double)rr * 0.69314718055994530942 + log((double)tot);
+            z[bnd0 + L] = fa.accept[pick];
+            zsum_ws[b] = tot;
+            zexp_ws[b] = rr;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------- 4. top-down
+
+// Midpoints of the nodes of level k+1: z_m ~ A[l, m)[z_l, s] * A[m, r)[s, z_r] (paperfeed.app,
+// "The scan trick"; papernotes.org key design 2: given the segment ends, the halves are
+// conditionally independent given the midpoint).  One warp per node.
+__global__ void __launch_bounds__(kThreads) k_midpoint(int S, int B, int L, int k, int nc, const float *__restrict__ mant_c,
+                                                     const int32_t *__restrict__ rho_c, uint64_t seed,
+                                                     uint64_t offset, int32_t *z, int32_t *status) {
+    const int np = (L + (1 << (k + 1)) - 1) >> (k + 1);
+    const long gw = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (gw >= (long)B * np) return;
+    const int b = (int)(gw / np), j = (int)(gw % np);
+    const int l = j << (k + 1), m = l + (1 << k);
+    if (m >= L) return;
+    const int r = min(l + (1 << (k + 1)), L);
+    if (__shfl_sync(0xffffffffu, status[b], 0) != FA_ROW_OK) return;
+    const int32_t *zb = z + (size_t)b * (L + 1);
+    const int zl = zb[l], zr = zb[r];
+    const size_t lnode = (size_t)b * nc + 2 * j, rnode = lnode + 1;
+    const float *Lrow = mant_c + lnode * (size_t)S * S + (size_t)zl * S;
+    const float *R = mant_c + rnode * (size_t)S * S;
+    const int32_t *rhoR = rho_c + rnode * S;
+    const int lane = threadIdx.x & 31;
+    int emax = FA_INT_NONE;
+    for (int s = lane; s < S; s += 32) {
+        const float a = Lrow[s], c = R[(size_t)s * S + zr];
+        if (a > 0.0f && c > 0.0f) emax = max(emax, rhoR[s] + fa_exponent(a) + fa_exponent(c));
+    }
+    emax = fa_warp_max_int(emax);
+    int pick = -1;
+    if (emax != FA_INT_NONE) {
+        const float u = fa_uniform(seed, offset, (uint32_t)m, (uint32_t)b, FA_RNG_MID);
+        pick = warp_categorical(S, u, [&](int s) {
+            const float a = Lrow[s], c = R[(size_t)s * S + zr];
+            if (!(a > 0.0f && c > 0.0f)) return 0.0f;
+            float ma, mc;
+            int ea, ec;
+            fa_split(a, ma, ea);
+            fa_split(c, mc, ec);
+            return fa_scale_pow2(ma * mc, rhoR[s] + ea + ec - emax);
+        });
+    }
+    if (lane == 0) {
+        if (pick < 0) status[b] = FA_ROW_UNDERFLOW;
+        else z[(size_t)b * (L + 1) + m] = pick;
+    }
+}
+
+// Prefix messages alpha_m = alpha_l A[l, m) (one thread per column) for the nodes of level
+// k+1; alpha is kept per entry as mantissa in [1, 2) and exponent, so no state is lost to range.
+__global__ void __launch_bounds__(kThreads) k_alpha(int S, int L, int k, int nc, const float *__restrict__ mant_c,
+                                                  const int32_t *__restrict__ rho_c, float *am, int32_t *ae) {
+    extern __shared__ unsigned char smem_raw[];
+    float *sa = (float *)smem_raw;
+    int *se = (int *)(sa + S);
+    const int b = blockIdx.z, j = blockIdx.y;
+    const int l = j << (k + 1), m = l + (1 << k);
+    if (m >= L) return;
+    const size_t bl = ((size_t)b * (L + 1) + l) * S, bmid = ((size_t)b * (L + 1) + m) * S;
+    for (int s = threadIdx.x; s < S; s += kThreads) { sa[s] = am[bl + s]; se[s] = ae[bl + s]; }
+    __syncthreads();
+    const int col = blockIdx.x * kThreads + threadIdx.x;
+    if (col >= S) return;
+    const size_t lnode = (size_t)b * nc + 2 * j;
+    const float *A = mant_c + lnode * (size_t)S * S;
+    const int32_t *rho = rho_c + lnode * S;
+    fa_xacc x;
+    x.init();
+    for (int q = 0; q < S; ++q) {
+        const float a = sa[q];
+        if (a <= 0.0f) continue;
+        const float v = A[(size_t)q * S + col];
+        if (v <= 0.0f) continue;
+        float mv;
+        int ev;
+        fa_split(v, mv, ev);
+        x.add(a * mv, se[q] + rho[q] + ev);
+    }
+    float mo;
+    int eo;
+    x.normalised(mo, eo);
+    am[bmid + col] = mo;
+    ae[bmid + col] = eo;
+}
+
+// Suffix messages beta_m = A[m, r) beta_r (one warp per row) for the nodes of level k+1.
+__global__ void __launch_bounds__(kThreads) k_beta(int S, int L, int k, int nc, const float *__restrict__ mant_c,
+                                                 const int32_t *__restrict__ rho_c, float *bm, int32_t *be) {
+    extern __shared__ unsigned char smem_raw[];
+    float *sb = (float *)smem_raw;
+    int *se = (int *)(sb + S);
+    const int b = blockIdx.z, j = blockIdx.y;
+    const int l = j << (k + 1), m = l + (1 << k);
+    if (m >= L) return;
+    const int r = min(l + (1 << (k + 1)), L);
+    const size_t br = ((size_t)b * (L + 1) + r) * S, bmid = ((size_t)b * (L + 1) + m) * S;
+    for (int s = threadIdx.x; s < S; s += kThreads) { sb[s] = bm[br + s]; se[s] = be[br + s]; }
+    __syncthreads();
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= S) return;
+    const size_t rnode = (size_t)b * nc + 2 * j + 1;
+    const float *Rrow = mant_c + rnode * (size_t)S * S + (size_t)row * S;
+    fa_xacc x;
+    x.init();
+    for (int q = lane; q < S; q += 32) {
+        const float bv = sb[q];
+        if (bv <= 0.0f) continue;
+        const float v = Rrow[q];
+        if (v <= 0.0f) continue;
+        float mv;
+        int ev;
+        fa_split(v, mv, ev);
+        x.add(bv * mv, se[q] + ev);
+    }
+    x.warp_reduce();
+    if (lane == 0) {
+        float mo;
+        int eo;
+        x.normalised(mo, eo);
+        bm[bmid + row] = mo;
+        be[bmid + row] = (mo > 0.0f) ? eo + rho_c[rnode * S + row] : 0;
+    }
+}
+
+// ----------------------------------------------------------------------------- 5. leaves
+
+// Token at each position: committed positions echo their token; a masked position draws
+// v ~ w_t(v) over the tokens of the edges z_{t-1} -> z_t (paperfeed.app: all tokens emit in
+// parallel at the leaves), then its constrained marginal
+//   p(x_t = v) = w_t(v) sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / Z
+// (papernotes.org key design 3).  One warp per position.
+__global__ void __launch_bounds__(kThreads) k_leaf(DevFA fa, int B, int L, const float *__restrict__ probs,
+                                                 const int32_t *__restrict__ committed, uint64_t seed, uint64_t offset,
+                                                 const int32_t *__restrict__ z, const float *__restrict__ am,
+                                                 const int32_t *__restrict__ ae, const float *__restrict__ bm,
+                                                 const int32_t *__restrict__ be, const float *__restrict__ zsum_ws,
+                                                 const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg,
+                                                 int32_t *status) {
+    const long gw = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (gw >= (long)B * L) return;
+    const int b = (int)(gw / L), t = (int)(gw % L);
+    const int lane = threadIdx.x & 31;
+    const size_t pos = (size_t)b * L + t;
+    const int c = committed[pos];
+    if (c >= 0) {
+        if (lane == 0) { tokens[pos] = c; marg[pos] = 1.0f; }
+        return;
+    }
+    if (__shfl_sync(0xffffffffu, status[b], 0) != FA_ROW_OK) {
+        if (lane == 0) { tokens[pos] = -1; marg[pos] = 0.0f; }
+        return;
+    }
+    const int S = fa.S;
+    const int32_t *zb = z + (size_t)b * (L + 1);
+    const int zp = zb[t], zn = zb[t + 1];
+    int lo = fa.row_cell_off[zp], hi = fa.row_cell_off[zp + 1];
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (fa.cell_dst[mid] < zn) lo = mid + 1; else hi = mid;
+    }
+    const bool found = lo < fa.row_cell_off[zp + 1] && fa.cell_dst[lo] == zn;
+    int v = -1;
+    const float *prow = probs + pos * (size_t)fa.V;
+    if (found) {
+        const int64_t a0 = fa.cell_off[lo];
+        const int n = (int)(fa.cell_off[lo + 1] - a0);
+        const float u = fa_uniform(seed, offset, (uint32_t)t, (uint32_t)b, FA_RNG_LEAF);
+        const int pick = warp_categorical(n, u, [&](int i) { return __ldg(prow + fa.cell_tok[a0 + i]); });
+        if (pick >= 0) v = fa.cell_tok[a0 + pick];
+    }
+    if (v < 0) {
+        if (lane == 0) { status[b] = FA_ROW_UNDERFLOW; tokens[pos] = -1; marg[pos] = 0.0f; }
+        return;
+    }
+    const size_t ba = ((size_t)b * (L + 1) + t) * S, bb = ((size_t)b * (L + 1) + t + 1) * S;
+    fa_xacc x;
+    x.init();
+    for (int64_t j = fa.tok_off[v] + lane; j < fa.tok_off[v + 1]; j += 32) {
+        const int e = fa.tok_edges[j];
+        const int s = fa.edge_src[e], d = fa.edge_dst[e];
+        const float a = am[ba + s], bv = bm[bb + d];
+        if (a > 0.0f && bv > 0.0f) x.add(a * bv, ae[ba + s] + be[bb + d]);
+    }
+    x.warp_reduce();
+    if (lane == 0) {
+        tokens[pos] = v;
+        float mo;
+        int eo;
+        x.normalised(mo, eo);
+        const float zs = zsum_ws[b];
+        double mval = 0.0;
+        if (mo > 0.0f && zs > 0.0f)
+            mval = ldexp((double)__ldg(prow + v) * (double)mo / (double)zs, eo - zexp_ws[b]);
+        marg[pos] = (float)mval;
+    }
+}
+
+// ----------------------------------------------------------------------------- 6. commit
+
+// Per sequence, the k masked positions of [lo, hi) with the largest marginal, descending,
+// ties to the lower position (papernotes.org key design 3, the "Mar" confidence; LLaDA's
+// highest-probability rule in the paperfeed.app summary).  Rank by counting larger keys.
+// A sequence whose status is not OK gets no commits and -1 tokens / 0 marginals at every
+// masked position (some leaves may have been drawn before the failure was recorded).
+__global__ void __launch_bounds__(kThreads) k_topk(int L, int k, int lo, int hi, float *marg,
+                                                 const int32_t *__restrict__ committed,
+                                                 const int32_t *__restrict__ status, int32_t *out, int32_t *tokens) {
+    const int b = blockIdx.x;
+    int32_t *o = out + (size_t)b * k;
+    for (int i = threadIdx.x; i < k; i += kThreads) o[i] = -1;
+    __syncthreads();
+    if (status[b] != FA_ROW_OK) {
+        for (int t = threadIdx.x; t < L; t += kThreads)
+            if (committed[(size_t)b * L + t] < 0) { tokens[(size_t)b * L + t] = -1; marg[(size_t)b * L + t] = 0.0f; }
+        return;
+    }
+    const float *mg = marg + (size_t)b * L;
+    const int32_t *cm = committed + (size_t)b * L;
+    auto key = [&](int t) -> unsigned long long {
+        if (t < lo || t >= hi || cm[t] >= 0) return 0ull;
+        return ((unsigned long long)(unsigned)__float_as_int(mg[t]) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)t);
+    };
+    for (int t = max(lo, 0) + threadIdx.x; t < min(hi, L); t += kThreads) {
+        const unsigned long long kt = key(t);
+        if (!kt) continue;
+        int rank = 0;
+        for (int q = max(lo, 0); q < min(hi, L) && rank < k; ++q) rank += key(q) > kt;
+        if (rank < k) o[rank] = t;
+    }
+}
+
+// L = 0: the empty string is the only candidate.
+__global__ void k_empty_length(int start, const int32_t *accept_mask, int B, int k, double *logZ, int32_t *status,
+                               int32_t *commit_idx) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const bool ok = accept_mask[start] != 0;
+    logZ[b] = ok ? 0.0 : -INFINITY;
+    status[b] = ok ? FA_ROW_OK : FA_ROW_EMPTY;
+    for (int i = 0; i < k; ++i) commit_idx[(size_t)b * k + i] = -1;
+}
+
+// ----------------------------------------------------------------------------- host glue
+
+fa_status launch_check(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        fa_set_error(std::string(what) + ": " + cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+int pick_row_blocks(const fa_automaton *a, long positions) {
+    // aim for roughly four blocks of work per SM over the masked positions
+    int lvl = 0;
+    while (lvl + 1 < a->n_rb_levels && positions * (1L << lvl) < 152L * 4) ++lvl;
+    return lvl;
+}
+
+fa_status check_device(const fa_automaton *a, const char *fn) {
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (dev != a->device) {
+        fa_set_error(std::string(fn) + ": current device differs from the automaton's device");
+        return FA_ERR_INVALID_ARG;
+    }
+    return FA_OK;
+}
+
+fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *probs, const int32_t *committed,
+                          float *mant, int32_t *rho, int32_t *rmax, cudaStream_t st) {
+    const int lvl = pick_row_blocks(a, (long)B * L);
+    const int nrb = 1 << lvl;
+    const int32_t *rb = a->rb_bounds + (nrb - 1) + lvl;
+    dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
+    k_reweight<<<grid, kThreads, 0, st>>>(dev_view(a), L, probs, committed, rb, nrb, mant, rho, rmax);
+    return launch_check("reweight");
+}
+
+}  // namespace
+
+extern "C" fa_status fa_step_workspace_bytes(const fa_automaton *aut, int32_t B, int32_t L, size_t *bytes) {
+    if (!aut || !bytes) { fa_set_error("fa_step_workspace_bytes: NULL argument"); return FA_ERR_INVALID_ARG; }
+    if (B < 0 || L < 0 || L > FA_MAX_LENGTH) { fa_set_error("fa_step_workspace_bytes: B or L out of range"); return FA_ERR_INVALID_ARG; }
+    *bytes = make_plan(aut, B, L).total;
+    return FA_OK;
+}
+
+extern "C" fa_status fa_transition_matrices(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                            const int32_t *committed, float *mant, int32_t *row_exp,
+                                            fa_stream stream) {
+    if (!aut) { fa_set_error("fa_transition_matrices: NULL automaton"); return FA_ERR_INVALID_ARG; }
+    if (B < 0 || L < 0 || B > 65535) { fa_set_error("fa_transition_matrices: B or L out of range"); return FA_ERR_INVALID_ARG; }
+    if ((long)B * L == 0) return FA_OK;
+    if (!probs || !committed || !mant || !row_exp) { fa_set_error("fa_transition_matrices: NULL buffer"); return FA_ERR_INVALID_ARG; }
+    fa_status st = check_device(aut, "fa_transition_matrices");
+    if (st != FA_OK) return st;
+    return launch_reweight(aut, B, L, probs, committed, mant, row_exp, nullptr, (cudaStream_t)stream);
+}
+
+extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                         const int32_t *committed, uint64_t philox_seed, uint64_t philox_offset,
+                                         int32_t k, int32_t commit_lo, int32_t commit_hi, void *workspace,
+                                         size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
+                                         int32_t *commit_idx, int32_t *row_status, fa_stream stream) {
+    if (!aut) { fa_set_error("fa_constrained_step: NULL automaton"); return FA_ERR_INVALID_ARG; }
+    if (B < 0 || B > 65535 || L < 0 || L > FA_MAX_LENGTH || k < 0) {
+        fa_set_error("fa_constrained_step: B, L or k out of range"); return FA_ERR_INVALID_ARG;
+    }
+    if (commit_lo < 0 || commit_hi < commit_lo || commit_hi > L) {
+        fa_set_error("fa_constrained_step: commit window must satisfy 0 <= lo <= hi <= L"); return FA_ERR_INVALID_ARG;
+    }
+    if (B == 0) return FA_OK;
+    if (!logZ || !row_status || (k > 0 && !commit_idx)) { fa_set_error("fa_constrained_step: NULL output"); return FA_ERR_INVALID_ARG; }
+    if (L > 0 && (!probs || !committed || !tokens || !marg)) { fa_set_error("fa_constrained_step: NULL buffer"); return FA_ERR_INVALID_ARG; }
+    fa_status st = check_device(aut, "fa_constrained_step");
+    if (st != FA_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (L == 0) {
+        k_empty_length<<<(B + 255) / 256, 256, 0, s>>>(aut->start, aut->accept_mask, B, k, logZ, row_status, commit_idx);
+        return launch_check("empty length");
+    }
+    const Plan p = make_plan(aut, B, L);
+    if (!workspace || ws_bytes < p.total) {
+        fa_set_error("fa_constrained_step: workspace needs " + std::to_string(p.total) + " bytes");
+        return FA_ERR_WORKSPACE_TOO_SMALL;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { fa_set_error("fa_constrained_step: workspace not 256-byte aligned"); return FA_ERR_INVALID_ARG; }
+    char *ws = (char *)workspace;
+    auto F = [&](size_t off) { return (float *)(ws + off); };
+    auto I = [&](size_t off) { return (int32_t *)(ws + off); };
+    const int S = aut->S;
+
+    // 1. emission reweighting -> level-0 spans
+    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), s);
+    if (st != FA_OK) return st;
+
+    // 2. up-sweep: level k from level k-1
+    for (int kk = 1; kk <= p.K; ++kk) {
+        dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
+        k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
+                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
+        if ((st = launch_check("rowshift")) != FA_OK) return st;
+        const long tiles = (S + GBN - 1) / GBN;
+        const long g2 = (long)B * p.nk[kk] * tiles * tiles;
+        k_gemm_simt<<<(unsigned)g2, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
+                                            p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]));
+        if ((st = launch_check("span product")) != FA_OK) return st;
+    }
+
+    // 3. root: logZ, end state, boundary messages
+    k_root<<<B, kThreads, 0, s>>>(dev_view(aut), L, p.K, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), philox_seed,
+                                  philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.zsum), I(p.zexp),
+                                  logZ, row_status);
+    if ((st = launch_check("root")) != FA_OK) return st;
+
+    // 4. top-down: midpoints and prefix/suffix messages, level K-1 .. 0
+    const size_t msg_smem = (size_t)S * 8;
+    for (int kk = p.K - 1; kk >= 0; --kk) {
+        const int np = p.nk[kk + 1];
+        const long warps = (long)B * np;
+        k_midpoint<<<(unsigned)((warps + kWarps - 1) / kWarps), kThreads, 0, s>>>(
+            S, B, L, kk, p.nk[kk], F(p.mant[kk]), I(p.rho[kk]), philox_seed, philox_offset, I(p.z), row_status);
+        if ((st = launch_check("midpoint")) != FA_OK) return st;
+        dim3 ga((S + kThreads - 1) / kThreads, np, B);
+        k_alpha<<<ga, kThreads, msg_smem, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk]), I(p.rho[kk]), F(p.am), I(p.ae));
+        if ((st = launch_check("alpha")) != FA_OK) return st;
+        dim3 gb((S + kWarps - 1) / kWarps, np, B);
+        k_beta<<<gb, kThreads, msg_smem, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk]), I(p.rho[kk]), F(p.bm), I(p.be));
+        if ((st = launch_check("beta")) != FA_OK) return st;
+    }
+
+    // 5. leaves: tokens and marginals
+    const long lw = (long)B * L;
+    k_leaf<<<(unsigned)((lw + kWarps - 1) / kWarps), kThreads, 0, s>>>(
+        dev_view(aut), B, L, probs, committed, philox_seed, philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be),
+        F(p.zsum), I(p.zexp), tokens, marg, row_status);
+    if ((st = launch_check("leaf")) != FA_OK) return st;
+
+    // 6. commit
+    k_topk<<<B, kThreads, 0, s>>>(L, k, commit_lo, commit_hi, marg, committed, row_status, commit_idx, tokens);
+    return launch_check("topk");
+}

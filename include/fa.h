@@ -1,0 +1,196 @@
+/*
+ * fa.h -- C ABI of the GB300 finite-automaton constrained denoising step.
+ *
+ * The method: "Constrained Decoding for Diffusion Language Models via
+ * Efficient Inference over Finite Automata" (arXiv 2607.07026), as summarised
+ * by the paperfeed.app page (sections "The insight: the constraint is a hidden
+ * Markov model" and "The scan trick: log-depth exact sampling") and the
+ * papernotes.org NeurIPS 2026 notes (method section, key designs 1-3).
+ *
+ * At one denoising step a diffusion LM gives a fully factorised distribution
+ * p(x | x^t) = prod_t p_t(x_t).  The constraint is an automaton
+ * M = (S, V, delta, s0, F) whose edges carry token label sets.  Viewing M as
+ * a hidden Markov model whose latent is the edge taken, the step samples
+ *     x ~ q(x) / Z,   q(x) = prod_t w_t(x_t) * N(x),
+ * where w_t = p_t for a masked position and the indicator of the committed
+ * token otherwise, and N(x) is the number of accepting paths labelled x (0/1
+ * for a DFA).  It returns logZ, the constrained marginal p(x_t = x^_t | x^t, C)
+ * of each sampled token, and the k masked positions with the highest such
+ * marginal (the "Mar" remasking rule of the notes' key design 3).
+ *
+ * Conventions
+ *  - Every pointer argument of fa_compile is HOST memory; every array argument
+ *    of the step calls is DEVICE memory owned by the caller.
+ *  - Calls that take a stream are asynchronous on it.  Their return value
+ *    reports only argument, launch and workspace errors; data-dependent
+ *    outcomes go to row_status on the device, with no host synchronisation.
+ *  - A compiled automaton is immutable and may be used by concurrent steps on
+ *    different streams, each with its own workspace.
+ *  - Results are a pure function of (inputs, philox_seed, philox_offset).
+ *  - On any error the call returns a non-zero fa_status and fa_last_error()
+ *    gives a message (thread-local).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fa_automaton fa_automaton; /* opaque, library-owned */
+typedef void *fa_stream;                  /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,
+    FA_ERR_CUDA = 2,
+    FA_ERR_OOM = 3,
+    FA_ERR_WORKSPACE_TOO_SMALL = 4,
+    FA_ERR_UNSUPPORTED = 5
+} fa_status;
+
+/* Per-sequence outcome written by the step into row_status[b]. */
+enum {
+    FA_ROW_OK = 0,
+    FA_ROW_EMPTY = 1,     /* Z == 0: no accepted string has positive weight */
+    FA_ROW_UNDERFLOW = 2, /* a categorical the sampler needed summed to 0 in fp32 range */
+    FA_ROW_TIMEOUT = 3    /* reserved for bounded inter-block waits */
+};
+
+/* Library limits. */
+#define FA_MAX_STATES 4096
+#define FA_MAX_LENGTH 65536
+
+/*
+ * fa_compile -- validate an automaton and upload it to the current device.
+ *
+ * The automaton as a hidden Markov model (paperfeed.app, "The insight": latent
+ * z_i = edge taken at step i, transition = the indicator that consecutive
+ * edges chain, emission = the indicator that x_i is in z_i's label set, start
+ * pinned to s0, final state accepting).
+ *
+ *   n_states            |S| in [1, FA_MAX_STATES]
+ *   start               s0 in [0, n_states)
+ *   accept[n_accept]    accepting states (repeats allowed; n_accept may be 0)
+ *   n_edges             E >= 0
+ *   edge_src/edge_dst   [E] state ids
+ *   label_offsets[E+1]  int64, label_offsets[0] = 0, non-decreasing; edge e reads
+ *                       label_tokens[label_offsets[e] .. label_offsets[e+1])
+ *   label_tokens        token ids in [0, vocab); a token repeated inside one set
+ *                       counts once; an empty set is rejected
+ *   vocab               |V| >= 1
+ *   stream              stream for the uploads
+ *   out                 receives the handle; release with fa_destroy
+ *
+ * Parallel edges s -> s' are kept: each is its own path (NFA path counting,
+ * paperfeed.app "Arbitrary schedules and NFAs").  Every edge consumes one
+ * token, so there are no epsilon edges.  The call synchronises the stream
+ * before returning (host staging buffers are freed).
+ * Errors: FA_ERR_INVALID_ARG (ids out of range, empty label set, bad offsets),
+ * FA_ERR_OOM, FA_ERR_CUDA.
+ */
+fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *accept, int32_t n_accept,
+                     int32_t n_edges, const int32_t *edge_src, const int32_t *edge_dst,
+                     const int64_t *label_offsets, const int32_t *label_tokens, int32_t vocab,
+                     fa_stream stream, fa_automaton **out);
+
+/* Free the device copy and the handle (NULL is accepted). */
+fa_status fa_destroy(fa_automaton *aut);
+
+/* Sizes of the compiled automaton: edges, token-edge incidences after
+ * de-duplication, whether no (state, token) pair has two edges, the number of
+ * distinct accepting states, |S| and |V|.  Any output pointer may be NULL. */
+fa_status fa_query(const fa_automaton *aut, int64_t *n_edges, int64_t *n_incidences, int32_t *is_dfa,
+                   int32_t *n_accept, int32_t *n_states, int32_t *vocab);
+
+/*
+ * fa_export_csr -- copy the canonical compiled arrays back to HOST buffers.
+ *
+ *   lab_off[E+1], lab_tok[I]     label sets, each sorted ascending, repeats removed
+ *   src_off[S+1], src_edges[E]   edge ids sorted by (src, dst, id)
+ *   dst_off[S+1], dst_edges[E]   edge ids sorted by (dst, src, id)
+ *   tok_off[V+1], tok_edges[I]   token -> edge incidence sorted by (token, src, dst, id)
+ *   accept[n_accept]             distinct accepting states, ascending
+ * Synchronous.  Errors: FA_ERR_INVALID_ARG (NULL buffer), FA_ERR_CUDA.
+ */
+fa_status fa_export_csr(const fa_automaton *aut, int64_t *lab_off, int32_t *lab_tok, int32_t *src_off,
+                        int32_t *src_edges, int32_t *dst_off, int32_t *dst_edges, int64_t *tok_off,
+                        int32_t *tok_edges, int32_t *accept);
+
+/* Bytes of device workspace fa_constrained_step needs for batch B and length L.
+ * Errors: FA_ERR_INVALID_ARG (B < 0, L < 0 or L > FA_MAX_LENGTH). */
+fa_status fa_step_workspace_bytes(const fa_automaton *aut, int32_t B, int32_t L, size_t *bytes);
+
+/*
+ * fa_transition_matrices -- the emission-reweighting stage alone.
+ *
+ * Key design 1 of the papernotes.org notes: the automaton's transitions stay
+ * fixed and every edge's emission is reweighted by the model's per-position
+ * probability, g(x_i = v | z_i = e) = 1[v in label(e)] * p_i(v), which folds
+ * into per-position state matrices
+ *     M_t(s, s') = sum_{e: s -> s'} sum_{v in label(e)} w_t(v).
+ * A committed position (committed[b,t] >= 0) has w_t = one-hot, so M_t counts
+ * the edges s -> s' that carry the committed token.
+ *
+ *   probs      [B, L, V] fp32, row-major, V contiguous; non-negative, finite
+ *   committed  [B, L] int32: a token id, or -1 = masked
+ *   mant       [B, L, S, S] fp32 out and row_exp [B, L, S] int32 out, with
+ *              M_t(s, s') = mant[b,t,s,s'] * 2^row_exp[b,t,s]
+ * A committed id outside [0, V) is treated as a token no edge carries.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_CUDA (launch).
+ */
+fa_status fa_transition_matrices(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                 const int32_t *committed, float *mant, int32_t *row_exp,
+                                 fa_stream stream);
+
+/*
+ * fa_constrained_step -- one constrained denoising step.
+ *
+ * Exact sampling from the constrained mean-field posterior by the log-depth
+ * tree of the paperfeed.app page ("The scan trick") and key design 2 of the
+ * notes: span matrices A[l, r) = M_{l+1} ... M_r are built bottom-up over
+ * 2^k steps by batched products, the end state is drawn from the root
+ * (z_0 = s0, z_L ~ A_root[s0, .] restricted to F), every midpoint
+ * z_m ~ A[l, m)[z_l, .] * A[m, r)[., z_r] top-down level by level, and finally
+ * every token is drawn from the label sets of the edges z_{t-1} -> z_t in
+ * proportion to w_t.  The constrained marginals of the sampled tokens come from
+ * prefix/suffix messages over the same tree (key design 3), and the commit set
+ * is the top k of those marginals among masked positions of [commit_lo,
+ * commit_hi), descending, ties to the lower position, padded with -1.
+ *
+ *   B, L            batch and length (B >= 0, 0 <= L <= FA_MAX_LENGTH)
+ *   probs           [B, L, V] fp32 device, read only
+ *   committed       [B, L] int32 device: token id, or -1 = masked
+ *   philox_seed,
+ *   philox_offset   Philox4x32-10 key and counter offset (Salmon et al., SC'11);
+ *                   advance the offset between steps
+ *   k               commit count >= 0
+ *   commit_lo/hi    commit window, 0 <= lo <= hi <= L
+ *   workspace       device scratch of at least fa_step_workspace_bytes(B, L)
+ *                   bytes, 256-byte aligned, caller-owned; contents are
+ *                   overwritten; concurrent steps need separate workspaces
+ *   tokens          [B, L] int32 out: sampled x^ (committed positions echoed)
+ *   logZ            [B] double out: ln Z (-inf when FA_ROW_EMPTY)
+ *   marg            [B, L] fp32 out: constrained marginal of x^_t (1 for committed)
+ *   commit_idx      [B, k] int32 out
+ *   row_status      [B] int32 out: FA_ROW_*
+ * When row_status[b] != FA_ROW_OK, tokens[b] echo committed (-1 where masked),
+ * marg[b] is 0 where masked and commit_idx[b] is all -1.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_WORKSPACE_TOO_SMALL, FA_ERR_CUDA (launch).
+ */
+fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                              const int32_t *committed, uint64_t philox_seed, uint64_t philox_offset,
+                              int32_t k, int32_t commit_lo, int32_t commit_hi, void *workspace,
+                              size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
+                              int32_t *commit_idx, int32_t *row_status, fa_stream stream);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *fa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_H_ */
