@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the finite-automaton constrained denoising step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--workload NAME]
+
+One step = one fa_constrained_step call over one batch: emission reweighting, the span
+up-sweep, root and top-down sampling with prefix/suffix messages, leaf tokens with
+constrained marginals, and the top-k commit.  The default workload is the random DFA with
+64 states, vocabulary 32000, L=128, B=1, half the positions committed (synthetic, seeded).
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier and a device
+synchronisation on both sides; each step is one CUDA-graph replay of the step, bracketed
+by CUDA events on its stream, with a 256 MiB L2 flush between steps outside the events.
+Stage boundaries are recorded inside the graph (fa_profile_enable), which gives the
+per-stage device time used for the roofline of the dominant stage.  N > 1 runs
+independent replicas (one per GPU, weak scaling); rank 0 prints one JSON line.
+
+--impl reference times the float64 CPU oracle on the host cores on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ms per constrained denoising step and positions/s at 1 GB300; % of roofline"
+UNIT = "positions/s"
+DEFAULT_WORKLOAD = "random_dfa_S64_L128"
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-graph", action="store_true", help="launch the step eagerly instead of a graph replay")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- roofline model
+
+def algorithmic(w, masked: int):
+    """Algorithmic bytes and FLOPs per step of each stage (the per-unit figures of the design
+    notes times the units one step processes)."""
+    B, L, S, V = w.B, w.L, w.S, w.V
+    K = max(0, math.ceil(math.log2(L))) if L > 1 else 0
+    nk = [(L + (1 << k) - 1) >> k for k in range(K + 1)]
+    span = 4 * S * S + 8 * S                      # mantissas + row exponent + row max
+    reweight = 4 * masked * V + B * L * span       # probs rows read once, leaf spans written
+    products = sum(B * (nk[k - 1] // 2) for k in range(1, K + 1))   # real products (not copies)
+    upsweep_bytes = sum(B * (nk[k - 1] + nk[k]) * span for k in range(1, K + 1))
+    upsweep_flops = products * 2 * S ** 3
+    topdown = sum(B * nk[k] * span for k in range(0, K))          # every non-root span read once
+    return {"reweight": {"bytes": reweight, "flops": 2 * masked * w.fa.n_incidences},
+            "upsweep": {"bytes": upsweep_bytes, "flops": upsweep_flops},
+            "topdown": {"bytes": topdown, "flops": 2 * B * S * S * sum(nk[:K])},
+            "leaf": {"bytes": 4 * B * L * 4, "flops": 0},
+            "commit": {"bytes": 8 * B * L, "flops": 0}}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.join(ROOT, "constrained_decoding_diffusion_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "constrained_decoding_diffusion_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(stage: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel sources (profiles/traffic_<stage>_<workload>.txt: 'source_sha <h>' and
+    'dram_bytes_per_launch <n>' lines)."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s_%s.txt" % (stage, workload))
+    try:
+        kv = {}
+        for line in open(path):
+            parts = line.split()
+            if len(parts) >= 2 and not line.startswith("#"):
+                kv[parts[0]] = parts[1]
+        if kv.get("source_sha") != source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU baseline
+
+def cpu_baseline(w, probs, seconds: float):
+    """The float64 oracle as it stands, single-threaded on a host core: sample, posterior
+    (logZ and marginals of the sample) and commit, repeated for about `seconds`."""
+    import oracle
+    o = oracle.OracleFA(w.fa)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for b in range(w.B):
+            x = o.sample(probs[b], w.committed[b], 1, seed=reps)[0]
+            r = o.posterior(probs[b], w.committed[b], tokens=x)
+            oracle.topk(r["marg_tokens"], w.committed[b], w.k, 0, w.window)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": reps * w.B * w.L / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d full steps of %s (B=%d, L=%d) in %.1f s, one thread" % (reps, w.name, w.B, w.L, el),
+            "ms_per_step": 1e3 * el / reps}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from constrained_decoding_diffusion_gb300 import synth
+    w = synth.workload(args.workload)
+    probs = w.probs()
+    import oracle
+    o = oracle.OracleFA(w.fa)
+
+    def one(seed):
+        for b in range(w.B):
+            x = o.sample(probs[b], w.committed[b], 1, seed=seed)[0]
+            r = o.posterior(probs[b], w.committed[b], tokens=x)
+            oracle.topk(r["marg_tokens"], w.committed[b], w.k, 0, w.window)
+
+    for i in range(min(args.warmup, 1)):
+        one(i)
+    t = time.perf_counter()
+    one(0)
+    est = time.perf_counter() - t
+    budget = 120.0
+    steps = max(1, min(args.steps, int(budget / max(est, 1e-6))))
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    el = time.perf_counter() - t0
+    ms = 1e3 * el / steps
+    value = w.B * w.L / (el / steps)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": steps,
+            "steps_requested": args.steps, "warmup": min(args.warmup, 1), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "V": w.V, "k": w.k},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "%d full steps, one thread (step count capped to a %.0f s budget)"
+                                       % (steps, budget)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- native arm
+
+def run_native(args, rank, world, local):
+    import torch
+    from constrained_decoding_diffusion_gb300 import native, synth
+
+    torch.cuda.set_device(local)
+    native.load()
+    w = synth.workload(args.workload)
+    probs_np = w.probs()
+    masked = int((w.committed < 0).sum())
+    aut = native.fa_compile(w.fa)
+    probs = torch.from_numpy(probs_np).cuda()
+    committed = torch.from_numpy(w.committed).cuda()
+    step = native.ConstrainedStep(aut, w.B, w.L, w.k)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    seed = 1234 + rank
+
+    def call(offset):
+        step(probs, committed, seed, offset, 0, w.window)
+
+    # launches per step (counted by the library)
+    with torch.cuda.stream(stream):
+        n0 = native.fa_launch_count()
+        call(0)
+        launches_per_step = native.fa_launch_count() - n0
+        for i in range(max(args.warmup, 3)):
+            call(i)
+    stream.synchronize()
+
+    native.fa_profile_enable(True)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call(0)
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                graph.replay()
+        stream.synchronize()
+
+    def run_one(i):
+        if graph is not None:
+            graph.replay()
+        else:
+            call(i)
+
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_ms = {k: 0.0 for k in native.STAGES}
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.zero_()
+                ev_s[i].record(stream)
+                run_one(i)
+                ev_e[i].record(stream)
+                st = native.fa_profile_read()
+                for key in stage_ms:
+                    stage_ms[key] += st[key]
+        torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    native.fa_profile_enable(False)
+    step_ms = [s.elapsed_time(e) for s, e in zip(ev_s, ev_e)]
+    ms = float(np.mean(step_ms))
+    ms_max = allreduce_max(ms, world)
+    status = step.row_status.cpu().numpy()
+
+    # end to end through the public call with host buffers: H2D of the step's inputs from
+    # pinned memory, the step, D2H of every output, all inside the events
+    h_probs = torch.from_numpy(probs_np).pin_memory()
+    h_com = torch.from_numpy(w.committed).pin_memory()
+    outs = [step.tokens, step.logZ, step.marg, step.commit_idx, step.row_status]
+    h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    e2e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    e2e_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            flush.zero_()
+            e2e_s[i].record(stream)
+            probs.copy_(h_probs, non_blocking=True)
+            committed.copy_(h_com, non_blocking=True)
+            run_one(i)
+            for h, d in zip(h_outs, outs):
+                h.copy_(d, non_blocking=True)
+            e2e_e[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(e2e_s, e2e_e)]))
+    e2e_ms = allreduce_max(e2e_ms, world)
+    h2d = probs.numel() * 4 + committed.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    if rank != 0:
+        return
+    positions = w.B * w.L * world
+    value = positions / (ms_max / 1e3)
+    alg = algorithmic(w, masked)
+    hbm, tc, src = peaks()
+    per_stage = {k: stage_ms[k] / args.steps for k in stage_ms}
+    dom = max(per_stage, key=per_stage.get)
+    dom_ms = per_stage[dom]
+    a = alg[dom]
+    achieved = a["bytes"] / (dom_ms / 1e3) / 1e9
+    roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": recorded_traffic(dom, w.name),
+            "algorithmic_bytes": a["bytes"], "ms": dom_ms, "peak_source": src + " (burst copy)"}
+    # the whole step against its own roofline (slower of bytes at HBM peak, span FLOPs at
+    # the bf16 tensor peak)
+    tot_bytes = sum(v["bytes"] for v in alg.values())
+    t_roof = max(tot_bytes / (hbm * 1e9), alg["upsweep"]["flops"] / (tc * 1e12))
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "V": w.V, "masked": masked,
+                       "k": w.k, "l2": "flushed between steps (256 MiB write)",
+                       "launch": "cuda_graph" if graph is not None else "eager",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "roofline": roof,
+            "step_roofline": {"ms_at_roofline": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_max,
+                              "bytes": tot_bytes, "span_flops": alg["upsweep"]["flops"]},
+            "stage_ms": per_stage,
+            "e2e": {"value": positions / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
+            "wall_s": wall, "row_status_ok": bool((status == 0).all()),
+            "clocks": clocks.summary()}
+    if world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, probs_np, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_native(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -11,6 +11,7 @@
 // span differ by far more than 2^254 once committed tokens pin the path, so a single
 // exponent per matrix would flush whole rows; per-row exponents keep every row at full
 // relative precision.  Only entries more than ~2^-126 below their own row's maximum are lost.
+#include <atomic>
 #include <cfloat>
 #include <cmath>
 #include <string>
@@ -602,13 +603,33 @@ __global__ void k_empty_length(int start, const int32_t *accept_mask, int B, int
 
 // ----------------------------------------------------------------------------- host glue
 
+std::atomic<unsigned long long> g_launches{0};
+
 fa_status launch_check(const char *what) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         fa_set_error(std::string(what) + ": " + cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
     return FA_OK;
+}
+
+// Stage-boundary timing events (per host thread): when enabled, every step records
+// FA_N_STAGES + 1 events on its stream, as graph nodes if the stream is being captured.
+struct StageEvents {
+    bool enabled = false;
+    bool created = false;
+    cudaEvent_t ev[FA_N_STAGES + 1];
+};
+thread_local StageEvents g_stage;
+
+void stage_mark(int i, cudaStream_t s) {
+    if (!g_stage.enabled) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(g_stage.ev[i], s, cudaEventRecordExternal);
+    else cudaEventRecord(g_stage.ev[i], s);
 }
 
 int pick_row_blocks(const fa_automaton *a, long positions) {
@@ -693,10 +714,12 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
     const int S = aut->S;
 
     // 1. emission reweighting -> level-0 spans
+    stage_mark(0, s);
     st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), s);
     if (st != FA_OK) return st;
 
     // 2. up-sweep: level k from level k-1
+    stage_mark(1, s);
     for (int kk = 1; kk <= p.K; ++kk) {
         dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
         k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
@@ -710,6 +733,7 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
     }
 
     // 3. root: logZ, end state, boundary messages
+    stage_mark(2, s);
     k_root<<<B, kThreads, 0, s>>>(dev_view(aut), L, p.K, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), philox_seed,
                                   philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.zsum), I(p.zexp),
                                   logZ, row_status);
@@ -732,6 +756,7 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
     }
 
     // 5. leaves: tokens and marginals
+    stage_mark(3, s);
     const long lw = (long)B * L;
     k_leaf<<<(unsigned)((lw + kWarps - 1) / kWarps), kThreads, 0, s>>>(
         dev_view(aut), B, L, probs, committed, philox_seed, philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be),
@@ -739,6 +764,39 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
     if ((st = launch_check("leaf")) != FA_OK) return st;
 
     // 6. commit
+    stage_mark(4, s);
     k_topk<<<B, kThreads, 0, s>>>(L, k, commit_lo, commit_hi, marg, committed, row_status, commit_idx, tokens);
-    return launch_check("topk");
+    st = launch_check("topk");
+    stage_mark(5, s);
+    return st;
+}
+
+extern "C" fa_status fa_profile_enable(int32_t enable) {
+    if (enable && !g_stage.created) {
+        for (int i = 0; i <= FA_N_STAGES; ++i) {
+            cudaError_t e = cudaEventCreate(&g_stage.ev[i]);
+            if (e != cudaSuccess) { fa_set_error(std::string("fa_profile_enable: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+        }
+        g_stage.created = true;
+    }
+    g_stage.enabled = enable != 0;
+    return FA_OK;
+}
+
+extern "C" fa_status fa_profile_read(float *ms) {
+    if (!ms) { fa_set_error("fa_profile_read: NULL argument"); return FA_ERR_INVALID_ARG; }
+    if (!g_stage.created) { fa_set_error("fa_profile_read: profiling never enabled"); return FA_ERR_INVALID_ARG; }
+    cudaError_t e = cudaEventSynchronize(g_stage.ev[FA_N_STAGES]);
+    if (e != cudaSuccess) { fa_set_error(std::string("fa_profile_read: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    for (int i = 0; i < FA_N_STAGES; ++i) {
+        e = cudaEventElapsedTime(&ms[i], g_stage.ev[i], g_stage.ev[i + 1]);
+        if (e != cudaSuccess) { fa_set_error(std::string("fa_profile_read: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    }
+    return FA_OK;
+}
+
+extern "C" fa_status fa_launch_count(uint64_t *n) {
+    if (!n) { fa_set_error("fa_launch_count: NULL argument"); return FA_ERR_INVALID_ARG; }
+    *n = g_launches.load(std::memory_order_relaxed);
+    return FA_OK;
 }

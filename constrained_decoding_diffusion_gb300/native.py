@@ -26,7 +26,10 @@ FA_ROW_OK, FA_ROW_EMPTY, FA_ROW_UNDERFLOW, FA_ROW_TIMEOUT = 0, 1, 2, 3
 
 # every entry point include/fa.h declares
 EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_workspace_bytes",
-           "fa_transition_matrices", "fa_constrained_step", "fa_last_error")
+           "fa_transition_matrices", "fa_constrained_step", "fa_profile_enable", "fa_profile_read",
+           "fa_launch_count", "fa_last_error")
+N_STAGES = 5
+STAGES = ("reweight", "upsweep", "topdown", "leaf", "commit")
 
 _lib = None
 
@@ -62,6 +65,12 @@ def load(path: str = LIB_PATH):
     lib.fa_transition_matrices.restype = st
     lib.fa_constrained_step.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, sz, P, P, P, P, P, P]
     lib.fa_constrained_step.restype = st
+    lib.fa_profile_enable.argtypes = [i32]
+    lib.fa_profile_enable.restype = st
+    lib.fa_profile_read.argtypes = [P]
+    lib.fa_profile_read.restype = st
+    lib.fa_launch_count.argtypes = [P]
+    lib.fa_launch_count.restype = st
     lib.fa_last_error.argtypes = []
     lib.fa_last_error.restype = ctypes.c_char_p
     _lib = lib
@@ -202,3 +211,22 @@ class ConstrainedStep:
                             self.workspace, self.tokens, self.logZ, self.marg, self.commit_idx, self.row_status,
                             stream)
         return self.tokens, self.logZ, self.marg, self.commit_idx, self.row_status
+
+
+def fa_profile_enable(enable: bool):
+    load()
+    _check(_lib.fa_profile_enable(1 if enable else 0))
+
+
+def fa_profile_read() -> dict:
+    """Stage durations (ms) of the most recent step recorded with profiling enabled."""
+    ms = np.zeros(N_STAGES, np.float32)
+    _check(_lib.fa_profile_read(_np_ptr(ms)))
+    return dict(zip(STAGES, (float(x) for x in ms)))
+
+
+def fa_launch_count() -> int:
+    load()
+    n = np.zeros(1, np.uint64)
+    _check(_lib.fa_launch_count(_np_ptr(n)))
+    return int(n[0])
