@@ -26,7 +26,8 @@ FA_ROW_OK, FA_ROW_EMPTY, FA_ROW_UNDERFLOW, FA_ROW_TIMEOUT = 0, 1, 2, 3
 
 # every entry point include/fa.h declares
 EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_workspace_bytes",
-           "fa_transition_matrices", "fa_constrained_step", "fa_profile_enable", "fa_profile_read",
+           "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_noalloc",
+           "fa_profile_enable", "fa_profile_read",
            "fa_launch_count", "fa_last_error")
 N_STAGES = 5
 STAGES = ("reweight", "upsweep", "topdown", "leaf", "commit")
@@ -65,6 +66,8 @@ def load(path: str = LIB_PATH):
     lib.fa_transition_matrices.restype = st
     lib.fa_constrained_step.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, sz, P, P, P, P, P, P]
     lib.fa_constrained_step.restype = st
+    lib.fa_constrained_step_noalloc.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, P, P, P, P, P]
+    lib.fa_constrained_step_noalloc.restype = st
     lib.fa_profile_enable.argtypes = [i32]
     lib.fa_profile_enable.restype = st
     lib.fa_profile_read.argtypes = [P]
@@ -230,3 +233,24 @@ def fa_launch_count() -> int:
     n = np.zeros(1, np.uint64)
     _check(_lib.fa_launch_count(_np_ptr(n)))
     return int(n[0])
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def fa_constrained_step_noalloc(aut: CompiledAutomaton, probs, committed, philox_seed: int, philox_offset: int,
+                                k: int, commit_lo: int, commit_hi: int, tokens, logZ, marg, commit_idx, row_status,
+                                stream=None):
+    """fa_constrained_step without a workspace argument: for callers that cannot allocate
+    device memory.  The library's built-in scratch array (NOALLOC_SCRATCH_BYTES per device)
+    is used instead; calls that overlap on the GPU must be serialised by the caller."""
+    import torch
+    B, L, V = probs.shape
+    _check(_lib.fa_constrained_step_noalloc(
+        aut.handle, B, L, _dev(probs, torch.float32, "probs", (B, L, aut.vocab)),
+        _dev(committed, torch.int32, "committed", (B, L)), ctypes.c_uint64(philox_seed & (2 ** 64 - 1)),
+        ctypes.c_uint64(philox_offset & (2 ** 64 - 1)), int(k), int(commit_lo), int(commit_hi),
+        _dev(tokens, torch.int32, "tokens", (B, L)), _dev(logZ, torch.float64, "logZ", (B,)),
+        _dev(marg, torch.float32, "marg", (B, L)),
+        _dev(commit_idx, torch.int32, "commit_idx", (B, k)) if k > 0 else None,
+        _dev(row_status, torch.int32, "row_status", (B,)), _stream_ptr(stream)))

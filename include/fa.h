@@ -188,6 +188,32 @@ fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int32_t L, con
                               int32_t *commit_idx, int32_t *row_status, fa_stream stream);
 
 /*
+ * fa_constrained_step_noalloc -- fa_constrained_step for callers that cannot allocate.
+ *
+ * No counterpart in the paper: this is a deployment convenience.  Some callers may not
+ * allocate device memory where they decode (an engine whose pool owns all device memory,
+ * a plugin or real-time loop where cudaMalloc would synchronise the device, code that only
+ * receives pointers).  They pass inputs and outputs exactly as for fa_constrained_step,
+ * but no workspace: the scratch is a fixed FA_NOALLOC_SCRATCH_BYTES array built into the
+ * library, which every GPU that loads the library holds until the process exits.  The call
+ * itself allocates nothing.
+ *
+ * The first call on a device (with that device current) looks up the array's device
+ * address; make it before any stream capture.  All calls on a device share the array and
+ * it keeps the last call's contents (the step initialises what it reads, so no clearing is
+ * needed); calls whose GPU work overlaps race on it and must be serialised by the caller.
+ * Errors: as fa_constrained_step, plus FA_ERR_WORKSPACE_TOO_SMALL when
+ * fa_step_workspace_bytes(B, L) exceeds FA_NOALLOC_SCRATCH_BYTES, FA_ERR_CUDA if the
+ * array's address cannot be obtained.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
+fa_status fa_constrained_step_noalloc(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                      const int32_t *committed, uint64_t philox_seed, uint64_t philox_offset,
+                                      int32_t k, int32_t commit_lo, int32_t commit_hi, int32_t *tokens,
+                                      double *logZ, float *marg, int32_t *commit_idx, int32_t *row_status,
+                                      fa_stream stream);
+
+/*
  * Stage timing and launch accounting (measurement support; no counterpart on the pages).
  *
  * fa_profile_enable(1) makes later fa_constrained_step calls on this host thread record
