@@ -161,8 +161,7 @@ def algorithmic(w, masked: int):
     return {"reweight": {"bytes": reweight, "flops": 2 * masked * w.fa.n_incidences},
             "upsweep": {"bytes": upsweep_bytes, "flops": upsweep_flops},
             "topdown": {"bytes": topdown, "flops": 2 * B * S * S * sum(nk[:K])},
-            "leaf": {"bytes": 4 * B * L * 4, "flops": 0},
-            "commit": {"bytes": 8 * B * L, "flops": 0}}
+            "leaf_commit": {"bytes": 4 * B * L * 4 + 8 * B * L, "flops": 0}}
 
 
 def peaks():

@@ -6,6 +6,7 @@
 // (section "The insight: the constraint is a hidden Markov model"): latent = the edge taken,
 // transition = the edges chain, emission = the token lies in the edge's label set.
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <numeric>
 #include <string>
@@ -155,23 +156,136 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     a->n_cells = (int32_t)cell_dst.size();
     a->max_cell_len = max_cell_len;
 
-    // row blocks with balanced cost, for nrb = 1, 2, 4, ... <= S
-    std::vector<int64_t> pref(S + 1, 0);
-    for (int s = 0; s < S; ++s) pref[s + 1] = pref[s] + row_cost[s] + 1;
-    std::vector<int32_t> rb;
-    int levels = 0;
-    for (int nrb = 1; nrb <= S && nrb <= 4096; nrb *= 2, ++levels) {
-        int r = 0;
+    // Reweight layout (sliced, ELL-like).  The vocabulary is read in chunks of CH tokens
+    // staged in shared memory.  Every cell's tokens in a chunk are cut into pieces of at most
+    // FA_PIECE_TOKENS; piece ids are cell-major (cell c owns pieces [pc[c], pc[c+1])).  For
+    // each (chunk, row) the row's pieces, longest first, form slices of 32: lane l of a slice
+    // sums piece l, reading 16-byte groups of 8 in-chunk token indices stored interleaved
+    // (group k of lane l at slice_start + 32 k + l, padded with the index CH, a zero slot).
+    const int CH = (V <= FA_REWEIGHT_MAX_CHUNK) ? V : FA_REWEIGHT_MAX_CHUNK;
+    const int nch = (V + CH - 1) / CH;
+    a->chunk_tokens = CH;
+    a->n_chunks = nch;
+    struct Piece { int32_t cell, chunk; int64_t first; int32_t len; };
+    std::vector<Piece> pieces;
+    std::vector<int32_t> pc(a->n_cells + 1, 0);
+    for (int c = 0; c < a->n_cells; ++c) {
+        pc[c] = (int32_t)pieces.size();
+        const int32_t *b0 = cell_tok.data() + cell_off[c], *b1 = cell_tok.data() + cell_off[c + 1];
+        for (int ch = 0; ch < nch; ++ch) {
+            const int32_t lo = ch * CH, hi = (int32_t)std::min<int64_t>((int64_t)(ch + 1) * CH, V);
+            const int32_t *q0 = std::lower_bound(b0, b1, lo), *q1 = std::lower_bound(b0, b1, hi);
+            for (const int32_t *q = q0; q < q1; q += FA_PIECE_TOKENS)
+                pieces.push_back({c, ch, (int64_t)(q - cell_tok.data()), (int32_t)std::min<int64_t>(FA_PIECE_TOKENS, q1 - q)});
+        }
+    }
+    pc[a->n_cells] = (int32_t)pieces.size();
+    std::vector<int32_t> row_pieces(S, 0);
+    for (auto &pz : pieces) row_pieces[cell_src[pz.cell]]++;
+    {
+        // dynamic shared memory of the reweight: staged chunk, per-piece sums, per-row maxima
+        const long budget = 232448L - 256 - 4L * (CH + 4) - 4L * S;
+        a->max_unit_pieces = (int32_t)std::min<long>(1 << 20, budget / 4);
+        int32_t mx = 0;
+        for (int r = 0; r < S; ++r) mx = std::max(mx, row_pieces[r]);
+        if (mx > a->max_unit_pieces) { delete a; fa_set_error("fa_compile: a state has too many token pieces for one block"); return FA_ERR_UNSUPPORTED; }
+    }
+    std::vector<int32_t> sl_row_off((size_t)nch * (S + 1)), sl_goff(1, 0), sl_piece;
+    std::vector<uint16_t> tok8;
+    {
+        std::vector<std::vector<int32_t>> by_row(S);
+        for (int ch = 0; ch < nch; ++ch) {
+            for (auto &v : by_row) v.clear();
+            for (int32_t pid = 0; pid < (int32_t)pieces.size(); ++pid)
+                if (pieces[pid].chunk == ch) by_row[cell_src[pieces[pid].cell]].push_back(pid);
+            for (int r = 0; r < S; ++r) {
+                sl_row_off[(size_t)ch * (S + 1) + r] = (int32_t)(sl_goff.size() - 1);
+                auto &v = by_row[r];
+                std::stable_sort(v.begin(), v.end(), [&](int32_t x, int32_t y) { return pieces[x].len > pieces[y].len; });
+                for (size_t s0 = 0; s0 < v.size(); s0 += 32) {
+                    const size_t n = std::min<size_t>(32, v.size() - s0);
+                    int32_t len = 0;
+                    for (size_t l = 0; l < n; ++l) len = std::max(len, (pieces[v[s0 + l]].len + 7) / 8);
+                    const size_t g0 = tok8.size() / 8;
+                    tok8.resize(tok8.size() + (size_t)len * 32 * 8, (uint16_t)CH);
+                    for (size_t l = 0; l < 32; ++l) {
+                        sl_piece.push_back(l < n ? v[s0 + l] : -1);
+                        if (l >= n) continue;
+                        const Piece &pz = pieces[v[s0 + l]];
+                        for (int32_t j = 0; j < pz.len; ++j)
+                            tok8[(g0 + (size_t)(j / 8) * 32 + l) * 8 + (j % 8)] =
+                                (uint16_t)(cell_tok[pz.first + j] - (int32_t)ch * CH);
+                    }
+                    // spread the 32 lanes' gathers of each group position over distinct banks:
+                    // permute the 8 entries of every group (their sum is order-free)
+                    for (int32_t k = 0; k < len; ++k) {
+                        uint16_t rem[32][8];
+                        int nrem[32];
+                        for (int l = 0; l < 32; ++l) {
+                            nrem[l] = 8;
+                            for (int h = 0; h < 8; ++h) rem[l][h] = tok8[(g0 + (size_t)k * 32 + l) * 8 + h];
+                        }
+                        for (int h = 0; h < 8; ++h) {
+                            int used[33] = {0};
+                            for (int l = 0; l < 32; ++l) {
+                                int best = 0, bc = 1 << 30;
+                                for (int x = 0; x < nrem[l]; ++x) {
+                                    const int cost = (rem[l][x] == (uint16_t)CH) ? used[32] : used[rem[l][x] & 31];
+                                    if (cost < bc) { bc = cost; best = x; }
+                                }
+                                const uint16_t tk = rem[l][best];
+                                rem[l][best] = rem[l][--nrem[l]];
+                                used[tk == (uint16_t)CH ? 32 : (tk & 31)]++;
+                                tok8[(g0 + (size_t)k * 32 + l) * 8 + h] = tk;
+                            }
+                        }
+                    }
+                    sl_goff.push_back((int32_t)(tok8.size() / 8));
+                }
+            }
+            sl_row_off[(size_t)ch * (S + 1) + S] = (int32_t)(sl_goff.size() - 1);
+        }
+        if (tok8.size() / 8 > (size_t)INT32_MAX) { delete a; fa_set_error("fa_compile: automaton too large"); return FA_ERR_INVALID_ARG; }
+        tok8.resize(tok8.size() + 64, (uint16_t)CH);
+    }
+    a->n_slices = (int32_t)(sl_goff.size() - 1);
+
+    // row blocks of balanced gather cost with at most max_unit_pieces pieces each, for target
+    // block counts 1, 2, 4, ...
+    int64_t total_cost = 0;
+    for (int r = 0; r < S; ++r) total_cost += row_cost[r] + 1;
+    std::vector<int32_t> rb, rbm;  // rbm: per block {r0, r1, first cell, end cell, first piece, pad}
+    for (int target = 1; ; target *= 2) {
+        const int64_t cap = std::max<int64_t>(1, (total_cost + target - 1) / target);
+        a->part_first.push_back((int32_t)rb.size());
         rb.push_back(0);
-        for (int i = 1; i < nrb; ++i) {
-            int64_t target = (pref[S] * i) / nrb;
-            while (r < S && pref[r] < target) ++r;
-            rb.push_back(r);
+        int64_t cost = 0;
+        int32_t np = 0;
+        for (int r = 0; r < S; ++r) {
+            const int64_t rc = row_cost[r] + 1;
+            if (r > rb.back() && (cost + rc > cap || np + row_pieces[r] > a->max_unit_pieces)) {
+                rb.push_back(r);
+                cost = 0;
+                np = 0;
+            }
+            cost += rc;
+            np += row_pieces[r];
         }
         rb.push_back(S);
+        a->part_count.push_back((int32_t)(rb.size() - a->part_first.back() - 1));
+        int32_t mp = 0, mr = 0;
+        for (size_t q = a->part_first.back(); q + 1 < rb.size(); ++q) {
+            mp = std::max(mp, pc[row_cell_off[rb[q + 1]]] - pc[row_cell_off[rb[q]]]);
+            mr = std::max(mr, rb[q + 1] - rb[q]);
+        }
+        a->part_max_pieces.push_back(mp);
+        a->part_max_rows.push_back(mr);
+        for (size_t q = a->part_first.back(); q + 1 < rb.size(); ++q) {
+            const int32_t c0 = row_cell_off[rb[q]], c1 = row_cell_off[rb[q + 1]];
+            rbm.insert(rbm.end(), {rb[q], rb[q + 1], c0, c1, pc[c0], 0, 0, 0});
+        }
+        if (a->part_count.back() >= S || target >= 4096) break;
     }
-    a->n_rb_levels = levels;
-    a->h_rb_bounds = rb;
 
     std::vector<int32_t> esrc(edge_src, edge_src + E), edst(edge_dst, edge_dst + E);
 
@@ -194,6 +308,12 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     bb.add(&a->cell_off, cell_off);
     bb.add(&a->cell_tok, cell_tok);
     bb.add(&a->rb_bounds, rb);
+    bb.add(&a->rb_meta, rbm);
+    bb.add(&a->tok8, tok8);
+    bb.add(&a->piece_cell_off, pc);
+    bb.add(&a->sl_row_off, sl_row_off);
+    bb.add(&a->sl_goff, sl_goff);
+    bb.add(&a->sl_piece, sl_piece);
 
     cudaError_t err = cudaMalloc(&a->blob, bb.total);
     if (err != cudaSuccess) { delete a; return cuda_fail("fa_compile: cudaMalloc", err); }

@@ -36,11 +36,23 @@ struct fa_automaton {
     int32_t *cell_src = nullptr;      // [n_cells]
     int64_t *cell_off = nullptr;      // [n_cells+1]
     int32_t *cell_tok = nullptr;      // [I]
-    // row blocks for the reweight grid: for nrb = 2^p (p = 0..n_rb_levels-1), the bounds of
-    // nrb contiguous row ranges with balanced token counts, at rb_bounds + (2^p - 1) + p.
+    // reweight layout (sliced, ELL-like; built in fa_compile): chunk_tokens-token vocabulary
+    // chunks; piece ids are cell-major, cell x owning pieces [piece_cell_off[x],
+    // piece_cell_off[x+1]); slices of (chunk c, row r) are sl_row_off[c*(S+1)+r] ..
+    // sl_row_off[c*(S+1)+r+1]; slice q has its 16-byte groups at tok8 + 8*sl_goff[q] ..
+    // 8*sl_goff[q+1], lane l reading groups sl_goff[q] + 32 k + l, and sums piece
+    // sl_piece[32 q + l] (-1 = none).
+    int32_t chunk_tokens = 0, n_chunks = 1, max_unit_pieces = 0, n_slices = 0;
+    uint16_t *tok8 = nullptr;
+    int32_t *piece_cell_off = nullptr, *sl_row_off = nullptr, *sl_goff = nullptr, *sl_piece = nullptr;
+    // row blocks for the reweight grid: partition p (p = 0..n_parts-1) splits the rows into
+    // part_count[p] contiguous blocks of balanced gather cost, each with at most
+    // max_unit_pieces pieces; its bounds are rb_bounds[part_first[p] .. + part_count[p]].
     int32_t *rb_bounds = nullptr;
-    int32_t n_rb_levels = 0;
-    std::vector<int32_t> h_rb_bounds;
+    // per row block of every partition (same order, part_first[p] - p + i for block i of
+    // partition p): {r0, r1, first cell, end cell, first piece, 0, 0, 0}
+    int32_t *rb_meta = nullptr;
+    std::vector<int32_t> part_first, part_count, part_max_pieces, part_max_rows;
     void *blob = nullptr;  // one device allocation holding every array above
     size_t blob_bytes = 0;
 };
@@ -50,6 +62,8 @@ void fa_set_error(const std::string &msg);
 // ----------------------------------------------------------------------------- device side
 
 #define FA_INT_NONE (-2147483647 - 1)
+#define FA_REWEIGHT_MAX_CHUNK 32767  // in-chunk indices and the pad index fit in 16 bits
+#define FA_PIECE_TOKENS 64          // tokens one lane sums per slice
 
 // floor(log2 x) of a positive normal float from its exponent field (subnormals give -127).
 __device__ __forceinline__ int fa_exponent(float x) {
@@ -61,6 +75,19 @@ __device__ __forceinline__ float fa_scale_pow2(float x, int d) {
     if (d < -300) return 0.0f;
     if (d > 254) d = 254;
     return ldexpf(x, d);
+}
+
+// 2^d for an integer d <= 127 (0 below the subnormal range).
+__device__ __forceinline__ float fa_pow2(int d) {
+    if (d >= -126) return __int_as_float((d + 127) << 23);
+    if (d >= -149) return __int_as_float(1 << (d + 149));
+    return 0.0f;
+}
+
+// x * 2^d for any integer d (the common case |d| <= 126 is one multiply).
+__device__ __forceinline__ float fa_mul_pow2(float x, int d) {
+    if (d >= -126 && d <= 127) return x * __int_as_float((d + 127) << 23);
+    return ldexpf(x, max(min(d, 300), -300));
 }
 
 // Split x > 0 into m in [1, 2) and integer e with x = m * 2^e (normal or subnormal x).

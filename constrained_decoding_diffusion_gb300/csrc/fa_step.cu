@@ -23,6 +23,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kRwThreads = 1024;
+constexpr int kRwWarps = kRwThreads / 32;
 
 // ----------------------------------------------------------------------------- workspace plan
 
@@ -30,7 +32,8 @@ struct Plan {
     int B = 0, L = 0, S = 0, V = 0, K = 0, Lp = 1;
     int nk[18] = {0};
     size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, mu[18] = {0};
-    size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, zsum = 0, zexp = 0;
+    size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, zsum = 0, zexp = 0;
+    size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0;
     size_t total = 0;
 };
 
@@ -49,8 +52,20 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
         size_t nodes = (size_t)B * (size_t)p.nk[k];
         p.mant[k] = take(nodes * S * S * sizeof(float));
         p.rho[k] = take(nodes * S * sizeof(int32_t));
-        p.rmax[k] = take(nodes * S * sizeof(int32_t));
         p.mu[k] = take(k ? nodes * S * sizeof(int32_t) : 0);
+    }
+    // row maxima: level 0, then levels 1..K back to back (cleared together by the reweight)
+    p.rmax[0] = take((size_t)B * p.nk[0] * S * sizeof(int32_t));
+    size_t hi = 0;
+    for (int k = 1; k <= p.K; ++k) hi += (size_t)B * p.nk[k] * S * sizeof(int32_t);
+    p.rmax_hi = off;
+    p.rmax_hi_bytes = hi;
+    {
+        size_t o = p.rmax_hi;
+        for (int k = 1; k <= p.K; ++k) { p.rmax[k] = o; o += (size_t)B * p.nk[k] * S * sizeof(int32_t); }
+        p.leaf_done = p.rmax_hi + hi;          // ticket counter of the leaf blocks, cleared with them
+        p.rmax_hi_bytes = hi + sizeof(int32_t);
+        off = align256(p.rmax_hi + hi + sizeof(int32_t));
     }
     size_t bnd = (size_t)B * (size_t)(L + 1);
     p.z = take(bnd * sizeof(int32_t));
@@ -58,6 +73,7 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
     p.ae = take(bnd * S * sizeof(int32_t));
     p.bm = take(bnd * S * sizeof(float));
     p.be = take(bnd * S * sizeof(int32_t));
+    p.keys = take((size_t)B * (size_t)L * sizeof(unsigned long long));
     p.zsum = take((size_t)B * sizeof(float));
     p.zexp = take((size_t)B * sizeof(int32_t));
     p.total = off;
@@ -73,6 +89,9 @@ struct DevFA {
     const int32_t *row_cell_off, *cell_dst, *cell_src;
     const int64_t *cell_off;
     const int32_t *cell_tok;
+    const uint16_t *tok8;
+    const int32_t *piece_cell_off, *sl_row_off, *sl_goff, *sl_piece;
+    int chunk_tokens, n_chunks, n_cells;
 };
 
 DevFA dev_view(const fa_automaton *a) {
@@ -82,6 +101,9 @@ DevFA dev_view(const fa_automaton *a) {
     d.tok_off = a->tok_off; d.tok_edges = a->tok_edges;
     d.row_cell_off = a->row_cell_off; d.cell_dst = a->cell_dst; d.cell_src = a->cell_src;
     d.cell_off = a->cell_off; d.cell_tok = a->cell_tok;
+    d.tok8 = a->tok8; d.piece_cell_off = a->piece_cell_off; d.sl_row_off = a->sl_row_off;
+    d.sl_goff = a->sl_goff; d.sl_piece = a->sl_piece;
+    d.chunk_tokens = a->chunk_tokens; d.n_chunks = a->n_chunks; d.n_cells = a->n_cells;
     return d;
 }
 
@@ -123,56 +145,124 @@ __device__ int warp_categorical(int n, float u, WF w) {
 
 // ----------------------------------------------------------------------------- 1. reweight
 
-// One block per (position, row block): M_t(s, s') for rows s in [r0, r1) as a dense fp32 row
-// segment with row exponent 0.  A masked position sums its probabilities over each cell's
-// tokens (papernotes.org key design 1: g(x=v | z=e) = 1[v in label(e)] p_t(v), aggregated
-// over edges s -> s'); a committed position counts the edges s -> s' that carry its token.
-__global__ void __launch_bounds__(kThreads) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
-                                                     const int32_t *__restrict__ committed,
-                                                     const int32_t *__restrict__ rb, int nrb, float *mant,
-                                                     int32_t *rho, int32_t *rmax) {
-    __shared__ int smax[FA_MAX_STATES];
-    const int S = fa.S;
+// One block per (position, row block): M_t(s, s') for rows s in [r0, r1), row exponent 0.  A
+// masked position sums its probabilities over each cell's tokens (papernotes.org key design
+// 1: g(x=v | z=e) = 1[v in label(e)] p_t(v), aggregated over the edges s -> s'); a committed
+// position counts the edges s -> s' that carry its token.
+//
+// The probability row is staged in shared memory one vocabulary chunk at a time (the whole
+// row when |V| <= 32767) by asynchronous copies.  The block's token indices are stored as
+// slices of 32 pieces (sliced ELL, see fa_automaton): one warp per slice, lane l sums piece l
+// from coalesced 16-byte groups of 8 in-chunk indices, with the entries of every group
+// ordered at compile time so the 32 lanes' gathers fall into distinct banks.  Each piece's
+// sum lands in its own shared-memory slot; after the last chunk every cell adds its pieces
+// in a fixed order, so the result is deterministic.
+__global__ void __launch_bounds__(kRwThreads) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
+                                                       const int32_t *__restrict__ committed,
+                                                       const int4 *__restrict__ rbm, int nrb, int max_pieces,
+                                                       float *mant, int32_t *rho, int32_t *rmax, int32_t *zero,
+                                                       long n_zero) {
+    extern __shared__ float smem_f[];
+    // clear the row maxima of the higher tree levels (their products accumulate with atomicMax)
+    {
+        const long nb = (long)gridDim.x * gridDim.y;
+        const long bid = (long)blockIdx.y * gridDim.x + blockIdx.x;
+        for (long i = bid * kRwThreads + threadIdx.x; i < n_zero; i += nb * kRwThreads) zero[i] = 0;
+    }
+    const int S = fa.S, CH = fa.chunk_tokens, nch = fa.n_chunks;
+    float *sp = smem_f;                                  // [CH + 1] staged chunk, sp[CH] = 0
+    float *part = sp + ((CH + 4) & ~3);                  // [max_pieces] per-piece sums
+    int *smax = (int *)(part + max_pieces);              // [rows] row maxima (bits)
     const int t = blockIdx.x / nrb, r = blockIdx.x % nrb, b = blockIdx.y;
-    const int r0 = rb[r], r1 = rb[r + 1];
-    if (r0 >= r1) return;
     const size_t pos = (size_t)b * L + t;
-    float *M = mant + pos * (size_t)S * S;
-    for (size_t i = (size_t)r0 * S + threadIdx.x; i < (size_t)r1 * S; i += kThreads) M[i] = 0.0f;
-    for (int i = threadIdx.x; i < r1 - r0; i += kThreads) smax[i] = 0;
-    __syncthreads();
+    // the block's metadata and the committed token, loaded together
+    const int4 m0 = __ldg(rbm + 2 * r), m1 = __ldg(rbm + 2 * r + 1);
     const int c = committed[pos];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = m0.x, r1 = m0.y, cb = m0.z, ce = m0.w, nc = ce - cb;
+    if (r0 >= r1) return;
+    float *M = mant + pos * (size_t)S * S;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < r1 - r0; i += kRwThreads) smax[i] = 0;
+    for (size_t i = (size_t)r0 * S + tid; i < (size_t)r1 * S; i += kRwThreads) M[i] = 0.0f;
     if (c < 0) {
+        const int pbase = m1.x;
         const float *prow = probs + pos * (size_t)fa.V;
-        const int cb = fa.row_cell_off[r0], ce = fa.row_cell_off[r1];
-        for (int cell = cb + warp; cell < ce; cell += kWarps) {
-            const int64_t a0 = fa.cell_off[cell], a1 = fa.cell_off[cell + 1];
-            float acc = 0.0f;
-            for (int64_t j = a0 + lane; j < a1; j += 32) acc += __ldg(prow + fa.cell_tok[j]);
-            acc = fa_warp_sum(acc);
-            if (lane == 0) {
-                const int s = fa.cell_src[cell];
-                M[(size_t)s * S + fa.cell_dst[cell]] = acc;
-                atomicMax(&smax[s - r0], __float_as_int(acc));
+        const uint4 *g8 = reinterpret_cast<const uint4 *>(fa.tok8);
+        for (int ch = 0; ch < nch; ++ch) {
+            const int base = ch * CH;
+            const int n = min(CH, fa.V - base);
+            __syncthreads();
+            if ((reinterpret_cast<uintptr_t>(prow + base) & 15) == 0) {
+                // asynchronous 16-byte global->shared copies, all in flight before one wait
+                const char *src = reinterpret_cast<const char *>(prow + base);
+                const unsigned dst = (unsigned)__cvta_generic_to_shared(sp);
+                for (int i = tid; i < (n >> 2); i += kRwThreads)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + 16u * i), "l"(src + 16 * (size_t)i)
+                                 : "memory");
+                asm volatile("cp.async.commit_group;\n" ::: "memory");
+                for (int i = (n & ~3) + tid; i < n; i += kRwThreads) sp[i] = __ldg(prow + base + i);
+            } else {
+                for (int i = tid; i < n; i += kRwThreads) sp[i] = __ldg(prow + base + i);
+            }
+            if (tid == 0) sp[CH] = 0.0f;
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
+            __syncthreads();
+            const int s0 = fa.sl_row_off[(size_t)ch * (S + 1) + r0], s1 = fa.sl_row_off[(size_t)ch * (S + 1) + r1];
+            for (int sl = s0 + warp; sl < s1; sl += kRwWarps) {
+                const int g0 = fa.sl_goff[sl];
+                const int len = (fa.sl_goff[sl + 1] - g0) >> 5;
+                const int pid = fa.sl_piece[(size_t)sl * 32 + lane];
+                float acc = 0.0f;
+                for (int k0 = 0; k0 < len; k0 += 4) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        v[u] = (k0 + u < len) ? __ldg(g8 + g0 + (k0 + u) * 32 + lane) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (k0 + u < len) {
+                            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                            float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                a0 += sp[wv[h] & 0xffffu];
+                                a1 += sp[wv[h] >> 16];
+                            }
+                            acc += a0 + a1;
+                        }
+                    }
+                }
+                if (pid >= 0) part[pid - pbase] = acc;
             }
         }
-    } else if (c < fa.V) {
-        const int64_t a0 = fa.tok_off[c], a1 = fa.tok_off[c + 1];
-        for (int64_t j = a0 + threadIdx.x; j < a1; j += kThreads) {
-            const int e = fa.tok_edges[j];
-            const int s = fa.edge_src[e];
-            if (s >= r0 && s < r1) atomicAdd(&M[(size_t)s * S + fa.edge_dst[e]], 1.0f);
-        }
         __syncthreads();
-        for (int64_t j = a0 + threadIdx.x; j < a1; j += kThreads) {
-            const int e = fa.tok_edges[j];
-            const int s = fa.edge_src[e];
-            if (s >= r0 && s < r1) atomicMax(&smax[s - r0], __float_as_int(M[(size_t)s * S + fa.edge_dst[e]]));
+        for (int i = tid; i < nc; i += kRwThreads) {
+            const int cell = cb + i;
+            float v = 0.0f;
+            for (int q = fa.piece_cell_off[cell]; q < fa.piece_cell_off[cell + 1]; ++q) v += part[q - pbase];
+            const int s = fa.cell_src[cell];
+            M[(size_t)s * S + fa.cell_dst[cell]] = v;
+            atomicMax(&smax[s - r0], __float_as_int(v));
+        }
+    } else {
+        __syncthreads();
+        if (c < fa.V) {
+            const int64_t a0 = fa.tok_off[c], a1 = fa.tok_off[c + 1];
+            for (int64_t j = a0 + tid; j < a1; j += kRwThreads) {
+                const int e = fa.tok_edges[j];
+                const int s = fa.edge_src[e];
+                if (s >= r0 && s < r1) atomicAdd(&M[(size_t)s * S + fa.edge_dst[e]], 1.0f);
+            }
+            __syncthreads();
+            for (int64_t j = a0 + tid; j < a1; j += kRwThreads) {
+                const int e = fa.tok_edges[j];
+                const int s = fa.edge_src[e];
+                if (s >= r0 && s < r1) atomicMax(&smax[s - r0], __float_as_int(M[(size_t)s * S + fa.edge_dst[e]]));
+            }
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < r1 - r0; i += kThreads) {
+    for (int i = tid; i < r1 - r0; i += kRwThreads) {
         rho[pos * S + r0 + i] = 0;
         if (rmax) rmax[pos * S + r0 + i] = smax[i];
     }
@@ -211,6 +301,120 @@ __global__ void __launch_bounds__(kThreads) k_rowshift(int S, int L, int k, int 
     }
     best = fa_warp_max_int(best);
     if (lane == 0) mu[pnode * S + i] = best;
+}
+
+// |S| <= 64: a product C = A_L A_R of one node is split into 32x32 output tiles, one block
+// each, with the row shift mu (see k_rowshift) recomputed per block from its 32 full rows and
+// the row maxima combined across column tiles with atomicMax (cleared by the reweight).
+constexpr int SMALL_S = 64;
+constexpr int ST = 32;
+
+__global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, int nk, const float *__restrict__ mant_c,
+                                                       const int32_t *__restrict__ rho_c,
+                                                       const int32_t *__restrict__ rmax_c, int nc, float *mant_p,
+                                                       int32_t *rho_p, int32_t *rmax_p) {
+    __shared__ float As[ST][SMALL_S + 1];
+    __shared__ float Bs[SMALL_S][ST + 1];
+    __shared__ int rhoR_s[SMALL_S], rmaxR_s[SMALL_S], mu_s[ST];
+    const int tpd = (S + ST - 1) / ST;
+    const int tile = blockIdx.x % (tpd * tpd);
+    const long bn = blockIdx.x / (tpd * tpd);
+    const int node = (int)(bn % nk), b = (int)(bn / nk);
+    const int i0 = (tile / tpd) * ST, j0 = (tile % tpd) * ST;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t pnode = (size_t)b * nk + node;
+    const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
+    const size_t SS = (size_t)S * S;
+    const float *A = mant_c + lnode * SS;
+    float *C = mant_p + pnode * SS;
+    if (((2 * node + 1) << (k - 1)) >= L) {      // right child is padding: C = A_L
+        for (int q = tid; q < ST * ST; q += kThreads) {
+            const int r = i0 + q / ST, c = j0 + q % ST;
+            if (r < S && c < S) C[(size_t)r * S + c] = A[(size_t)r * S + c];
+        }
+        if (j0 == 0)
+            for (int r = i0 + tid; r < min(i0 + ST, S); r += kThreads) {
+                rho_p[pnode * S + r] = rho_c[lnode * S + r];
+                rmax_p[pnode * S + r] = rmax_c[lnode * S + r];
+            }
+        return;
+    }
+    const float *Bm = mant_c + rnode * SS;
+    {
+        // all loads of this thread in flight before any shared-memory store
+        constexpr int U = ST * SMALL_S / kThreads;  // 8
+        float va[U], vb[U];
+        int ra = 0, rr = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = tid + u * kThreads;
+            const int r = q / SMALL_S, c = q % SMALL_S;                  // A: 32 rows x 64 cols
+            va[u] = (i0 + r < S && c < S) ? __ldg(A + (size_t)(i0 + r) * S + c) : 0.0f;
+            const int rb = q / ST, cb = q % ST;                          // B: 64 rows x 32 cols
+            vb[u] = (rb < S && j0 + cb < S) ? __ldg(Bm + (size_t)rb * S + j0 + cb) : 0.0f;
+        }
+        if (tid < SMALL_S) {
+            ra = tid < S ? rho_c[rnode * S + tid] : 0;
+            rr = tid < S ? rmax_c[rnode * S + tid] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = tid + u * kThreads;
+            As[q / SMALL_S][q % SMALL_S] = va[u];
+            Bs[q / ST][q % ST] = vb[u];
+        }
+        if (tid < SMALL_S) { rhoR_s[tid] = ra; rmaxR_s[tid] = rr; }
+    }
+    __syncthreads();
+    for (int r = warp; r < ST; r += kWarps) {
+        int best = FA_INT_NONE;
+        for (int m = lane; m < S; m += 32) {
+            const float x = As[r][m];
+            const int q = rmaxR_s[m];
+            if (x > 0.0f && q > 0) best = max(best, rhoR_s[m] + fa_exponent(__int_as_float(q)) + fa_exponent(x));
+        }
+        best = fa_warp_max_int(best);
+        if (lane == 0) mu_s[r] = best;
+    }
+    __syncthreads();
+    for (int q = tid; q < ST * SMALL_S; q += kThreads) {
+        const int r = q / SMALL_S, m = q % SMALL_S;
+        const float x = As[r][m];
+        const int mr = mu_s[r];
+        As[r][m] = (x > 0.0f && mr != FA_INT_NONE && m < S && rmaxR_s[m] > 0) ? fa_mul_pow2(x, rhoR_s[m] - mr) : 0.0f;
+    }
+    __syncthreads();
+    const int tx = tid & 15, ty = tid >> 4;          // 2x2 outputs per thread
+    float c00 = 0.0f, c01 = 0.0f, c10 = 0.0f, c11 = 0.0f;
+    for (int m = 0; m < S; ++m) {
+        const float a0 = As[2 * ty][m], a1 = As[2 * ty + 1][m];
+        const float b0 = Bs[m][2 * tx], b1 = Bs[m][2 * tx + 1];
+        c00 = fmaf(a0, b0, c00); c01 = fmaf(a0, b1, c01);
+        c10 = fmaf(a1, b0, c10); c11 = fmaf(a1, b1, c11);
+    }
+    const float cv[2][2] = {{c00, c01}, {c10, c11}};
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int i = i0 + 2 * ty + p;
+        float mx = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int j = j0 + 2 * tx + q;
+            if (i < S && j < S) {
+                C[(size_t)i * S + j] = cv[p][q];
+                mx = fmaxf(mx, cv[p][q]);
+            }
+        }
+#pragma unroll
+        for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (tx == 0 && i < S) {
+            if (mx > 0.0f) atomicMax(&rmax_p[pnode * S + i], __float_as_int(mx));
+            if (j0 == 0) {
+                const int mr = mu_s[2 * ty + p];
+                rho_p[pnode * S + i] = (mr == FA_INT_NONE) ? 0 : rho_c[lnode * S + i] + mr;
+            }
+        }
+    }
 }
 
 constexpr int GBM = 64, GBN = 64, GBK = 16;
@@ -267,7 +471,7 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int
             if (i < S && m < S) {
                 const float x = A[(size_t)i * S + m];
                 const int mr = mu_s[r];
-                if (x > 0.0f && mr != FA_INT_NONE && rmaxR[m] > 0) v = fa_scale_pow2(x, rhoR[m] - mr);
+                if (x > 0.0f && mr != FA_INT_NONE && rmaxR[m] > 0) v = fa_mul_pow2(x, rhoR[m] - mr);
             }
             As[kk][r] = v;
         }
@@ -360,127 +564,192 @@ __global__ void __launch_bounds__(kThreads) k_root(DevFA fa, int L, int K, int n
 
 // ----------------------------------------------------------------------------- 4. top-down
 
-// Midpoints of the nodes of level k+1: z_m ~ A[l, m)[z_l, s] * A[m, r)[s, z_r] (paperfeed.app,
-// "The scan trick"; papernotes.org key design 2: given the segment ends, the halves are
-// conditionally independent given the midpoint).  One warp per node.
-__global__ void __launch_bounds__(kThreads) k_midpoint(int S, int B, int L, int k, int nc, const float *__restrict__ mant_c,
-                                                     const int32_t *__restrict__ rho_c, uint64_t seed,
-                                                     uint64_t offset, int32_t *z, int32_t *status) {
-    const int np = (L + (1 << (k + 1)) - 1) >> (k + 1);
-    const long gw = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (gw >= (long)B * np) return;
-    const int b = (int)(gw / np), j = (int)(gw % np);
+// One launch per tree level k+1 (K-1 down to 0) does three independent jobs for every node
+// [l, r) of that level with midpoint m < L (blocks are split by role):
+//  - midpoint: z_m ~ A[l, m)[z_l, s] * A[m, r)[s, z_r] (paperfeed.app, "The scan trick";
+//    papernotes.org key design 2: given the segment ends the two halves are conditionally
+//    independent given the midpoint), one warp per node;
+//  - prefix message alpha_m = alpha_l A[l, m), CB columns x QS row splits per block;
+//  - suffix message beta_m = A[m, r) beta_r, one warp per row.
+// Messages keep a mantissa in [1, 2) and an exponent per state, so no state is lost to range;
+// each sum is formed in two passes (largest term exponent, then terms scaled to it).
+struct TopdownArgs {
+    int S, B, L, k, nc, np;
+    int nA, nB;           // number of alpha and beta blocks
+    int CB, QS;           // alpha: columns per block, row splits
+    const float *mant;    // level-k spans
+    const int32_t *rho;
+    uint64_t seed, offset;
+    int32_t *z, *status;
+    float *am, *bm;
+    int32_t *ae, *be;
+};
+
+__device__ void topdown_midpoint(const TopdownArgs &a, int blk) {
+    const int S = a.S, L = a.L, k = a.k;
+    const long gw = (long)blk * kWarps + (threadIdx.x >> 5);
+    if (gw >= (long)a.B * a.np) return;
+    const int b = (int)(gw / a.np), j = (int)(gw % a.np);
     const int l = j << (k + 1), m = l + (1 << k);
     if (m >= L) return;
     const int r = min(l + (1 << (k + 1)), L);
-    if (__shfl_sync(0xffffffffu, status[b], 0) != FA_ROW_OK) return;
-    const int32_t *zb = z + (size_t)b * (L + 1);
+    if (__shfl_sync(0xffffffffu, a.status[b], 0) != FA_ROW_OK) return;
+    const int32_t *zb = a.z + (size_t)b * (L + 1);
     const int zl = zb[l], zr = zb[r];
-    const size_t lnode = (size_t)b * nc + 2 * j, rnode = lnode + 1;
-    const float *Lrow = mant_c + lnode * (size_t)S * S + (size_t)zl * S;
-    const float *R = mant_c + rnode * (size_t)S * S;
-    const int32_t *rhoR = rho_c + rnode * S;
+    const size_t lnode = (size_t)b * a.nc + 2 * j, rnode = lnode + 1;
+    const float *Lrow = a.mant + lnode * (size_t)S * S + (size_t)zl * S;
+    const float *R = a.mant + rnode * (size_t)S * S;
+    const int32_t *rhoR = a.rho + rnode * S;
     const int lane = threadIdx.x & 31;
     int emax = FA_INT_NONE;
     for (int s = lane; s < S; s += 32) {
-        const float a = Lrow[s], c = R[(size_t)s * S + zr];
-        if (a > 0.0f && c > 0.0f) emax = max(emax, rhoR[s] + fa_exponent(a) + fa_exponent(c));
+        const float x = Lrow[s], y = R[(size_t)s * S + zr];
+        if (x > 0.0f && y > 0.0f) emax = max(emax, rhoR[s] + fa_exponent(x) + fa_exponent(y));
     }
     emax = fa_warp_max_int(emax);
     int pick = -1;
     if (emax != FA_INT_NONE) {
-        const float u = fa_uniform(seed, offset, (uint32_t)m, (uint32_t)b, FA_RNG_MID);
+        const float u = fa_uniform(a.seed, a.offset, (uint32_t)m, (uint32_t)b, FA_RNG_MID);
         pick = warp_categorical(S, u, [&](int s) {
-            const float a = Lrow[s], c = R[(size_t)s * S + zr];
-            if (!(a > 0.0f && c > 0.0f)) return 0.0f;
-            float ma, mc;
-            int ea, ec;
-            fa_split(a, ma, ea);
-            fa_split(c, mc, ec);
-            return fa_scale_pow2(ma * mc, rhoR[s] + ea + ec - emax);
+            const float x = Lrow[s], y = R[(size_t)s * S + zr];
+            if (!(x > 0.0f && y > 0.0f)) return 0.0f;
+            float mx, my;
+            int ex, ey;
+            fa_split(x, mx, ex);
+            fa_split(y, my, ey);
+            return mx * my * fa_pow2(rhoR[s] + ex + ey - emax);
         });
     }
     if (lane == 0) {
-        if (pick < 0) status[b] = FA_ROW_UNDERFLOW;
-        else z[(size_t)b * (L + 1) + m] = pick;
+        if (pick < 0) a.status[b] = FA_ROW_UNDERFLOW;
+        else a.z[(size_t)b * (L + 1) + m] = pick;
     }
 }
 
-// Prefix messages alpha_m = alpha_l A[l, m) (one thread per column) for the nodes of level
-// k+1; alpha is kept per entry as mantissa in [1, 2) and exponent, so no state is lost to range.
-__global__ void __launch_bounds__(kThreads) k_alpha(int S, int L, int k, int nc, const float *__restrict__ mant_c,
-                                                  const int32_t *__restrict__ rho_c, float *am, int32_t *ae) {
-    extern __shared__ unsigned char smem_raw[];
-    float *sa = (float *)smem_raw;
-    int *se = (int *)(sa + S);
-    const int b = blockIdx.z, j = blockIdx.y;
+__device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
+    const int S = a.S, L = a.L, k = a.k, CB = a.CB, QS = a.QS;
+    const int ncb = (S + CB - 1) / CB;
+    const int cbk = blk % ncb;
+    const long bj = blk / ncb;
+    const int j = (int)(bj % a.np), b = (int)(bj / a.np);
     const int l = j << (k + 1), m = l + (1 << k);
     if (m >= L) return;
+    float *sa = sm;                          // [S] mantissas of alpha_l
+    int *sc = (int *)(sa + S);               // [S] alpha exponent + row exponent of A[l, m)
+    int *pe = sc + S;                        // [QS * CB] partial max exponents
+    float *ps = (float *)(pe + QS * CB);     // [QS * CB] partial sums
+    const size_t lnode = (size_t)b * a.nc + 2 * j;
     const size_t bl = ((size_t)b * (L + 1) + l) * S, bmid = ((size_t)b * (L + 1) + m) * S;
-    for (int s = threadIdx.x; s < S; s += kThreads) { sa[s] = am[bl + s]; se[s] = ae[bl + s]; }
+    const int32_t *rho = a.rho + lnode * S;
+    for (int q = threadIdx.x; q < S; q += kThreads) { sa[q] = a.am[bl + q]; sc[q] = a.ae[bl + q] + rho[q]; }
     __syncthreads();
-    const int col = blockIdx.x * kThreads + threadIdx.x;
-    if (col >= S) return;
-    const size_t lnode = (size_t)b * nc + 2 * j;
-    const float *A = mant_c + lnode * (size_t)S * S;
-    const int32_t *rho = rho_c + lnode * S;
-    fa_xacc x;
-    x.init();
-    for (int q = 0; q < S; ++q) {
-        const float a = sa[q];
-        if (a <= 0.0f) continue;
-        const float v = A[(size_t)q * S + col];
-        if (v <= 0.0f) continue;
-        float mv;
-        int ev;
-        fa_split(v, mv, ev);
-        x.add(a * mv, se[q] + rho[q] + ev);
+    const int c = threadIdx.x % CB, qs = threadIdx.x / CB;
+    const int col = cbk * CB + c;
+    const float *A = a.mant + lnode * (size_t)S * S;
+    constexpr int U = 16;  // loads issued together
+    int e = FA_INT_NONE;
+    if (col < S)
+        for (int q0 = qs; q0 < S; q0 += U * QS) {
+            float v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + u * QS;
+                v[u] = q < S ? __ldg(A + (size_t)q * S + col) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + u * QS;
+                if (v[u] > 0.0f && sa[q] > 0.0f) e = max(e, sc[q] + fa_exponent(v[u]));
+            }
+        }
+    pe[qs * CB + c] = e;
+    __syncthreads();
+    int E = FA_INT_NONE;
+    for (int t = 0; t < QS; ++t) E = max(E, pe[t * CB + c]);
+    float sum = 0.0f;
+    if (col < S && E != FA_INT_NONE)
+        for (int q0 = qs; q0 < S; q0 += U * QS) {
+            float v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + u * QS;
+                v[u] = q < S ? __ldg(A + (size_t)q * S + col) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + u * QS;
+                if (v[u] > 0.0f && sa[q] > 0.0f) {
+                    float mv;
+                    int ev;
+                    fa_split(v[u], mv, ev);
+                    sum += sa[q] * mv * fa_pow2(sc[q] + ev - E);
+                }
+            }
+        }
+    ps[qs * CB + c] = sum;
+    __syncthreads();
+    if (qs == 0 && col < S) {
+        float tot = 0.0f;
+        for (int t = 0; t < QS; ++t) tot += ps[t * CB + c];
+        float mo = 0.0f;
+        int eo = 0;
+        if (tot > 0.0f) { fa_split(tot, mo, eo); eo += E; }
+        a.am[bmid + col] = mo;
+        a.ae[bmid + col] = eo;
     }
-    float mo;
-    int eo;
-    x.normalised(mo, eo);
-    am[bmid + col] = mo;
-    ae[bmid + col] = eo;
 }
 
-// Suffix messages beta_m = A[m, r) beta_r (one warp per row) for the nodes of level k+1.
-__global__ void __launch_bounds__(kThreads) k_beta(int S, int L, int k, int nc, const float *__restrict__ mant_c,
-                                                 const int32_t *__restrict__ rho_c, float *bm, int32_t *be) {
-    extern __shared__ unsigned char smem_raw[];
-    float *sb = (float *)smem_raw;
-    int *se = (int *)(sb + S);
-    const int b = blockIdx.z, j = blockIdx.y;
+__device__ void topdown_beta(const TopdownArgs &a, int blk, float *sm) {
+    const int S = a.S, L = a.L, k = a.k;
+    const int nrbk = (S + kWarps - 1) / kWarps;
+    const int rbk = blk % nrbk;
+    const long bj = blk / nrbk;
+    const int j = (int)(bj % a.np), b = (int)(bj / a.np);
     const int l = j << (k + 1), m = l + (1 << k);
     if (m >= L) return;
     const int r = min(l + (1 << (k + 1)), L);
+    float *sb = sm;
+    int *se = (int *)(sb + S);
     const size_t br = ((size_t)b * (L + 1) + r) * S, bmid = ((size_t)b * (L + 1) + m) * S;
-    for (int s = threadIdx.x; s < S; s += kThreads) { sb[s] = bm[br + s]; se[s] = be[br + s]; }
+    for (int q = threadIdx.x; q < S; q += kThreads) { sb[q] = a.bm[br + q]; se[q] = a.be[br + q]; }
     __syncthreads();
-    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int row = rbk * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= S) return;
-    const size_t rnode = (size_t)b * nc + 2 * j + 1;
-    const float *Rrow = mant_c + rnode * (size_t)S * S + (size_t)row * S;
-    fa_xacc x;
-    x.init();
+    const size_t rnode = (size_t)b * a.nc + 2 * j + 1;
+    const float *Rrow = a.mant + rnode * (size_t)S * S + (size_t)row * S;
+    int e = FA_INT_NONE;
     for (int q = lane; q < S; q += 32) {
-        const float bv = sb[q];
-        if (bv <= 0.0f) continue;
         const float v = Rrow[q];
-        if (v <= 0.0f) continue;
-        float mv;
-        int ev;
-        fa_split(v, mv, ev);
-        x.add(bv * mv, se[q] + ev);
+        if (v > 0.0f && sb[q] > 0.0f) e = max(e, se[q] + fa_exponent(v));
     }
-    x.warp_reduce();
+    e = fa_warp_max_int(e);
+    float sum = 0.0f;
+    if (e != FA_INT_NONE)
+        for (int q = lane; q < S; q += 32) {
+            const float v = Rrow[q];
+            if (v > 0.0f && sb[q] > 0.0f) {
+                float mv;
+                int ev;
+                fa_split(v, mv, ev);
+                sum += sb[q] * mv * fa_pow2(se[q] + ev - e);
+            }
+        }
+    sum = fa_warp_sum(sum);
     if (lane == 0) {
-        float mo;
-        int eo;
-        x.normalised(mo, eo);
-        bm[bmid + row] = mo;
-        be[bmid + row] = (mo > 0.0f) ? eo + rho_c[rnode * S + row] : 0;
+        float mo = 0.0f;
+        int eo = 0;
+        if (sum > 0.0f) { fa_split(sum, mo, eo); eo += e + a.rho[rnode * S + row]; }
+        a.bm[bmid + row] = mo;
+        a.be[bmid + row] = eo;
     }
+}
+
+__global__ void __launch_bounds__(kThreads) k_topdown(TopdownArgs a) {
+    extern __shared__ float smem_td[];
+    const int blk = blockIdx.x;
+    if (blk < a.nA) topdown_alpha(a, blk, smem_td);
+    else if (blk < a.nA + a.nB) topdown_beta(a, blk - a.nA, smem_td);
+    else topdown_midpoint(a, blk - a.nA - a.nB);
 }
 
 // ----------------------------------------------------------------------------- 5. leaves
@@ -490,13 +759,12 @@ __global__ void __launch_bounds__(kThreads) k_beta(int S, int L, int k, int nc, 
 // parallel at the leaves), then its constrained marginal
 //   p(x_t = v) = w_t(v) sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / Z
 // (papernotes.org key design 3).  One warp per position.
-__global__ void __launch_bounds__(kThreads) k_leaf(DevFA fa, int B, int L, const float *__restrict__ probs,
-                                                 const int32_t *__restrict__ committed, uint64_t seed, uint64_t offset,
-                                                 const int32_t *__restrict__ z, const float *__restrict__ am,
-                                                 const int32_t *__restrict__ ae, const float *__restrict__ bm,
-                                                 const int32_t *__restrict__ be, const float *__restrict__ zsum_ws,
-                                                 const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg,
-                                                 int32_t *status) {
+__device__ void leaf_position(const DevFA &fa, int B, int L, const float *__restrict__ probs,
+                              const int32_t *__restrict__ committed, uint64_t seed, uint64_t offset,
+                              const int32_t *__restrict__ z, const float *__restrict__ am,
+                              const int32_t *__restrict__ ae, const float *__restrict__ bm,
+                              const int32_t *__restrict__ be, const float *__restrict__ zsum_ws,
+                              const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg, int32_t *status) {
     const long gw = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (gw >= (long)B * L) return;
     const int b = (int)(gw / L), t = (int)(gw % L);
@@ -556,6 +824,37 @@ __global__ void __launch_bounds__(kThreads) k_leaf(DevFA fa, int B, int L, const
     }
 }
 
+
+__device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const int32_t *__restrict__ committed,
+                         const int32_t *status, int32_t *out, int32_t *tokens, unsigned long long *skey);
+
+// Leaves, then the commit: every block takes a ticket after its positions are written; the
+// last block to finish sees all marginals and runs the top-k of every sequence.
+__global__ void __launch_bounds__(kThreads) k_leaf_commit(DevFA fa, int B, int L, const float *__restrict__ probs,
+                                                        const int32_t *__restrict__ committed, uint64_t seed,
+                                                        uint64_t offset, const int32_t *__restrict__ z,
+                                                        const float *__restrict__ am, const int32_t *__restrict__ ae,
+                                                        const float *__restrict__ bm, const int32_t *__restrict__ be,
+                                                        const float *__restrict__ zsum_ws,
+                                                        const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg,
+                                                        int32_t *status, int k, int lo, int hi, int32_t *commit_idx,
+                                                        unsigned long long *keys, int32_t *done) {
+    leaf_position(fa, B, L, probs, committed, seed, offset, z, am, ae, bm, be, zsum_ws, zexp_ws, tokens, marg, status);
+    __shared__ int last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int b = 0; b < B; ++b) {
+        topk_row(b, L, k, lo, hi, marg, committed, status, commit_idx, tokens, keys + (size_t)b * L);
+        __syncthreads();
+    }
+}
+
 // ----------------------------------------------------------------------------- 6. commit
 
 // Per sequence, the k masked positions of [lo, hi) with the largest marginal, descending,
@@ -563,30 +862,33 @@ __global__ void __launch_bounds__(kThreads) k_leaf(DevFA fa, int B, int L, const
 // highest-probability rule in the paperfeed.app summary).  Rank by counting larger keys.
 // A sequence whose status is not OK gets no commits and -1 tokens / 0 marginals at every
 // masked position (some leaves may have been drawn before the failure was recorded).
-__global__ void __launch_bounds__(kThreads) k_topk(int L, int k, int lo, int hi, float *marg,
-                                                 const int32_t *__restrict__ committed,
-                                                 const int32_t *__restrict__ status, int32_t *out, int32_t *tokens) {
-    const int b = blockIdx.x;
+// Executed by one whole block; skey holds hi - lo keys.
+__device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const int32_t *__restrict__ committed,
+                         const int32_t *status, int32_t *out, int32_t *tokens, unsigned long long *skey) {
     int32_t *o = out + (size_t)b * k;
-    for (int i = threadIdx.x; i < k; i += kThreads) o[i] = -1;
-    __syncthreads();
+    for (int i = threadIdx.x; i < k; i += blockDim.x) o[i] = -1;
     if (status[b] != FA_ROW_OK) {
-        for (int t = threadIdx.x; t < L; t += kThreads)
+        for (int t = threadIdx.x; t < L; t += blockDim.x)
             if (committed[(size_t)b * L + t] < 0) { tokens[(size_t)b * L + t] = -1; marg[(size_t)b * L + t] = 0.0f; }
         return;
     }
     const float *mg = marg + (size_t)b * L;
     const int32_t *cm = committed + (size_t)b * L;
-    auto key = [&](int t) -> unsigned long long {
-        if (t < lo || t >= hi || cm[t] >= 0) return 0ull;
-        return ((unsigned long long)(unsigned)__float_as_int(mg[t]) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)t);
-    };
-    for (int t = max(lo, 0) + threadIdx.x; t < min(hi, L); t += kThreads) {
-        const unsigned long long kt = key(t);
+    const int t0 = max(lo, 0), t1 = min(hi, L), n = t1 - t0;
+    // key = (marginal bits, ~t): larger marginal first, then lower position; 0 = not eligible
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int t = t0 + i;
+        skey[i] = (cm[t] >= 0) ? 0ull
+                               : (((unsigned long long)(unsigned)__float_as_int(mg[t]) << 32) |
+                                  (unsigned long long)(0xFFFFFFFFu - (unsigned)t));
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const unsigned long long kt = skey[i];
         if (!kt) continue;
         int rank = 0;
-        for (int q = max(lo, 0); q < min(hi, L) && rank < k; ++q) rank += key(q) > kt;
-        if (rank < k) o[rank] = t;
+        for (int q = 0; q < n && rank < k; ++q) rank += skey[q] > kt;
+        if (rank < k) o[rank] = t0 + i;
     }
 }
 
@@ -632,11 +934,12 @@ void stage_mark(int i, cudaStream_t s) {
     else cudaEventRecord(g_stage.ev[i], s);
 }
 
-int pick_row_blocks(const fa_automaton *a, long positions) {
-    // aim for roughly four blocks of work per SM over the masked positions
-    int lvl = 0;
-    while (lvl + 1 < a->n_rb_levels && positions * (1L << lvl) < 152L * 4) ++lvl;
-    return lvl;
+int pick_partition(const fa_automaton *a, long positions) {
+    // the first partition giving about two blocks per SM over all positions: every extra
+    // block re-stages its probability row and repeats its metadata round trips
+    int p = 0;
+    while (p + 1 < (int)a->part_count.size() && positions * a->part_count[p] < 152L * 2) ++p;
+    return p;
 }
 
 fa_status check_device(const fa_automaton *a, const char *fn) {
@@ -650,12 +953,20 @@ fa_status check_device(const fa_automaton *a, const char *fn) {
 }
 
 fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *probs, const int32_t *committed,
-                          float *mant, int32_t *rho, int32_t *rmax, cudaStream_t st) {
-    const int lvl = pick_row_blocks(a, (long)B * L);
-    const int nrb = 1 << lvl;
-    const int32_t *rb = a->rb_bounds + (nrb - 1) + lvl;
+                          float *mant, int32_t *rho, int32_t *rmax, cudaStream_t st, int32_t *zero = nullptr,
+                          long n_zero = 0) {
+    const int p = pick_partition(a, (long)B * L);
+    const int nrb = a->part_count[p];
+    const int4 *rbm = reinterpret_cast<const int4 *>(a->rb_meta) + 2 * (a->part_first[p] - p);
+    const int max_pieces = a->part_max_pieces[p];
+    const size_t smem = sizeof(float) * (size_t)(((a->chunk_tokens + 4) & ~3) + max_pieces + a->part_max_rows[p]);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_reweight, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) { fa_set_error(std::string("reweight smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    }
     dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
-    k_reweight<<<grid, kThreads, 0, st>>>(dev_view(a), L, probs, committed, rb, nrb, mant, rho, rmax);
+    k_reweight<<<grid, kRwThreads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, max_pieces, mant, rho, rmax,
+                                               zero, n_zero);
     return launch_check("reweight");
 }
 
@@ -713,14 +1024,23 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
     auto I = [&](size_t off) { return (int32_t *)(ws + off); };
     const int S = aut->S;
 
-    // 1. emission reweighting -> level-0 spans
+    // 1. emission reweighting -> level-0 spans (also clears the row maxima of levels >= 1)
     stage_mark(0, s);
-    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), s);
+    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), s, I(p.rmax_hi),
+                         (long)(p.rmax_hi_bytes / sizeof(int32_t)));
     if (st != FA_OK) return st;
 
     // 2. up-sweep: level k from level k-1
     stage_mark(1, s);
     for (int kk = 1; kk <= p.K; ++kk) {
+        if (S <= SMALL_S) {
+            const long tpd = (S + ST - 1) / ST;
+            k_span_small<<<(unsigned)((long)B * p.nk[kk] * tpd * tpd), kThreads, 0, s>>>(
+                S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), p.nk[kk - 1], F(p.mant[kk]),
+                I(p.rho[kk]), I(p.rmax[kk]));
+            if ((st = launch_check("span product (small)")) != FA_OK) return st;
+            continue;
+        }
         dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
         k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
                                            p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
@@ -740,34 +1060,32 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
     if ((st = launch_check("root")) != FA_OK) return st;
 
     // 4. top-down: midpoints and prefix/suffix messages, level K-1 .. 0
-    const size_t msg_smem = (size_t)S * 8;
     for (int kk = p.K - 1; kk >= 0; --kk) {
-        const int np = p.nk[kk + 1];
-        const long warps = (long)B * np;
-        k_midpoint<<<(unsigned)((warps + kWarps - 1) / kWarps), kThreads, 0, s>>>(
-            S, B, L, kk, p.nk[kk], F(p.mant[kk]), I(p.rho[kk]), philox_seed, philox_offset, I(p.z), row_status);
-        if ((st = launch_check("midpoint")) != FA_OK) return st;
-        dim3 ga((S + kThreads - 1) / kThreads, np, B);
-        k_alpha<<<ga, kThreads, msg_smem, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk]), I(p.rho[kk]), F(p.am), I(p.ae));
-        if ((st = launch_check("alpha")) != FA_OK) return st;
-        dim3 gb((S + kWarps - 1) / kWarps, np, B);
-        k_beta<<<gb, kThreads, msg_smem, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk]), I(p.rho[kk]), F(p.bm), I(p.be));
-        if ((st = launch_check("beta")) != FA_OK) return st;
+        TopdownArgs ta;
+        ta.S = S; ta.B = B; ta.L = L; ta.k = kk; ta.nc = p.nk[kk]; ta.np = p.nk[kk + 1];
+        ta.CB = S >= 64 ? 64 : ((S + 31) / 32) * 32;
+        ta.QS = kThreads / ta.CB;
+        ta.nA = B * ta.np * ((S + ta.CB - 1) / ta.CB);
+        ta.nB = B * ta.np * ((S + kWarps - 1) / kWarps);
+        const int nM = (B * ta.np + kWarps - 1) / kWarps;
+        ta.mant = F(p.mant[kk]); ta.rho = I(p.rho[kk]);
+        ta.seed = philox_seed; ta.offset = philox_offset;
+        ta.z = I(p.z); ta.status = row_status;
+        ta.am = F(p.am); ta.ae = I(p.ae); ta.bm = F(p.bm); ta.be = I(p.be);
+        const size_t smem = (size_t)S * 8 + (size_t)kThreads * 8;
+        k_topdown<<<(unsigned)(ta.nA + ta.nB + nM), kThreads, smem, s>>>(ta);
+        if ((st = launch_check("top-down level")) != FA_OK) return st;
     }
 
-    // 5. leaves: tokens and marginals
+    // 5. leaves: tokens and marginals, then the commit (one launch)
     stage_mark(3, s);
     const long lw = (long)B * L;
-    k_leaf<<<(unsigned)((lw + kWarps - 1) / kWarps), kThreads, 0, s>>>(
+    k_leaf_commit<<<(unsigned)((lw + kWarps - 1) / kWarps), kThreads, 0, s>>>(
         dev_view(aut), B, L, probs, committed, philox_seed, philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be),
-        F(p.zsum), I(p.zexp), tokens, marg, row_status);
-    if ((st = launch_check("leaf")) != FA_OK) return st;
-
-    // 6. commit
+        F(p.zsum), I(p.zexp), tokens, marg, row_status, k, commit_lo, commit_hi, commit_idx,
+        (unsigned long long *)(ws + p.keys), I(p.leaf_done));
+    st = launch_check("leaf and commit");
     stage_mark(4, s);
-    k_topk<<<B, kThreads, 0, s>>>(L, k, commit_lo, commit_hi, marg, committed, row_status, commit_idx, tokens);
-    st = launch_check("topk");
-    stage_mark(5, s);
     return st;
 }
 

@@ -29,8 +29,8 @@ EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_wor
            "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_noalloc",
            "fa_profile_enable", "fa_profile_read",
            "fa_launch_count", "fa_last_error")
-N_STAGES = 5
-STAGES = ("reweight", "upsweep", "topdown", "leaf", "commit")
+N_STAGES = 4
+STAGES = ("reweight", "upsweep", "topdown", "leaf_commit")
 
 _lib = None
 

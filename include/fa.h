@@ -218,15 +218,15 @@ fa_status fa_constrained_step_noalloc(const fa_automaton *aut, int32_t B, int32_
  *
  * fa_profile_enable(1) makes later fa_constrained_step calls on this host thread record
  * FA_N_STAGES + 1 CUDA events on their stream at the stage boundaries: 0 reweight,
- * 1 span up-sweep, 2 root + top-down sampling and messages, 3 leaf tokens and marginals,
- * 4 commit.  Inside a stream capture they become event-record graph nodes.
+ * 1 span up-sweep, 2 root + top-down sampling and messages, 3 leaf tokens, marginals and
+ * the commit.  Inside a stream capture they become event-record graph nodes.
  * fa_profile_read waits for the last boundary event and writes the FA_N_STAGES elapsed
  * times (ms) of the most recent recorded step into ms[FA_N_STAGES].
  * fa_launch_count gives the number of kernel launches this library has issued in the
  * process (one per kernel node when a step is captured into a graph).
  * Errors: FA_ERR_INVALID_ARG (NULL pointer, profiling never enabled), FA_ERR_CUDA.
  */
-#define FA_N_STAGES 5
+#define FA_N_STAGES 4
 fa_status fa_profile_enable(int32_t enable);
 fa_status fa_profile_read(float *ms);
 fa_status fa_launch_count(uint64_t *n);

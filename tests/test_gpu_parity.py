@@ -326,3 +326,47 @@ def test_determinism_and_offsets(native):
         assert np.array_equal(a[key], b[key]), key
     assert not np.array_equal(a["tokens"], c["tokens"])
     assert a["logZ"][0] == c["logZ"][0]
+
+
+# --------------------------------------------------------------------------- larger shapes
+
+def test_step_tiled_span_products(native):
+    """|S| = 100: tiled span products with a ragged last tile, and the row shift kernel."""
+    rng = np.random.default_rng(8)
+    fa = synth.random_dfa(100, 2000, 0.6, 10, seed=8)
+    o = oracle.OracleFA(fa)
+    aut = native.fa_compile(fa)
+    L = 40
+    probs = synth.gaussian_probs(rng, 2, L, 2000, 3.0)
+    committed = np.full((2, L), -1, np.int32)
+    x = synth.random_accepted_string(fa, L, rng)
+    idx = rng.choice(L, 10, replace=False)
+    committed[1, idx] = x[idx]
+    res = run_step(aut, probs, committed, seed=2, offset=0, k=6)
+    check_against_oracle(fa, o, probs, committed, res, 6)
+
+
+def test_step_layered_chain_full_size(native):
+    """JSON-schema-like layered chain at full size (B=4, L=256, |S|=256, |V|=151936); the
+    oracle checks two of the rows."""
+    w = synth.workload("layered_chain_S256_L256")
+    o = oracle.OracleFA(w.fa)
+    aut = native.fa_compile(w.fa)
+    probs = w.probs()
+    res = run_step(aut, probs, w.committed, seed=3, offset=0, k=w.k)
+    assert (res["status"] == 0).all()
+    check_against_oracle(w.fa, o, probs, w.committed, res, w.k, rows=[0, 3])
+    for b in (1, 2):
+        assert o.accepts(res["tokens"][b])
+
+
+def test_step_long_sequence_global_topk(native):
+    """L = 30000 > the shared-memory top-k window: keys go through the workspace."""
+    rng = np.random.default_rng(9)
+    fa = synth.random_dfa(3, 5, 0.2, 2, seed=1)
+    o = oracle.OracleFA(fa)
+    L = 30000
+    probs = synth.gaussian_probs(rng, 1, L, 5, 1.0)
+    committed = np.full((1, L), -1, np.int32)
+    res = run_step(native.fa_compile(fa), probs, committed, seed=4, offset=0, k=40)
+    check_against_oracle(fa, o, probs, committed, res, 40)
