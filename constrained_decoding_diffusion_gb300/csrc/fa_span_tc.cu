@@ -1,0 +1,330 @@
+// Span products on the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// One tree level of the up-sweep of the paperfeed.app summary of "Constrained Decoding for
+// Diffusion Language Models via Efficient Inference over Finite Automata" ("The scan trick":
+// 2^k-step transition matrices from two 2^(k-1)-step ones by batched matrix products; the
+// papernotes.org notes, key design 2): C = A_L * A_R for every node, in the per-row exponent
+// format of fa_step.cu.  The left operand is prescaled per (row, m) by 2^(rhoR[m] - mu[row])
+// (mu from the row-shift kernel) and both operands are split x = hi + lo with hi = x
+// truncated to TF32, so hi*hi + hi*lo + lo*hi on the TF32 tensor cores (fp32 accumulation)
+// keeps fp32 accuracy ("3xTF32"); lo*lo is below fp32 rounding.
+//
+// Tile: 128 rows x 256 columns per CTA, K in tiles of 32, two shared-memory stages.  All 256
+// threads convert a stage (global fp32 -> prescale -> hi/lo -> canonical K-major
+// no-swizzle layout: 8-row x 16-byte core matrices, K-direction core stride 128 B, row-group
+// stride 1024 B); one thread issues the MMAs (M=128, N=256, K=8 each) and commits them to the
+// stage's mbarrier; the stage is rewritten only after that mbarrier completes.  The
+// accumulators (128 lanes x 2 x 256 fp32 columns of tensor memory; k-tiles alternate between
+// them) are read back by the 8 warps, each from its own 32-lane quarter, added, and written
+// row-major with the tile's row maxima.
+//
+// Every mbarrier wait is bounded; a wait that runs out records FA_ROW_TIMEOUT in the error
+// word, waits (bounded) for the MMAs already issued, releases tensor memory and returns.
+#include <stdint.h>
+
+#include "fa_internal.cuh"
+
+namespace {
+
+constexpr int TM = 128, TN = 256, TK = 32, NTHR = 256;
+constexpr int A_BYTES = TM * TK * 4;        // 16 KB per copy (hi or lo)
+constexpr int B_BYTES = TN * TK * 4;        // 32 KB
+constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 96 KB
+constexpr int NSTAGE = 2;
+constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
+constexpr long long kSpinCycles = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// tcgen05 shared-memory matrix descriptor: start address, leading (K-direction) and stride
+// (8-row group) byte offsets, descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+    d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor of kind::tf32: D fp32, A and B TF32, both K-major, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t umma_idesc_tf32() {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// bounded wait (about a second of SM clock); false when the limit ran out
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kSpinCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// byte offset of element (row, k) in a K-major no-swizzle tile with 32 K-columns
+__device__ __forceinline__ uint32_t kmaj_off(int row, int k) {
+    return (uint32_t)((row >> 3) * 1024 + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4);
+}
+
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
+    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    lo = x - hi;
+}
+
+__global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk, const float *__restrict__ mant_c,
+                                                    const int32_t *__restrict__ rho_c,
+                                                    const int32_t *__restrict__ rmax_c, int nc,
+                                                    const int32_t *__restrict__ mu, float *mant_p, int32_t *rho_p,
+                                                    int32_t *rmax_p, int32_t *err) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ uint64_t mbar[NSTAGE];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int mu_s[TM];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN;
+    const long flat = blockIdx.x;
+    const int tn = (int)(flat % tiles_n), tm = (int)((flat / tiles_n) % tiles_m);
+    const long bn = flat / ((long)tiles_n * tiles_m);
+    const int node = (int)(bn % nk), b = (int)(bn / nk);
+    const int i0 = tm * TM, j0 = tn * TN;
+    const size_t SS = (size_t)S * S;
+    const size_t pnode = (size_t)b * nk + node;
+    const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
+    const float *A = mant_c + lnode * SS;
+    float *C = mant_p + pnode * SS;
+    if (((2 * node + 1) << (k - 1)) >= L) {           // right child is padding: C = A_L
+        for (int q = tid; q < TM * TN; q += NTHR) {
+            const int r = i0 + q / TN, c = j0 + q % TN;
+            if (r < S && c < S) C[(size_t)r * S + c] = A[(size_t)r * S + c];
+        }
+        if (tn == 0)
+            for (int r = i0 + tid; r < min(i0 + TM, S); r += NTHR) {
+                rho_p[pnode * S + r] = rho_c[lnode * S + r];
+                rmax_p[pnode * S + r] = rmax_c[lnode * S + r];
+            }
+        return;
+    }
+    const float *Bm = mant_c + rnode * SS;
+    const int32_t *rhoR = rho_c + rnode * S;
+    const int32_t *rmaxR = rmax_c + rnode * S;
+    // shared memory: NSTAGE x [A_hi | A_lo | B_hi | B_lo], then rhoR and rmaxR for every m
+    int *rhoR_s = reinterpret_cast<int *>(smem + NSTAGE * STAGE_BYTES);
+    int *rmaxR_s = rhoR_s + S;
+    for (int m = tid; m < S; m += NTHR) { rhoR_s[m] = rhoR[m]; rmaxR_s[m] = rmaxR[m]; }
+    for (int r = tid; r < TM; r += NTHR) mu_s[r] = (i0 + r < S) ? mu[pnode * S + i0 + r] : FA_INT_NONE;
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(&mbar[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_s)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t idesc = umma_idesc_tf32();
+    const int nkt = (S + TK - 1) / TK;
+    bool ok = true;
+    uint32_t phase[NSTAGE] = {0, 0};
+    int issued[NSTAGE] = {0, 0};
+
+    for (int kt = 0; kt < nkt; ++kt) {
+        const int st = kt % NSTAGE;
+        unsigned char *stage = smem + st * STAGE_BYTES;
+        // the MMAs that last read this stage must be complete before it is rewritten
+        if (issued[st]) {
+            if (!mbar_wait(&mbar[st], phase[st])) ok = false;
+            phase[st] ^= 1;
+            issued[st] = 0;
+        }
+        if (!__syncthreads_and(ok)) { ok = false; break; }
+        const int k0 = kt * TK;
+        // A: 128 rows x 32 k; thread -> (row = tid / 2, k half = tid % 2), 4 float4 loads
+        {
+            const int row = tid >> 1, kh = (tid & 1) * 16;
+            const int gi = i0 + row;
+            const int mrow = mu_s[row];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int kk = kh + 4 * q;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gi < S && k0 + kk < S) v = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gi * S + k0 + kk));
+                float x[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = k0 + kk + e;
+                    float y = 0.0f;
+                    if (x[e] > 0.0f && mrow != FA_INT_NONE && m < S && rmaxR_s[m] > 0)
+                        y = fa_mul_pow2(x[e], rhoR_s[m] - mrow);
+                    split_tf32(y, hi[e], lo[e]);
+                }
+                const uint32_t off = kmaj_off(row, kk);
+                *reinterpret_cast<float4 *>(stage + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4 *>(stage + A_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        // B: 256 columns n x 32 k; thread -> column n = tid, 8 groups of 4 k
+        {
+            const int n = tid, gj = j0 + n;
+#pragma unroll
+            for (int g = 0; g < TK / 4; ++g) {
+                float x[4], hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = k0 + 4 * g + e;
+                    x[e] = (gj < S && m < S) ? __ldg(Bm + (size_t)m * S + gj) : 0.0f;
+                    split_tf32(x[e], hi[e], lo[e]);
+                }
+                const uint32_t off = kmaj_off(n, 4 * g);
+                *reinterpret_cast<float4 *>(stage + 2 * A_BYTES + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4 *>(stage + 2 * A_BYTES + B_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t a_hi = smem_u32(stage), a_lo = a_hi + A_BYTES;
+            const uint32_t b_hi = a_hi + 2 * A_BYTES, b_lo = b_hi + B_BYTES;
+#pragma unroll
+            // k-tiles alternate between two accumulators: the tensor cores' fp32 accumulation
+            // truncates, so each chain of additions is kept half as long, and the two are
+            // added with round-to-nearest in the epilogue
+            const uint32_t dacc = tmem + (uint32_t)(kt & 1) * TN;
+#pragma unroll
+            for (int ks = 0; ks < TK / 8; ++ks) {
+                const uint32_t o = ks * 256;   // 8 K-columns = two 128-byte core matrices
+                const uint32_t first = (kt < 2 && ks == 0) ? 0u : 1u;
+                umma_tf32(dacc, umma_desc(a_hi + o, 128, 1024), umma_desc(b_hi + o, 128, 1024), idesc, first);
+                umma_tf32(dacc, umma_desc(a_hi + o, 128, 1024), umma_desc(b_lo + o, 128, 1024), idesc, 1u);
+                umma_tf32(dacc, umma_desc(a_lo + o, 128, 1024), umma_desc(b_hi + o, 128, 1024), idesc, 1u);
+            }
+            umma_commit(&mbar[st]);
+        }
+        issued[st] = 1;
+    }
+    // wait for every issued MMA (bounded), then read the accumulator
+    for (int s = 0; s < NSTAGE; ++s)
+        if (issued[s]) {
+            if (!mbar_wait(&mbar[s], phase[s])) ok = false;
+            phase[s] ^= 1;
+        }
+    tc_fence_after();
+    const bool all_ok = __syncthreads_and(ok);
+    if (all_ok) {
+        const int q = warp & 3, half = warp >> 2;
+        const int row = 32 * q + lane, gi = i0 + row;
+        float mx = 0.0f;
+#pragma unroll 1
+        for (int cch = 0; cch < 4; ++cch) {
+            const int col = 128 * half + 32 * cch;
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+            if (nkt > 1) {
+                float v2[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(TN + col), v2);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] += v2[e];
+            }
+            if (gi < S) {
+                float *dst = C + (size_t)gi * S + j0 + col;
+                if (j0 + col + 32 <= S) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, v[e]);
+                } else {
+                    for (int e = 0; e < 32; ++e)
+                        if (j0 + col + e < S) { dst[e] = v[e]; mx = fmaxf(mx, v[e]); }
+                }
+            }
+        }
+        if (gi < S) {
+            if (mx > 0.0f) atomicMax(&rmax_p[pnode * S + gi], __float_as_int(mx));
+            if (tn == 0 && half == 0) {
+                const int mr = mu_s[row];
+                rho_p[pnode * S + gi] = (mr == FA_INT_NONE) ? 0 : rho_c[lnode * S + gi] + mr;
+            }
+        }
+    } else if (tid == 0) {
+        atomicExch(err, FA_ROW_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace
+
+size_t fa_span_tc_smem(int S) { return (size_t)NSTAGE * STAGE_BYTES + (size_t)S * 8; }
+
+bool fa_span_tc_supported(int S) { return S >= 128 && (S % 4) == 0 && fa_span_tc_smem(S) <= 227 * 1024; }
+
+fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant_c, const int32_t *rho_c,
+                           const int32_t *rmax_c, int nc, const int32_t *mu, float *mant_p, int32_t *rho_p,
+                           int32_t *rmax_p, int32_t *err, cudaStream_t stream) {
+    const size_t smem = fa_span_tc_smem(S);
+    cudaError_t e = cudaFuncSetAttribute(k_span_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    const long tiles = (long)((S + TM - 1) / TM) * ((S + TN - 1) / TN);
+    const long grid = (long)B * nk * tiles;
+    k_span_tc<<<(unsigned)grid, NTHR, smem, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, nc, mu, mant_p, rho_p, rmax_p,
+                                                      err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    return FA_OK;
+}

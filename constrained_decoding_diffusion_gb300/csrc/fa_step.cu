@@ -33,7 +33,7 @@ struct Plan {
     int nk[18] = {0};
     size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, mu[18] = {0};
     size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, zsum = 0, zexp = 0;
-    size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0;
+    size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0;
     size_t total = 0;
 };
 
@@ -64,8 +64,9 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
         size_t o = p.rmax_hi;
         for (int k = 1; k <= p.K; ++k) { p.rmax[k] = o; o += (size_t)B * p.nk[k] * S * sizeof(int32_t); }
         p.leaf_done = p.rmax_hi + hi;          // ticket counter of the leaf blocks, cleared with them
-        p.rmax_hi_bytes = hi + sizeof(int32_t);
-        off = align256(p.rmax_hi + hi + sizeof(int32_t));
+        p.tc_err = p.leaf_done + sizeof(int32_t);  // timeout word of the tensor-core span products
+        p.rmax_hi_bytes = hi + 2 * sizeof(int32_t);
+        off = align256(p.rmax_hi + hi + 2 * sizeof(int32_t));
     }
     size_t bnd = (size_t)B * (size_t)(L + 1);
     p.z = take(bnd * sizeof(int32_t));
@@ -527,7 +528,8 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int
 __global__ void __launch_bounds__(kThreads) k_root(DevFA fa, int L, int K, int nK, const float *__restrict__ mant_root,
                                                  const int32_t *__restrict__ rho_root, uint64_t seed, uint64_t offset,
                                                  int32_t *z, float *am, int32_t *ae, float *bm, int32_t *be,
-                                                 float *zsum_ws, int32_t *zexp_ws, double *logZ, int32_t *status) {
+                                                 float *zsum_ws, int32_t *zexp_ws, double *logZ, int32_t *status,
+                                                 const int32_t *__restrict__ tc_err) {
     const int b = blockIdx.x, S = fa.S, s0 = fa.start;
     const float *row = mant_root + (size_t)b * nK * S * S + (size_t)s0 * S;
     const size_t bnd0 = (size_t)b * (L + 1);
@@ -545,7 +547,13 @@ __global__ void __launch_bounds__(kThreads) k_root(DevFA fa, int L, int K, int n
     tot = fa_warp_sum(tot);
     if (threadIdx.x == 0) {
         z[bnd0] = s0;
-        if (pick < 0 || !(tot > 0.0f)) {
+        if (tc_err && *tc_err) {
+            status[b] = FA_ROW_TIMEOUT;
+            logZ[b] = -INFINITY;
+            z[bnd0 + L] = s0;
+            zsum_ws[b] = 0.0f;
+            zexp_ws[b] = 0;
+        } else if (pick < 0 || !(tot > 0.0f)) {
             status[b] = FA_ROW_EMPTY;
             logZ[b] = -INFINITY;
             z[bnd0 + L] = s0;
@@ -764,7 +772,8 @@ __device__ void leaf_position(const DevFA &fa, int B, int L, const float *__rest
                               const int32_t *__restrict__ z, const float *__restrict__ am,
                               const int32_t *__restrict__ ae, const float *__restrict__ bm,
                               const int32_t *__restrict__ be, const float *__restrict__ zsum_ws,
-                              const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg, int32_t *status) {
+                              const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg, int32_t *status,
+                              const float *__restrict__ leaf) {
     const long gw = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (gw >= (long)B * L) return;
     const int b = (int)(gw / L), t = (int)(gw % L);
@@ -802,6 +811,7 @@ __device__ void leaf_position(const DevFA &fa, int B, int L, const float *__rest
         return;
     }
     const size_t ba = ((size_t)b * (L + 1) + t) * S, bb = ((size_t)b * (L + 1) + t + 1) * S;
+    // numerator: sum over the edges carrying v of alpha_{t-1}(src) beta_t(dst)
     fa_xacc x;
     x.init();
     for (int64_t j = fa.tok_off[v] + lane; j < fa.tok_off[v + 1]; j += 32) {
@@ -811,19 +821,41 @@ __device__ void leaf_position(const DevFA &fa, int B, int L, const float *__rest
         if (a > 0.0f && bv > 0.0f) x.add(a * bv, ae[ba + s] + be[bb + d]);
     }
     x.warp_reduce();
+    // local normaliser D_t = alpha_{t-1}^T M_t beta_t over the cells of M_t (equal to Z, and
+    // sharing alpha and beta with the numerator, so their errors cancel): the largest term
+    // exponent first, then the terms scaled to it
+    const float *Mt = leaf + pos * (size_t)S * S;
+    int emax = FA_INT_NONE;
+    for (int cell = lane; cell < fa.n_cells; cell += 32) {
+        const int s = fa.cell_src[cell], d = fa.cell_dst[cell];
+        const float a = am[ba + s], bv = bm[bb + d], mv = Mt[(size_t)s * S + d];
+        if (a > 0.0f && bv > 0.0f && mv > 0.0f) emax = max(emax, ae[ba + s] + be[bb + d] + fa_exponent(mv));
+    }
+    emax = fa_warp_max_int(emax);
+    float den = 0.0f;
+    if (emax != FA_INT_NONE)
+        for (int cell = lane; cell < fa.n_cells; cell += 32) {
+            const int s = fa.cell_src[cell], d = fa.cell_dst[cell];
+            const float a = am[ba + s], bv = bm[bb + d], mv = Mt[(size_t)s * S + d];
+            if (a > 0.0f && bv > 0.0f && mv > 0.0f) {
+                float mm;
+                int em;
+                fa_split(mv, mm, em);
+                den += a * bv * mm * fa_pow2(ae[ba + s] + be[bb + d] + em - emax);
+            }
+        }
+    den = fa_warp_sum(den);
     if (lane == 0) {
         tokens[pos] = v;
         float mo;
         int eo;
         x.normalised(mo, eo);
-        const float zs = zsum_ws[b];
         double mval = 0.0;
-        if (mo > 0.0f && zs > 0.0f)
-            mval = ldexp((double)__ldg(prow + v) * (double)mo / (double)zs, eo - zexp_ws[b]);
+        if (mo > 0.0f && den > 0.0f)
+            mval = ldexp((double)__ldg(prow + v) * (double)mo / (double)den, eo - emax);
         marg[pos] = (float)mval;
     }
 }
-
 
 __device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const int32_t *__restrict__ committed,
                          const int32_t *status, int32_t *out, int32_t *tokens, unsigned long long *skey);
@@ -838,8 +870,10 @@ __global__ void __launch_bounds__(kThreads) k_leaf_commit(DevFA fa, int B, int L
                                                         const float *__restrict__ zsum_ws,
                                                         const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg,
                                                         int32_t *status, int k, int lo, int hi, int32_t *commit_idx,
-                                                        unsigned long long *keys, int32_t *done) {
-    leaf_position(fa, B, L, probs, committed, seed, offset, z, am, ae, bm, be, zsum_ws, zexp_ws, tokens, marg, status);
+                                                        unsigned long long *keys, int32_t *done,
+                                                        const float *__restrict__ leaf) {
+    leaf_position(fa, B, L, probs, committed, seed, offset, z, am, ae, bm, be, zsum_ws, zexp_ws, tokens, marg, status,
+                  leaf);
     __shared__ int last;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -1045,6 +1079,13 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
         k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
                                            p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
         if ((st = launch_check("rowshift")) != FA_OK) return st;
+        if (fa_span_tc_supported(S)) {
+            g_launches.fetch_add(1, std::memory_order_relaxed);
+            st = fa_span_tc_level(S, B, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
+                                  p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]), I(p.tc_err), s);
+            if (st != FA_OK) return st;
+            continue;
+        }
         const long tiles = (S + GBN - 1) / GBN;
         const long g2 = (long)B * p.nk[kk] * tiles * tiles;
         k_gemm_simt<<<(unsigned)g2, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
@@ -1056,7 +1097,7 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
     stage_mark(2, s);
     k_root<<<B, kThreads, 0, s>>>(dev_view(aut), L, p.K, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), philox_seed,
                                   philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.zsum), I(p.zexp),
-                                  logZ, row_status);
+                                  logZ, row_status, I(p.tc_err));
     if ((st = launch_check("root")) != FA_OK) return st;
 
     // 4. top-down: midpoints and prefix/suffix messages, level K-1 .. 0
@@ -1083,7 +1124,7 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
     k_leaf_commit<<<(unsigned)((lw + kWarps - 1) / kWarps), kThreads, 0, s>>>(
         dev_view(aut), B, L, probs, committed, philox_seed, philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be),
         F(p.zsum), I(p.zexp), tokens, marg, row_status, k, commit_lo, commit_hi, commit_idx,
-        (unsigned long long *)(ws + p.keys), I(p.leaf_done));
+        (unsigned long long *)(ws + p.keys), I(p.leaf_done), F(p.mant[0]));
     st = launch_check("leaf and commit");
     stage_mark(4, s);
     return st;

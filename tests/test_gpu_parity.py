@@ -370,3 +370,20 @@ def test_step_long_sequence_global_topk(native):
     committed = np.full((1, L), -1, np.int32)
     res = run_step(native.fa_compile(fa), probs, committed, seed=4, offset=0, k=40)
     check_against_oracle(fa, o, probs, committed, res, 40)
+
+
+@pytest.mark.parametrize("S", [128, 300])
+def test_step_tensor_core_span_products(native, S):
+    """|S| >= 128 takes the tcgen05 3xTF32 span products; 300 leaves ragged 128x256 tiles."""
+    rng = np.random.default_rng(S)
+    fa = synth.random_dfa(S, 3000, 0.8, 12, seed=S)
+    o = oracle.OracleFA(fa)
+    aut = native.fa_compile(fa)
+    L = 24
+    probs = synth.gaussian_probs(rng, 2, L, 3000, 3.0)
+    committed = np.full((2, L), -1, np.int32)
+    x = synth.random_accepted_string(fa, L, rng)
+    idx = rng.choice(L, 8, replace=False)
+    committed[0, idx] = x[idx]
+    res = run_step(aut, probs, committed, seed=5, offset=1, k=4)
+    check_against_oracle(fa, o, probs, committed, res, 4)
