@@ -926,6 +926,16 @@ __device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const
     }
 }
 
+// committed[b, idx] = tokens[b, idx] for every idx >= 0 in commit_idx[b, :].
+__global__ void k_apply_commits(int B, int L, int k, const int32_t *__restrict__ commit_idx,
+                                const int32_t *__restrict__ tokens, int32_t *committed) {
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long)B * k) return;
+    const int b = (int)(i / k);
+    const int t = commit_idx[i];
+    if (t >= 0 && t < L) committed[(size_t)b * L + t] = tokens[(size_t)b * L + t];
+}
+
 // L = 0: the empty string is the only candidate.
 __global__ void k_empty_length(int start, const int32_t *accept_mask, int B, int k, double *logZ, int32_t *status,
                                int32_t *commit_idx) {
@@ -1158,4 +1168,14 @@ extern "C" fa_status fa_launch_count(uint64_t *n) {
     if (!n) { fa_set_error("fa_launch_count: NULL argument"); return FA_ERR_INVALID_ARG; }
     *n = g_launches.load(std::memory_order_relaxed);
     return FA_OK;
+}
+
+extern "C" fa_status fa_apply_commits(int32_t B, int32_t L, int32_t k, const int32_t *commit_idx, const int32_t *tokens,
+                                      int32_t *committed, fa_stream stream) {
+    if (B < 0 || L < 0 || k < 0) { fa_set_error("fa_apply_commits: B, L or k negative"); return FA_ERR_INVALID_ARG; }
+    if ((long)B * k == 0) return FA_OK;
+    if (!commit_idx || !tokens || !committed) { fa_set_error("fa_apply_commits: NULL buffer"); return FA_ERR_INVALID_ARG; }
+    const long n = (long)B * k;
+    k_apply_commits<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(B, L, k, commit_idx, tokens, committed);
+    return launch_check("apply commits");
 }

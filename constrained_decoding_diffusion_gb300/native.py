@@ -26,7 +26,7 @@ FA_ROW_OK, FA_ROW_EMPTY, FA_ROW_UNDERFLOW, FA_ROW_TIMEOUT = 0, 1, 2, 3
 
 # every entry point include/fa.h declares
 EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_workspace_bytes",
-           "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_noalloc",
+           "fa_transition_matrices", "fa_constrained_step", "fa_apply_commits", "fa_constrained_step_noalloc",
            "fa_profile_enable", "fa_profile_read",
            "fa_launch_count", "fa_last_error")
 N_STAGES = 4
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH):
     lib.fa_transition_matrices.restype = st
     lib.fa_constrained_step.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, sz, P, P, P, P, P, P]
     lib.fa_constrained_step.restype = st
+    lib.fa_apply_commits.argtypes = [i32, i32, i32, P, P, P, P]
+    lib.fa_apply_commits.restype = st
     lib.fa_constrained_step_noalloc.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, P, P, P, P, P]
     lib.fa_constrained_step_noalloc.restype = st
     lib.fa_profile_enable.argtypes = [i32]
@@ -192,6 +194,16 @@ def fa_constrained_step(aut: CompiledAutomaton, probs, committed, philox_seed: i
         _dev(logZ, torch.float64, "logZ", (B,)), _dev(marg, torch.float32, "marg", (B, L)),
         _dev(commit_idx, torch.int32, "commit_idx", (B, k)) if k > 0 else None,
         _dev(row_status, torch.int32, "row_status", (B,)), _stream_ptr(stream)))
+
+
+def fa_apply_commits(commit_idx, tokens, committed, stream=None):
+    """committed[b, t] = tokens[b, t] for every t in commit_idx[b] (t >= 0), on the device."""
+    import torch
+    B, L = committed.shape
+    k = commit_idx.shape[1]
+    _check(_lib.fa_apply_commits(B, L, k, _dev(commit_idx, torch.int32, "commit_idx", (B, k)),
+                                 _dev(tokens, torch.int32, "tokens", (B, L)),
+                                 _dev(committed, torch.int32, "committed", (B, L)), _stream_ptr(stream)))
 
 
 class ConstrainedStep:

@@ -188,6 +188,17 @@ fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int32_t L, con
                               int32_t *commit_idx, int32_t *row_status, fa_stream stream);
 
 /*
+ * fa_apply_commits -- the commit of a remasking schedule: committed[b, t] = tokens[b, t] for
+ * every t = commit_idx[b, i] >= 0 (i < k).  With fa_constrained_step this gives any
+ * schedule of the papernotes.org notes (key design 3) or the paperfeed.app summary
+ * ("Arbitrary schedules and NFAs"): parallel, block-wise (through the commit window) or
+ * fewer steps with larger k.  All arrays are device memory: commit_idx [B, k], tokens and
+ * committed [B, L].  Asynchronous on stream.  Errors: FA_ERR_INVALID_ARG, FA_ERR_CUDA.
+ */
+fa_status fa_apply_commits(int32_t B, int32_t L, int32_t k, const int32_t *commit_idx, const int32_t *tokens,
+                           int32_t *committed, fa_stream stream);
+
+/*
  * fa_constrained_step_noalloc -- fa_constrained_step for callers that cannot allocate.
  *
  * No counterpart in the paper: this is a deployment convenience.  Some callers may not
