@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="launch the step eagerly instead of a graph replay")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--length", type=int, default=None, help="override L (smaller profiling cases)")
     return ap.parse_args()
 
 
@@ -272,6 +273,10 @@ def run_native(args, rank, world, local):
     torch.cuda.set_device(local)
     native.load()
     w = synth.workload(args.workload)
+    if args.length is not None:
+        w.L = args.length
+        w.committed = np.ascontiguousarray(w.committed[:, :args.length])
+        w.window = min(w.window, args.length)
     masked = int((w.committed < 0).sum())
     aut = native.fa_compile(w.fa)
     if w.B * w.L * w.V <= (1 << 27):
