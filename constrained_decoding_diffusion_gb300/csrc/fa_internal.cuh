@@ -184,6 +184,7 @@ struct fa_xacc {
 
 // Tensor-core span products (fa_span_tc.cu).
 bool fa_span_tc_supported(int S);
+size_t fa_span_tc_image_bytes(int S, long products);
 fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant_c, const int32_t *rho_c,
                            const int32_t *rmax_c, int nc, const int32_t *mu, float *mant_p, int32_t *rho_p,
-                           int32_t *rmax_p, int32_t *err, cudaStream_t stream);
+                           int32_t *rmax_p, int32_t *err, void *img, cudaStream_t stream);

@@ -9,17 +9,22 @@
 // truncated to TF32, so hi*hi + hi*lo + lo*hi on the TF32 tensor cores (fp32 accumulation)
 // keeps fp32 accuracy ("3xTF32"); lo*lo is below fp32 rounding.
 //
-// Tile: 128 rows x 256 columns per CTA, K in tiles of 32, two shared-memory stages.  All 256
-// threads convert a stage (global fp32 -> prescale -> hi/lo -> canonical K-major
-// no-swizzle layout: 8-row x 16-byte core matrices, K-direction core stride 128 B, row-group
-// stride 1024 B); one thread issues the MMAs (M=128, N=256, K=8 each) and commits them to the
-// stage's mbarrier; the stage is rewritten only after that mbarrier completes.  The
-// accumulators (128 lanes x 2 x 256 fp32 columns of tensor memory; k-tiles alternate between
-// them) are read back by the 8 warps, each from its own 32-lane quarter, added, and written
-// row-major with the tile's row maxima.
+// Two kernels per tree level.  k_tc_prep converts every operand once: the left child, row
+// prescaled, and the right child are split into hi/lo and written as the exact images of the
+// shared-memory tiles the MMAs read (canonical K-major no-swizzle layout: 8-row x 16-byte
+// core matrices, K-direction core stride 128 B, row-group stride 1024 B; 128x32 left tiles,
+// 256x32 right tiles).  k_span_tc then runs a warp-specialised pipeline per 128x256 output
+// tile: one producer thread streams the tile images of each K step (4 bulk copies, 96 KB)
+// into one of two shared-memory stages, tracked by the stage's "full" mbarrier; one thread
+// issues the MMAs (M=128, N=256, K=8; hi*hi, hi*lo, lo*hi) and commits them to the stage's
+// "empty" mbarrier, which releases the stage to the producer.  K steps alternate between two
+// tensor-memory accumulators (128 lanes x 256 fp32 columns each): the tensor cores' fp32
+// accumulation truncates, so each chain of additions is kept half as long and the two are
+// added with round-to-nearest in the epilogue, where the 8 warps read tensor memory (each
+// from its own 32-lane quarter) and write the tile row-major with its row maxima.
 //
-// Every mbarrier wait is bounded; a wait that runs out records FA_ROW_TIMEOUT in the error
-// word, waits (bounded) for the MMAs already issued, releases tensor memory and returns.
+// Every mbarrier wait is bounded (about a second); a wait that runs out records
+// FA_ROW_TIMEOUT in the error word, tensor memory is released and the CTA returns.
 #include <stdint.h>
 
 #include "fa_internal.cuh"
@@ -33,6 +38,8 @@ constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 96 KB
 constexpr int NSTAGE = 2;
 constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 constexpr long long kSpinCycles = 2000000000LL;
+constexpr int A_IMG = 2 * A_BYTES;          // hi + lo image of one 128x32 left tile
+constexpr int B_IMG = 2 * B_BYTES;          // hi + lo image of one 256x32 right tile
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -72,6 +79,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     while (!mbar_try_wait(bar, parity))
         if (clock64() - t0 > kSpinCycles) return false;
     return true;
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// one-dimensional bulk copy global -> shared, completing bytes on the mbarrier
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -117,17 +136,87 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
     lo = x - hi;
 }
 
+// Operand images for one level.  Blocks: (product, side, tile); side 0 = left operand
+// (prescaled by 2^(rhoR[m] - mu[row]), 128-row tiles), side 1 = right operand (256-column
+// tiles, transposed to K-major).  Each block converts its tile for every K step.
+__global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, const float *__restrict__ mant_c,
+                                                const int32_t *__restrict__ rho_c,
+                                                const int32_t *__restrict__ rmax_c, int nc,
+                                                const int32_t *__restrict__ mu, unsigned char *img) {
+    const int tid = threadIdx.x;
+    const int tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN, nkt = (S + TK - 1) / TK;
+    const int per = tiles_m + tiles_n;
+    const long flat = blockIdx.x;
+    const int w = (int)(flat % per);
+    const long bn = flat / per;
+    const int node = (int)(bn % nk), b = (int)(bn / nk);
+    if (((2 * node + 1) << (k - 1)) >= L) return;     // a copy, no product
+    const size_t SS = (size_t)S * S;
+    const size_t pnode = (size_t)b * nk + node;
+    const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
+    const size_t per_prod_a = (size_t)tiles_m * nkt * A_IMG, per_prod_b = (size_t)tiles_n * nkt * B_IMG;
+    const size_t total_a = (size_t)gridDim.x / per * per_prod_a;        // all products' left images first
+    if (w < tiles_m) {
+        const int tm = w, row = tid >> 1, gi = tm * TM + row;
+        const float *A = mant_c + lnode * SS;
+        const int32_t *rhoR = rho_c + rnode * S, *rmaxR = rmax_c + rnode * S;
+        const int mrow = gi < S ? mu[pnode * S + gi] : FA_INT_NONE;
+        unsigned char *base = img + (size_t)bn * per_prod_a + (size_t)tm * nkt * A_IMG;
+        for (int kt = 0; kt < nkt; ++kt) {
+            unsigned char *t = base + (size_t)kt * A_IMG;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int kk = (tid & 1) * 16 + 4 * q, m0 = kt * TK + kk;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gi < S && m0 < S) v = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gi * S + m0));
+                float x[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = m0 + e;
+                    float y = 0.0f;
+                    if (x[e] > 0.0f && mrow != FA_INT_NONE && m < S && __ldg(rmaxR + m) > 0)
+                        y = fa_mul_pow2(x[e], __ldg(rhoR + m) - mrow);
+                    split_tf32(y, hi[e], lo[e]);
+                }
+                const uint32_t off = kmaj_off(row, kk);
+                *reinterpret_cast<float4 *>(t + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4 *>(t + A_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+    } else {
+        const int tn = w - tiles_m, n = tid, gj = tn * TN + n;
+        const float *Bm = mant_c + rnode * SS;
+        unsigned char *base = img + total_a + (size_t)bn * per_prod_b + (size_t)tn * nkt * B_IMG;
+        for (int kt = 0; kt < nkt; ++kt) {
+            unsigned char *t = base + (size_t)kt * B_IMG;
+#pragma unroll
+            for (int g = 0; g < TK / 4; ++g) {
+                float x[4], hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = kt * TK + 4 * g + e;
+                    x[e] = (gj < S && m < S) ? __ldg(Bm + (size_t)m * S + gj) : 0.0f;
+                    split_tf32(x[e], hi[e], lo[e]);
+                }
+                const uint32_t off = kmaj_off(n, 4 * g);
+                *reinterpret_cast<float4 *>(t + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4 *>(t + B_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                     const int32_t *__restrict__ rho_c,
                                                     const int32_t *__restrict__ rmax_c, int nc,
-                                                    const int32_t *__restrict__ mu, float *mant_p, int32_t *rho_p,
-                                                    int32_t *rmax_p, int32_t *err) {
+                                                    const int32_t *__restrict__ mu, const unsigned char *__restrict__ img,
+                                                    float *mant_p, int32_t *rho_p, int32_t *rmax_p, int32_t *err) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ uint64_t mbar[NSTAGE];
+    __shared__ uint64_t full[NSTAGE], empty[NSTAGE], done;
     __shared__ uint32_t tmem_base_s;
-    __shared__ int mu_s[TM];
+    __shared__ int fail_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN;
+    const int tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN, nkt = (S + TK - 1) / TK;
     const long flat = blockIdx.x;
     const int tn = (int)(flat % tiles_n), tm = (int)((flat / tiles_n) % tiles_m);
     const long bn = flat / ((long)tiles_n * tiles_m);
@@ -135,7 +224,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
     const int i0 = tm * TM, j0 = tn * TN;
     const size_t SS = (size_t)S * S;
     const size_t pnode = (size_t)b * nk + node;
-    const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
+    const size_t lnode = (size_t)b * nc + 2 * node;
     const float *A = mant_c + lnode * SS;
     float *C = mant_p + pnode * SS;
     if (((2 * node + 1) << (k - 1)) >= L) {           // right child is padding: C = A_L
@@ -150,16 +239,14 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
             }
         return;
     }
-    const float *Bm = mant_c + rnode * SS;
-    const int32_t *rhoR = rho_c + rnode * S;
-    const int32_t *rmaxR = rmax_c + rnode * S;
-    // shared memory: NSTAGE x [A_hi | A_lo | B_hi | B_lo], then rhoR and rmaxR for every m
-    int *rhoR_s = reinterpret_cast<int *>(smem + NSTAGE * STAGE_BYTES);
-    int *rmaxR_s = rhoR_s + S;
-    for (int m = tid; m < S; m += NTHR) { rhoR_s[m] = rhoR[m]; rmaxR_s[m] = rmaxR[m]; }
-    for (int r = tid; r < TM; r += NTHR) mu_s[r] = (i0 + r < S) ? mu[pnode * S + i0 + r] : FA_INT_NONE;
+    const size_t per_prod_a = (size_t)tiles_m * nkt * A_IMG, per_prod_b = (size_t)tiles_n * nkt * B_IMG;
+    const size_t n_prod_slots = (size_t)gridDim.x / ((size_t)tiles_m * tiles_n);
+    const unsigned char *a_img = img + (size_t)bn * per_prod_a + (size_t)tm * nkt * A_IMG;
+    const unsigned char *b_img = img + n_prod_slots * per_prod_a + (size_t)bn * per_prod_b + (size_t)tn * nkt * B_IMG;
     if (tid == 0) {
-        for (int s = 0; s < NSTAGE; ++s) mbar_init(&mbar[s], 1);
+        for (int s2 = 0; s2 < NSTAGE; ++s2) { mbar_init(&full[s2], 1); mbar_init(&empty[s2], 1); }
+        mbar_init(&done, 1);
+        fail_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -172,74 +259,26 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
-    const uint32_t idesc = umma_idesc_tf32();
-    const int nkt = (S + TK - 1) / TK;
-    bool ok = true;
-    uint32_t phase[NSTAGE] = {0, 0};
-    int issued[NSTAGE] = {0, 0};
-
-    for (int kt = 0; kt < nkt; ++kt) {
-        const int st = kt % NSTAGE;
-        unsigned char *stage = smem + st * STAGE_BYTES;
-        // the MMAs that last read this stage must be complete before it is rewritten
-        if (issued[st]) {
-            if (!mbar_wait(&mbar[st], phase[st])) ok = false;
-            phase[st] ^= 1;
-            issued[st] = 0;
+    if (tid == 0) {
+        // producer: stream the operand images of every K step into the stages
+        for (int kt = 0; kt < nkt; ++kt) {
+            const int st = kt % NSTAGE;
+            if (kt >= NSTAGE && !mbar_wait(&empty[st], ((kt / NSTAGE) - 1) & 1)) { atomicExch(&fail_s, 1); break; }
+            unsigned char *stage = smem + st * STAGE_BYTES;
+            mbar_expect_tx(&full[st], STAGE_BYTES);
+            bulk_g2s(stage, a_img + (size_t)kt * A_IMG, A_IMG, &full[st]);
+            bulk_g2s(stage + A_IMG, b_img + (size_t)kt * B_IMG, B_IMG, &full[st]);
         }
-        if (!__syncthreads_and(ok)) { ok = false; break; }
-        const int k0 = kt * TK;
-        // A: 128 rows x 32 k; thread -> (row = tid / 2, k half = tid % 2), 4 float4 loads
-        {
-            const int row = tid >> 1, kh = (tid & 1) * 16;
-            const int gi = i0 + row;
-            const int mrow = mu_s[row];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int kk = kh + 4 * q;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (gi < S && k0 + kk < S) v = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gi * S + k0 + kk));
-                float x[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = k0 + kk + e;
-                    float y = 0.0f;
-                    if (x[e] > 0.0f && mrow != FA_INT_NONE && m < S && rmaxR_s[m] > 0)
-                        y = fa_mul_pow2(x[e], rhoR_s[m] - mrow);
-                    split_tf32(y, hi[e], lo[e]);
-                }
-                const uint32_t off = kmaj_off(row, kk);
-                *reinterpret_cast<float4 *>(stage + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4 *>(stage + A_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            }
-        }
-        // B: 256 columns n x 32 k; thread -> column n = tid, 8 groups of 4 k
-        {
-            const int n = tid, gj = j0 + n;
-#pragma unroll
-            for (int g = 0; g < TK / 4; ++g) {
-                float x[4], hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = k0 + 4 * g + e;
-                    x[e] = (gj < S && m < S) ? __ldg(Bm + (size_t)m * S + gj) : 0.0f;
-                    split_tf32(x[e], hi[e], lo[e]);
-                }
-                const uint32_t off = kmaj_off(n, 4 * g);
-                *reinterpret_cast<float4 *>(stage + 2 * A_BYTES + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4 *>(stage + 2 * A_BYTES + B_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            }
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+    } else if (tid == 32) {
+        // MMA issuer
+        const uint32_t idesc = umma_idesc_tf32();
+        int kt = 0;
+        for (; kt < nkt; ++kt) {
+            const int st = kt % NSTAGE;
+            if (!mbar_wait(&full[st], (kt / NSTAGE) & 1)) { atomicExch(&fail_s, 1); break; }
             tc_fence_after();
-            const uint32_t a_hi = smem_u32(stage), a_lo = a_hi + A_BYTES;
-            const uint32_t b_hi = a_hi + 2 * A_BYTES, b_lo = b_hi + B_BYTES;
-#pragma unroll
-            // k-tiles alternate between two accumulators: the tensor cores' fp32 accumulation
-            // truncates, so each chain of additions is kept half as long, and the two are
-            // added with round-to-nearest in the epilogue
+            const uint32_t a_hi = smem_u32(smem + st * STAGE_BYTES), a_lo = a_hi + A_BYTES;
+            const uint32_t b_hi = a_hi + A_IMG, b_lo = b_hi + B_BYTES;
             const uint32_t dacc = tmem + (uint32_t)(kt & 1) * TN;
 #pragma unroll
             for (int ks = 0; ks < TK / 8; ++ks) {
@@ -249,19 +288,15 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
                 umma_tf32(dacc, umma_desc(a_hi + o, 128, 1024), umma_desc(b_lo + o, 128, 1024), idesc, 1u);
                 umma_tf32(dacc, umma_desc(a_lo + o, 128, 1024), umma_desc(b_hi + o, 128, 1024), idesc, 1u);
             }
-            umma_commit(&mbar[st]);
+            umma_commit(&empty[st]);
         }
-        issued[st] = 1;
+        umma_commit(&done);
     }
-    // wait for every issued MMA (bounded), then read the accumulator
-    for (int s = 0; s < NSTAGE; ++s)
-        if (issued[s]) {
-            if (!mbar_wait(&mbar[s], phase[s])) ok = false;
-            phase[s] ^= 1;
-        }
+    // everyone: wait for the last MMAs, then read the accumulators
+    if (!mbar_wait(&done, 0)) atomicExch(&fail_s, 1);
     tc_fence_after();
-    const bool all_ok = __syncthreads_and(ok);
-    if (all_ok) {
+    __syncthreads();
+    if (!fail_s) {
         const int q = warp & 3, half = warp >> 2;
         const int row = 32 * q + lane, gi = i0 + row;
         float mx = 0.0f;
@@ -293,7 +328,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
         if (gi < S) {
             if (mx > 0.0f) atomicMax(&rmax_p[pnode * S + gi], __float_as_int(mx));
             if (tn == 0 && half == 0) {
-                const int mr = mu_s[row];
+                const int mr = mu[pnode * S + gi];
                 rho_p[pnode * S + gi] = (mr == FA_INT_NONE) ? 0 : rho_c[lnode * S + gi] + mr;
             }
         }
@@ -310,20 +345,29 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
 
 }  // namespace
 
-size_t fa_span_tc_smem(int S) { return (size_t)NSTAGE * STAGE_BYTES + (size_t)S * 8; }
+size_t fa_span_tc_smem(int S) { (void)S; return (size_t)NSTAGE * STAGE_BYTES; }
 
-bool fa_span_tc_supported(int S) { return S >= 128 && (S % 4) == 0 && fa_span_tc_smem(S) <= 227 * 1024; }
+bool fa_span_tc_supported(int S) { return S >= 128 && (S % 4) == 0; }
+
+size_t fa_span_tc_image_bytes(int S, long products) {
+    const size_t tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN, nkt = (S + TK - 1) / TK;
+    return (size_t)products * nkt * (tiles_m * A_IMG + tiles_n * B_IMG);
+}
 
 fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant_c, const int32_t *rho_c,
                            const int32_t *rmax_c, int nc, const int32_t *mu, float *mant_p, int32_t *rho_p,
-                           int32_t *rmax_p, int32_t *err, cudaStream_t stream) {
+                           int32_t *rmax_p, int32_t *err, void *img, cudaStream_t stream) {
     const size_t smem = fa_span_tc_smem(S);
     cudaError_t e = cudaFuncSetAttribute(k_span_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
-    const long tiles = (long)((S + TM - 1) / TM) * ((S + TN - 1) / TN);
-    const long grid = (long)B * nk * tiles;
-    k_span_tc<<<(unsigned)grid, NTHR, smem, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, nc, mu, mant_p, rho_p, rmax_p,
-                                                      err);
+    const long tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN;
+    k_tc_prep<<<(unsigned)((long)B * nk * (tiles_m + tiles_n)), NTHR, 0, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, nc,
+                                                                                  mu, (unsigned char *)img);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { fa_set_error(std::string("operand images (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    const long grid = (long)B * nk * tiles_m * tiles_n;
+    k_span_tc<<<(unsigned)grid, NTHR, smem, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, nc, mu,
+                                                      (const unsigned char *)img, mant_p, rho_p, rmax_p, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     return FA_OK;

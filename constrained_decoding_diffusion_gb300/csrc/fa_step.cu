@@ -33,7 +33,7 @@ struct Plan {
     int nk[18] = {0};
     size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, mu[18] = {0};
     size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, zsum = 0, zexp = 0;
-    size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0;
+    size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0, img = 0;
     size_t total = 0;
 };
 
@@ -75,6 +75,8 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
     p.bm = take(bnd * S * sizeof(float));
     p.be = take(bnd * S * sizeof(int32_t));
     p.keys = take((size_t)B * (size_t)L * sizeof(unsigned long long));
+    // tensor-core operand images, sized for the level with the most node slots (level 1)
+    if (fa_span_tc_supported(a->S) && p.K >= 1) p.img = take(fa_span_tc_image_bytes(a->S, (long)B * p.nk[1]));
     p.zsum = take((size_t)B * sizeof(float));
     p.zexp = take((size_t)B * sizeof(int32_t));
     p.total = off;
@@ -1090,9 +1092,10 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
                                            p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
         if ((st = launch_check("rowshift")) != FA_OK) return st;
         if (fa_span_tc_supported(S)) {
-            g_launches.fetch_add(1, std::memory_order_relaxed);
+            g_launches.fetch_add(2, std::memory_order_relaxed);
             st = fa_span_tc_level(S, B, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
-                                  p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]), I(p.tc_err), s);
+                                  p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]), I(p.tc_err),
+                                  ws + p.img, s);
             if (st != FA_OK) return st;
             continue;
         }
