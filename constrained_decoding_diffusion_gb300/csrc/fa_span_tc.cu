@@ -39,6 +39,7 @@ constexpr int NSTAGE = 2;
 constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 constexpr long long kSpinCycles = 2000000000LL;
 constexpr int A_IMG = 2 * A_BYTES;          // hi + lo image of one 128x32 left tile
+constexpr int PREP_KT = 8;                  // K steps converted per k_tc_prep block
 constexpr int B_IMG = 2 * B_BYTES;          // hi + lo image of one 256x32 right tile
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -136,9 +137,9 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
     lo = x - hi;
 }
 
-// Operand images for one level.  Blocks: (product, side, tile); side 0 = left operand
-// (prescaled by 2^(rhoR[m] - mu[row]), 128-row tiles), side 1 = right operand (256-column
-// tiles, transposed to K-major).  Each block converts its tile for every K step.
+// Operand images for one level.  Blocks: (product, side, tile, chunk of PREP_KT K steps);
+// side 0 = left operand (prescaled by 2^(rhoR[m] - mu[row]), 128-row tiles), side 1 = right
+// operand (256-column tiles, transposed to K-major).
 __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                 const int32_t *__restrict__ rho_c,
                                                 const int32_t *__restrict__ rmax_c, int nc,
@@ -146,23 +147,26 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
     const int tid = threadIdx.x;
     const int tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN, nkt = (S + TK - 1) / TK;
     const int per = tiles_m + tiles_n;
-    const long flat = blockIdx.x;
+    const int kch = (nkt + PREP_KT - 1) / PREP_KT;                 // K-step chunks per tile
+    const int kc = blockIdx.x % kch;
+    const long flat = blockIdx.x / kch;
     const int w = (int)(flat % per);
     const long bn = flat / per;
+    const int kt0 = kc * PREP_KT, kt1 = min(nkt, kt0 + PREP_KT);
     const int node = (int)(bn % nk), b = (int)(bn / nk);
     if (((2 * node + 1) << (k - 1)) >= L) return;     // a copy, no product
     const size_t SS = (size_t)S * S;
     const size_t pnode = (size_t)b * nk + node;
     const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
     const size_t per_prod_a = (size_t)tiles_m * nkt * A_IMG, per_prod_b = (size_t)tiles_n * nkt * B_IMG;
-    const size_t total_a = (size_t)gridDim.x / per * per_prod_a;        // all products' left images first
+    const size_t total_a = (size_t)gridDim.x / ((size_t)per * kch) * per_prod_a;  // left images come first
     if (w < tiles_m) {
         const int tm = w, row = tid >> 1, gi = tm * TM + row;
         const float *A = mant_c + lnode * SS;
         const int32_t *rhoR = rho_c + rnode * S, *rmaxR = rmax_c + rnode * S;
         const int mrow = gi < S ? mu[pnode * S + gi] : FA_INT_NONE;
         unsigned char *base = img + (size_t)bn * per_prod_a + (size_t)tm * nkt * A_IMG;
-        for (int kt = 0; kt < nkt; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
             unsigned char *t = base + (size_t)kt * A_IMG;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -187,7 +191,7 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
         const int tn = w - tiles_m, n = tid, gj = tn * TN + n;
         const float *Bm = mant_c + rnode * SS;
         unsigned char *base = img + total_a + (size_t)bn * per_prod_b + (size_t)tn * nkt * B_IMG;
-        for (int kt = 0; kt < nkt; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
             unsigned char *t = base + (size_t)kt * B_IMG;
 #pragma unroll
             for (int g = 0; g < TK / 4; ++g) {
@@ -361,7 +365,8 @@ fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant
     cudaError_t e = cudaFuncSetAttribute(k_span_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     const long tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN;
-    k_tc_prep<<<(unsigned)((long)B * nk * (tiles_m + tiles_n)), NTHR, 0, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, nc,
+    const long kch = ((S + TK - 1) / TK + PREP_KT - 1) / PREP_KT;
+    k_tc_prep<<<(unsigned)((long)B * nk * (tiles_m + tiles_n) * kch), NTHR, 0, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, nc,
                                                                                   mu, (unsigned char *)img);
     e = cudaGetLastError();
     if (e != cudaSuccess) { fa_set_error(std::string("operand images (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
