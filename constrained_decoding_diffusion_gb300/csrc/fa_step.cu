@@ -63,10 +63,10 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
     {
         size_t o = p.rmax_hi;
         for (int k = 1; k <= p.K; ++k) { p.rmax[k] = o; o += (size_t)B * p.nk[k] * S * sizeof(int32_t); }
-        p.leaf_done = p.rmax_hi + hi;          // ticket counter of the leaf blocks, cleared with them
-        p.tc_err = p.leaf_done + sizeof(int32_t);  // timeout word of the tensor-core span products
-        p.rmax_hi_bytes = hi + 2 * sizeof(int32_t);
-        off = align256(p.rmax_hi + hi + 2 * sizeof(int32_t));
+        p.tc_err = p.rmax_hi + hi;             // timeout word of the tensor-core span products
+        p.leaf_done = p.tc_err + sizeof(int32_t);  // per-sequence ticket counters of the leaf blocks
+        p.rmax_hi_bytes = hi + (1 + (size_t)B) * sizeof(int32_t);
+        off = align256(p.rmax_hi + p.rmax_hi_bytes);
     }
     size_t bnd = (size_t)B * (size_t)(L + 1);
     p.z = take(bnd * sizeof(int32_t));
@@ -767,128 +767,219 @@ __global__ void __launch_bounds__(kThreads) k_topdown(TopdownArgs a) {
 // Token at each position: committed positions echo their token; a masked position draws
 // v ~ w_t(v) over the tokens of the edges z_{t-1} -> z_t (paperfeed.app: all tokens emit in
 // parallel at the leaves), then its constrained marginal
-//   p(x_t = v) = w_t(v) sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / Z
-// (papernotes.org key design 3).  One warp per position.
-__device__ void leaf_position(const DevFA &fa, int B, int L, const float *__restrict__ probs,
+//   p(x_t = v) = w_t(v) sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / D_t
+// (papernotes.org key design 3), D_t = alpha_{t-1}^T M_t beta_t the local normaliser (equal
+// to Z, and sharing alpha and beta with the numerator, so their errors cancel).
+//
+// One block per position.  The three reductions of a masked position (the normaliser over
+// the cells of M_t, the draw over the cell's tokens, the numerator over the token's
+// incidences) are spread over all threads, so that a position costs a few dependent memory
+// round trips instead of hundreds.
+constexpr int kLeafThreads = 256;
+constexpr int kLeafWarps = kLeafThreads / 32;
+constexpr int kLeafStageStates = 2048;  // alpha/beta rows staged in shared memory up to this |S|
+
+struct LeafShared {
+    float wm[kLeafWarps];
+    int we[kLeafWarps];
+    float wsum[kLeafWarps];
+    float xm;
+    int xe;
+    int cell, pick_thread, last_thread, v, ok;
+    int last;
+};
+
+// Merge every thread's accumulator; the result lands in sh.xm / sh.xe (mantissa, exponent).
+__device__ void block_xacc(fa_xacc x, LeafShared &sh) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    x.warp_reduce();
+    if (lane == 0) { sh.wm[w] = x.acc; sh.we[w] = x.E; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        fa_xacc y;
+        y.init();
+        for (int i = 0; i < kLeafWarps; ++i) y.merge(sh.wm[i], sh.we[i]);
+        y.normalised(sh.xm, sh.xe);
+    }
+    __syncthreads();
+}
+
+// Inclusive scan of one value per thread over the block (thread order); returns this
+// thread's inclusive prefix and the block total in *total.
+__device__ float block_scan(float x, LeafShared &sh, float *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh.wsum[w] = incl;
+    __syncthreads();
+    float before = 0.0f, all = 0.0f;
+    for (int i = 0; i < kLeafWarps; ++i) {
+        if (i < w) before += sh.wsum[i];
+        all += sh.wsum[i];
+    }
+    __syncthreads();
+    *total = all;
+    return before + incl;
+}
+
+__device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float *__restrict__ probs,
                               const int32_t *__restrict__ committed, uint64_t seed, uint64_t offset,
                               const int32_t *__restrict__ z, const float *__restrict__ am,
                               const int32_t *__restrict__ ae, const float *__restrict__ bm,
-                              const int32_t *__restrict__ be, const float *__restrict__ zsum_ws,
-                              const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg, int32_t *status,
-                              const float *__restrict__ leaf) {
-    const long gw = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (gw >= (long)B * L) return;
-    const int b = (int)(gw / L), t = (int)(gw % L);
-    const int lane = threadIdx.x & 31;
+                              const int32_t *__restrict__ be, int32_t *tokens, float *marg, int32_t *status,
+                              const float *__restrict__ leaf, LeafShared &sh, float *stage) {
+    const int tid = threadIdx.x;
     const size_t pos = (size_t)b * L + t;
     const int c = committed[pos];
     if (c >= 0) {
-        if (lane == 0) { tokens[pos] = c; marg[pos] = 1.0f; }
-        return;
+        if (tid == 0) { tokens[pos] = c; marg[pos] = 1.0f; }
+        return true;
     }
-    if (__shfl_sync(0xffffffffu, status[b], 0) != FA_ROW_OK) {
-        if (lane == 0) { tokens[pos] = -1; marg[pos] = 0.0f; }
-        return;
+    // one read of the status for the whole block (another block of the sequence may change it)
+    if (tid == 0) { sh.cell = -1; sh.pick_thread = INT_MAX; sh.last_thread = -1; sh.v = -1; sh.ok = status[b] == FA_ROW_OK; }
+    __syncthreads();
+    if (!sh.ok) {
+        if (tid == 0) { tokens[pos] = -1; marg[pos] = 0.0f; }
+        return true;
     }
     const int S = fa.S;
     const int32_t *zb = z + (size_t)b * (L + 1);
     const int zp = zb[t], zn = zb[t + 1];
-    int lo = fa.row_cell_off[zp], hi = fa.row_cell_off[zp + 1];
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (fa.cell_dst[mid] < zn) lo = mid + 1; else hi = mid;
-    }
-    const bool found = lo < fa.row_cell_off[zp + 1] && fa.cell_dst[lo] == zn;
-    int v = -1;
-    const float *prow = probs + pos * (size_t)fa.V;
-    if (found) {
-        const int64_t a0 = fa.cell_off[lo];
-        const int n = (int)(fa.cell_off[lo + 1] - a0);
-        const float u = fa_uniform(seed, offset, (uint32_t)t, (uint32_t)b, FA_RNG_LEAF);
-        const int pick = warp_categorical(n, u, [&](int i) { return __ldg(prow + fa.cell_tok[a0 + i]); });
-        if (pick >= 0) v = fa.cell_tok[a0 + pick];
-    }
-    if (v < 0) {
-        if (lane == 0) { status[b] = FA_ROW_UNDERFLOW; tokens[pos] = -1; marg[pos] = 0.0f; }
-        return;
-    }
     const size_t ba = ((size_t)b * (L + 1) + t) * S, bb = ((size_t)b * (L + 1) + t + 1) * S;
+    // the cell z_{t-1} -> z_t (one pass over the source's cells) and the two messages
+    const float *a_m = am + ba, *b_m = bm + bb;
+    const int32_t *a_e = ae + ba, *b_e = be + bb;
+    if (stage) {
+        float *sam = stage, *sbm = stage + S;
+        int32_t *sae = (int32_t *)(stage + 2 * S), *sbe = (int32_t *)(stage + 3 * S);
+        for (int s = tid; s < S; s += kLeafThreads) {
+            sam[s] = a_m[s]; sae[s] = a_e[s]; sbm[s] = b_m[s]; sbe[s] = b_e[s];
+        }
+        a_m = sam; b_m = sbm; a_e = sae; b_e = sbe;
+    }
+    __syncthreads();
+    for (int i = fa.row_cell_off[zp] + tid; i < fa.row_cell_off[zp + 1]; i += kLeafThreads)
+        if (fa.cell_dst[i] == zn) sh.cell = i;  // at most one cell per (src, dst)
+    __syncthreads();
+    const int cell = sh.cell;
+
+    // the draw, first half: this thread's share of the cell's tokens (i = tid, tid + T, ...),
+    // taken in thread order for the inverse CDF
+    const float *prow = probs + pos * (size_t)fa.V;
+    int64_t a0 = 0;
+    int n = 0;
+    if (cell >= 0) { a0 = fa.cell_off[cell]; n = (int)(fa.cell_off[cell + 1] - a0); }
+    float own = 0.0f;
+    for (int i = tid; i < n; i += kLeafThreads) own += __ldg(prow + fa.cell_tok[a0 + i]);
+
+    // the normaliser over the cells of M_t
+    const float *Mt = leaf + pos * (size_t)S * S;
+    fa_xacc dx;
+    dx.init();
+#pragma unroll 4
+    for (int q = tid; q < fa.n_cells; q += kLeafThreads) {
+        const int s = fa.cell_src[q], d = fa.cell_dst[q];
+        const float a = a_m[s], bv = b_m[d], mv = __ldg(Mt + (size_t)s * S + d);
+        if (a > 0.0f && bv > 0.0f && mv > 0.0f) {
+            float mm;
+            int em;
+            fa_split(mv, mm, em);
+            dx.add(a * bv * mm, a_e[s] + b_e[d] + em);
+        }
+    }
+
+    float total;
+    const float incl = block_scan(own, sh, &total);
+    block_xacc(dx, sh);
+    const float den_m = sh.xm;
+    const int den_e = sh.xe;
+    if (!(total > 0.0f)) {
+        if (tid == 0) { status[b] = FA_ROW_UNDERFLOW; tokens[pos] = -1; marg[pos] = 0.0f; }
+        return false;
+    }
+    const float u = fa_uniform(seed, offset, (uint32_t)t, (uint32_t)b, FA_RNG_LEAF);
+    const float target = u * total;
+    if (own > 0.0f) {
+        if (incl > target) atomicMin(&sh.pick_thread, tid);
+        atomicMax(&sh.last_thread, tid);
+    }
+    __syncthreads();
+    // the draw, second half: the first thread whose prefix passes the target walks its share
+    // (a rounding shortfall falls back to the last positive token)
+    const int who = sh.pick_thread != INT_MAX ? sh.pick_thread : sh.last_thread;
+    if (tid == who) {
+        float run = incl - own;
+        int pick = -1, lastpos = -1;
+        for (int i = tid; i < n; i += kLeafThreads) {
+            const float w = __ldg(prow + fa.cell_tok[a0 + i]);
+            if (w > 0.0f) {
+                lastpos = i;
+                run += w;
+                if (run > target) { pick = i; break; }
+            }
+        }
+        if (pick < 0) pick = lastpos;
+        sh.v = pick >= 0 ? fa.cell_tok[a0 + pick] : -1;
+    }
+    __syncthreads();
+    const int v = sh.v;
+    if (v < 0) {
+        if (tid == 0) { status[b] = FA_ROW_UNDERFLOW; tokens[pos] = -1; marg[pos] = 0.0f; }
+        return false;
+    }
     // numerator: sum over the edges carrying v of alpha_{t-1}(src) beta_t(dst)
     fa_xacc x;
     x.init();
-    for (int64_t j = fa.tok_off[v] + lane; j < fa.tok_off[v + 1]; j += 32) {
+    for (int64_t j = fa.tok_off[v] + tid; j < fa.tok_off[v + 1]; j += kLeafThreads) {
         const int e = fa.tok_edges[j];
         const int s = fa.edge_src[e], d = fa.edge_dst[e];
-        const float a = am[ba + s], bv = bm[bb + d];
-        if (a > 0.0f && bv > 0.0f) x.add(a * bv, ae[ba + s] + be[bb + d]);
+        const float a = a_m[s], bv = b_m[d];
+        if (a > 0.0f && bv > 0.0f) x.add(a * bv, a_e[s] + b_e[d]);
     }
-    x.warp_reduce();
-    // local normaliser D_t = alpha_{t-1}^T M_t beta_t over the cells of M_t (equal to Z, and
-    // sharing alpha and beta with the numerator, so their errors cancel): the largest term
-    // exponent first, then the terms scaled to it
-    const float *Mt = leaf + pos * (size_t)S * S;
-    int emax = FA_INT_NONE;
-    for (int cell = lane; cell < fa.n_cells; cell += 32) {
-        const int s = fa.cell_src[cell], d = fa.cell_dst[cell];
-        const float a = am[ba + s], bv = bm[bb + d], mv = Mt[(size_t)s * S + d];
-        if (a > 0.0f && bv > 0.0f && mv > 0.0f) emax = max(emax, ae[ba + s] + be[bb + d] + fa_exponent(mv));
-    }
-    emax = fa_warp_max_int(emax);
-    float den = 0.0f;
-    if (emax != FA_INT_NONE)
-        for (int cell = lane; cell < fa.n_cells; cell += 32) {
-            const int s = fa.cell_src[cell], d = fa.cell_dst[cell];
-            const float a = am[ba + s], bv = bm[bb + d], mv = Mt[(size_t)s * S + d];
-            if (a > 0.0f && bv > 0.0f && mv > 0.0f) {
-                float mm;
-                int em;
-                fa_split(mv, mm, em);
-                den += a * bv * mm * fa_pow2(ae[ba + s] + be[bb + d] + em - emax);
-            }
-        }
-    den = fa_warp_sum(den);
-    if (lane == 0) {
+    block_xacc(x, sh);
+    if (tid == 0) {
         tokens[pos] = v;
-        float mo;
-        int eo;
-        x.normalised(mo, eo);
         double mval = 0.0;
-        if (mo > 0.0f && den > 0.0f)
-            mval = ldexp((double)__ldg(prow + v) * (double)mo / (double)den, eo - emax);
+        if (sh.xm > 0.0f && den_m > 0.0f)
+            mval = ldexp((double)__ldg(prow + v) * (double)sh.xm / (double)den_m, sh.xe - den_e);
         marg[pos] = (float)mval;
     }
+    return true;
 }
 
 __device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const int32_t *__restrict__ committed,
                          const int32_t *status, int32_t *out, int32_t *tokens, unsigned long long *skey);
 
-// Leaves, then the commit: every block takes a ticket after its positions are written; the
-// last block to finish sees all marginals and runs the top-k of every sequence.
-__global__ void __launch_bounds__(kThreads) k_leaf_commit(DevFA fa, int B, int L, const float *__restrict__ probs,
-                                                        const int32_t *__restrict__ committed, uint64_t seed,
-                                                        uint64_t offset, const int32_t *__restrict__ z,
-                                                        const float *__restrict__ am, const int32_t *__restrict__ ae,
-                                                        const float *__restrict__ bm, const int32_t *__restrict__ be,
-                                                        const float *__restrict__ zsum_ws,
-                                                        const int32_t *__restrict__ zexp_ws, int32_t *tokens, float *marg,
-                                                        int32_t *status, int k, int lo, int hi, int32_t *commit_idx,
-                                                        unsigned long long *keys, int32_t *done,
-                                                        const float *__restrict__ leaf) {
-    leaf_position(fa, B, L, probs, committed, seed, offset, z, am, ae, bm, be, zsum_ws, zexp_ws, tokens, marg, status,
-                  leaf);
-    __shared__ int last;
+// Leaves, then the commit: every block takes its sequence's ticket after its position is
+// written; the last block of a sequence sees all of its marginals and runs its top-k.
+__global__ void __launch_bounds__(kLeafThreads) k_leaf_commit(DevFA fa, int B, int L, const float *__restrict__ probs,
+                                                            const int32_t *__restrict__ committed, uint64_t seed,
+                                                            uint64_t offset, const int32_t *__restrict__ z,
+                                                            const float *__restrict__ am,
+                                                            const int32_t *__restrict__ ae,
+                                                            const float *__restrict__ bm,
+                                                            const int32_t *__restrict__ be, int32_t *tokens,
+                                                            float *marg, int32_t *status, int k, int lo, int hi,
+                                                            int32_t *commit_idx, unsigned long long *keys,
+                                                            int32_t *done, const float *__restrict__ leaf) {
+    extern __shared__ float leaf_stage[];
+    __shared__ LeafShared sh;
+    const int b = (int)(blockIdx.x / (unsigned)L), t = (int)(blockIdx.x % (unsigned)L);
+    leaf_position(fa, b, t, L, probs, committed, seed, offset, z, am, ae, bm, be, tokens, marg, status, leaf, sh,
+                  fa.S <= kLeafStageStates ? leaf_stage : nullptr);
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+        sh.last = atomicAdd(done + b, 1) == L - 1;
     }
     __syncthreads();
-    if (!last) return;
+    if (!sh.last) return;
     __threadfence();
-    for (int b = 0; b < B; ++b) {
-        topk_row(b, L, k, lo, hi, marg, committed, status, commit_idx, tokens, keys + (size_t)b * L);
-        __syncthreads();
-    }
+    topk_row(b, L, k, lo, hi, marg, committed, status, commit_idx, tokens, keys + (size_t)b * L);
 }
 
 // ----------------------------------------------------------------------------- 6. commit
@@ -1133,11 +1224,11 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
 
     // 5. leaves: tokens and marginals, then the commit (one launch)
     stage_mark(3, s);
-    const long lw = (long)B * L;
-    k_leaf_commit<<<(unsigned)((lw + kWarps - 1) / kWarps), kThreads, 0, s>>>(
+    const size_t leaf_smem = S <= kLeafStageStates ? (size_t)S * 16 : 0;
+    k_leaf_commit<<<(unsigned)((long)B * L), kLeafThreads, leaf_smem, s>>>(
         dev_view(aut), B, L, probs, committed, philox_seed, philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be),
-        F(p.zsum), I(p.zexp), tokens, marg, row_status, k, commit_lo, commit_hi, commit_idx,
-        (unsigned long long *)(ws + p.keys), I(p.leaf_done), F(p.mant[0]));
+        tokens, marg, row_status, k, commit_lo, commit_hi, commit_idx, (unsigned long long *)(ws + p.keys),
+        I(p.leaf_done), F(p.mant[0]));
     st = launch_check("leaf and commit");
     stage_mark(4, s);
     return st;
