@@ -7,6 +7,7 @@
 // transition = the edges chain, emission = the token lies in the edge's label set.
 #include <algorithm>
 #include <climits>
+#include <functional>
 #include <cstring>
 #include <numeric>
 #include <string>
@@ -38,6 +39,294 @@ struct BlobBuilder {
 fa_status cuda_fail(const char *what, cudaError_t e) {
     fa_set_error(std::string(what) + ": " + cudaGetErrorString(e));
     return e == cudaErrorMemoryAllocation ? FA_ERR_OOM : FA_ERR_CUDA;
+}
+
+// Reweight layout (runs) over the cells of an automaton: see fa_automaton for the format.
+// Returns an empty string, or what went wrong.
+struct RunLayout {
+    int32_t chunk_tokens = 0, n_chunks = 1, n_units = 0;
+    std::vector<int32_t> row_unit0, crun_off, ru_goff, rbm, part_first, part_count, part_max_units, part_max_rows;
+    std::vector<uint16_t> crun_slot, ru_tok;
+};
+
+std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_t> &row_cell_off,
+                             const std::vector<int64_t> &cell_off, const std::vector<int32_t> &cell_tok,
+                             RunLayout &out) {
+    // Reweight layout (runs).  The vocabulary is read in chunks of CH tokens staged in shared
+    // memory.  Rows are taken in groups: a row with many tokens or cells gets one or more
+    // warp units of its own, consecutive small rows share one unit.  Within a group every
+    // cell's sorted tokens are cut into runs of about the group's tokens / (2 x its lanes),
+    // and the runs are dealt longest first, each to the least-loaded lane that still has a
+    // free slot.  A lane's stream for one chunk is its runs' in-chunk tokens, run after run,
+    // each run padded to whole groups of FA_GROUP_ENTRIES (a run with no token in the chunk
+    // is one group of pads), the last entry of each run flagged, the 32 lanes padded to a
+    // common number of groups.
+    const int CH = (V <= FA_REWEIGHT_MAX_CHUNK) ? V : FA_REWEIGHT_MAX_CHUNK;
+    const int nch = (V + CH - 1) / CH;
+    out.chunk_tokens = CH;
+    out.n_chunks = nch;
+    const int64_t kUnitTokens = 8192;        // tokens per warp unit (over all chunks)
+    const int kSmallCells = 128, kUnitCells = 192;  // at most 6 runs per lane on average
+    struct Group { int32_t r0, r1, u0, nu, c0, c1; };
+    std::vector<Group> groups;
+    std::vector<int32_t> &row_unit0 = out.row_unit0;
+    row_unit0.assign(S, 0);
+    auto row_tokens = [&](int r) { return cell_off[row_cell_off[r + 1]] - cell_off[row_cell_off[r]]; };
+    auto row_is_big = [&](int r) {
+        return row_tokens(r) * 2 >= kUnitTokens || row_cell_off[r + 1] - row_cell_off[r] > kSmallCells;
+    };
+    int32_t n_units = 0;
+    for (int r = 0; r < S;) {
+        Group g{};
+        g.r0 = r;
+        g.u0 = n_units;
+        if (row_is_big(r)) {
+            const int64_t rt = row_tokens(r), rc = row_cell_off[r + 1] - row_cell_off[r];
+            int64_t nu = std::max<int64_t>((rt + kUnitTokens - 1) / kUnitTokens, (rc + kUnitCells - 1) / kUnitCells);
+            g.nu = (int32_t)std::min<int64_t>(std::max<int64_t>(nu, 1), FA_RW_MAX_UNITS);
+            g.r1 = r + 1;
+        } else {
+            int64_t tok = 0;
+            int cells = 0, r1 = r;
+            while (r1 < S && !row_is_big(r1)) {
+                const int64_t t2 = row_tokens(r1);
+                const int c2 = row_cell_off[r1 + 1] - row_cell_off[r1];
+                if (r1 > r && (tok + t2 > kUnitTokens || cells + c2 > kUnitCells)) break;
+                tok += t2;
+                cells += c2;
+                ++r1;
+            }
+            g.nu = 1;
+            g.r1 = r1;
+        }
+        r = g.r1;
+        g.c0 = row_cell_off[g.r0];
+        g.c1 = row_cell_off[g.r1];
+        for (int q = g.r0; q < g.r1; ++q) row_unit0[q] = g.u0;
+        n_units += g.nu;
+        groups.push_back(g);
+    }
+    out.n_units = n_units;
+
+    std::vector<int32_t> &crun_off = out.crun_off, &ru_goff = out.ru_goff;
+    std::vector<uint16_t> &crun_slot = out.crun_slot, &ru_tok = out.ru_tok;
+    crun_off.assign(n_cells + 1, 0);
+    std::vector<std::vector<uint16_t>> cell_slots(n_cells);
+    struct Run { int32_t cell; int64_t q, nr; };  // tokens cell_tok[cell_off[cell] + q + nr i]
+    for (const Group &g : groups) {
+        const int lanes = 32 * g.nu;
+        const int64_t gt = cell_off[g.c1] - cell_off[g.c0];
+        const int64_t T = std::max<int64_t>(8, (gt + 2 * lanes - 1) / (2 * lanes));
+        // run q of a cell of nr runs takes the cell's tokens q, q + nr, q + 2 nr, ... (so every
+        // run follows the cell's spread over the chunks); per-chunk token counts of each run
+        std::vector<Run> runs;
+        std::vector<int32_t> rch;  // [run][chunk]
+        for (int c = g.c0; c < g.c1; ++c) {
+            const int64_t len = cell_off[c + 1] - cell_off[c];
+            const int64_t nr = std::max<int64_t>(1, (len + T - 1) / T);
+            for (int64_t q = 0; q < nr; ++q) {
+                runs.push_back({c, q, nr});
+                for (int ch = 0; ch < nch; ++ch) rch.push_back(0);
+                int32_t *rc = rch.data() + (runs.size() - 1) * nch;
+                for (int64_t x = cell_off[c] + q; x < cell_off[c + 1]; x += nr) rc[cell_tok[x] / CH]++;
+                // a run's entries in a chunk are padded to whole groups; an empty run still
+                // ends once, with a group of pads
+                for (int ch = 0; ch < nch; ++ch)
+                    rc[ch] = std::max(FA_GROUP_ENTRIES, (rc[ch] + FA_GROUP_ENTRIES - 1) / FA_GROUP_ENTRIES * FA_GROUP_ENTRIES);
+            }
+        }
+        std::vector<int64_t> rsize(runs.size(), 0);
+        for (size_t ri = 0; ri < runs.size(); ++ri)
+            for (int ch = 0; ch < nch; ++ch) rsize[ri] += rch[ri * nch + ch];
+        std::vector<int32_t> order(runs.size());
+        std::iota(order.begin(), order.end(), 0);
+        std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return rsize[x] > rsize[y]; });
+        // deal longest first to the lane where the run raises its unit's per-chunk maxima (the
+        // padded stream lengths) least, then to the least-loaded such lane
+        std::vector<int64_t> load(lanes, 0), lch((size_t)lanes * nch, 0), umax((size_t)g.nu * nch, 0);
+        std::vector<std::vector<int32_t>> lane_runs(lanes);
+        std::vector<int32_t> slot_of(runs.size(), 0);
+        for (int32_t ri : order) {
+            const int32_t *rc = rch.data() + (size_t)ri * nch;
+            int best = -1;
+            int64_t best_inc = 0;
+            for (int l = 0; l < lanes; ++l) {
+                if ((int)lane_runs[l].size() >= FA_RUN_SLOTS) continue;
+                int64_t inc = 0;
+                const int64_t *ll = lch.data() + (size_t)l * nch, *um = umax.data() + (size_t)(l >> 5) * nch;
+                for (int ch = 0; ch < nch; ++ch) inc += std::max<int64_t>(0, ll[ch] + rc[ch] - um[ch]);
+                if (best < 0 || inc < best_inc || (inc == best_inc && load[l] < load[best])) { best = l; best_inc = inc; }
+            }
+            if (best < 0) return "reweight layout overflow";
+            slot_of[ri] = (best >> 5) * FA_UNIT_SLOTS + (int32_t)lane_runs[best].size() * 32 + (best & 31);
+            lane_runs[best].push_back(ri);
+            load[best] += rsize[ri];
+            int64_t *ll = lch.data() + (size_t)best * nch, *um = umax.data() + (size_t)(best >> 5) * nch;
+            for (int ch = 0; ch < nch; ++ch) { ll[ch] += rc[ch]; um[ch] = std::max(um[ch], ll[ch]); }
+        }
+        for (size_t ri = 0; ri < runs.size(); ++ri) cell_slots[runs[ri].cell].push_back((uint16_t)slot_of[ri]);
+        for (int w = 0; w < g.nu; ++w) {
+            for (int ch = 0; ch < nch; ++ch) {
+                const int32_t lo = ch * CH, hi = (int32_t)std::min<int64_t>((int64_t)(ch + 1) * CH, V);
+                // every lane's runs as lists of in-chunk indices, padded to whole groups
+                std::vector<std::vector<std::vector<uint16_t>>> lr(32);
+                for (int l = 0; l < 32; ++l) {
+                    for (int32_t ri : lane_runs[w * 32 + l]) {
+                        const Run &rn = runs[ri];
+                        std::vector<uint16_t> e;
+                        for (int64_t x = cell_off[rn.cell] + rn.q; x < cell_off[rn.cell + 1]; x += rn.nr)
+                            if (cell_tok[x] >= lo && cell_tok[x] < hi) e.push_back((uint16_t)(cell_tok[x] - lo));
+                        do e.push_back((uint16_t)CH);
+                        while (e.size() % FA_GROUP_ENTRIES);
+                        lr[l].push_back(std::move(e));
+                    }
+                }
+                // entry order: position by position, the 32 lanes' entries are chosen from their
+                // current runs (a run's sum is order-free; its last entry carries the end flag)
+                // so that they fall into distinct shared-memory banks or share an address:
+                // lanes with the fewest choices first, then augmenting paths for the rest
+                std::vector<std::vector<uint16_t>> out(32);
+                std::vector<size_t> cur(32, 0);
+                const int kWin = 48;
+                for (;;) {
+                    int lanes_left[32], nl = 0;
+                    for (int l = 0; l < 32; ++l)
+                        if (cur[l] < lr[l].size()) lanes_left[nl++] = l;
+                    if (!nl) break;
+                    int bank_addr[32], bank_lane[32];  // address held by a bank (-1 free), its first lane
+                    for (int q = 0; q < 32; ++q) { bank_addr[q] = -1; bank_lane[q] = -1; }
+                    int pick[32];
+                    for (int l = 0; l < 32; ++l) pick[l] = -1;
+                    std::sort(lanes_left, lanes_left + nl, [&](int x, int y) {
+                        return std::min<size_t>(lr[x][cur[x]].size(), kWin) < std::min<size_t>(lr[y][cur[y]].size(), kWin);
+                    });
+                    auto fits = [&](uint16_t tk) {
+                        return tk == (uint16_t)CH || bank_addr[tk & 31] == -1 || bank_addr[tk & 31] == tk;
+                    };
+                    std::vector<int> pending;
+                    for (int qi = 0; qi < nl; ++qi) {
+                        const int l = lanes_left[qi];
+                        const auto &rem = lr[l][cur[l]];
+                        const int nscan = (int)std::min<size_t>(rem.size(), kWin);
+                        int got = -1;
+                        for (int x = 0; x < nscan && got < 0; ++x)
+                            if (fits(rem[x])) got = x;
+                        if (got < 0) { pending.push_back(l); continue; }
+                        pick[l] = got;
+                        const uint16_t tk = rem[got];
+                        if (tk != (uint16_t)CH && bank_addr[tk & 31] == -1) { bank_addr[tk & 31] = tk; bank_lane[tk & 31] = l; }
+                    }
+                    // augmenting paths: lane l takes bank b from its sole holder m, which moves to
+                    // another free bank among its own candidates (depth-limited search)
+                    std::function<bool(int, int, std::vector<char> &)> augment = [&](int l, int depth,
+                                                                                      std::vector<char> &seen) {
+                        const auto &rem = lr[l][cur[l]];
+                        const int nscan = (int)std::min<size_t>(rem.size(), kWin);
+                        for (int x = 0; x < nscan; ++x) {
+                            const uint16_t tk = rem[x];
+                            if (fits(tk)) {
+                                pick[l] = x;
+                                if (tk != (uint16_t)CH && bank_addr[tk & 31] == -1) { bank_addr[tk & 31] = tk; bank_lane[tk & 31] = l; }
+                                return true;
+                            }
+                        }
+                        if (depth == 0) return false;
+                        for (int x = 0; x < nscan; ++x) {
+                            const int b = rem[x] & 31;
+                            if (seen[b]) continue;
+                            seen[b] = 1;
+                            const int m = bank_lane[b];
+                            if (m < 0) continue;
+                            // m must be the only lane on bank b (no other lane shares its address)
+                            bool sole = true;
+                            for (int o = 0; o < 32 && sole; ++o)
+                                if (o != m && pick[o] >= 0 && lr[o][cur[o]][pick[o]] == (uint16_t)bank_addr[b]) sole = false;
+                            if (!sole) continue;
+                            const int keep_pick = pick[m];
+                            const int keep_addr = bank_addr[b];
+                            pick[m] = -1;
+                            bank_addr[b] = -2;  // reserved for l: m may not return to it
+                            bank_lane[b] = -1;
+                            if (augment(m, depth - 1, seen)) {
+                                bank_addr[b] = rem[x];
+                                bank_lane[b] = l;
+                                pick[l] = x;
+                                return true;
+                            }
+                            bank_addr[b] = keep_addr;
+                            bank_lane[b] = m;
+                            pick[m] = keep_pick;
+                        }
+                        return false;
+                    };
+                    int used[32] = {0};
+                    for (int l : pending) {
+                        std::vector<char> seen(32, 0);
+                        if (augment(l, 3, seen)) continue;
+                        // no free bank: the least-used bank among the candidates
+                        const auto &rem = lr[l][cur[l]];
+                        const int nscan = (int)std::min<size_t>(rem.size(), kWin);
+                        int best = 0, bc = 1 << 30;
+                        for (int x = 0; x < nscan; ++x)
+                            if (used[rem[x] & 31] < bc) { bc = used[rem[x] & 31]; best = x; }
+                        pick[l] = best;
+                        used[rem[best] & 31]++;
+                    }
+                    for (int qi = 0; qi < nl; ++qi) {
+                        const int l = lanes_left[qi];
+                        auto &rem = lr[l][cur[l]];
+                        uint16_t tk = rem[pick[l]];
+                        rem[pick[l]] = rem.back();
+                        rem.pop_back();
+                        if (rem.empty()) { tk = (uint16_t)(tk | FA_RUN_END); cur[l]++; }
+                        out[l].push_back(tk);
+                    }
+                }
+                const int G = FA_GROUP_ENTRIES;
+                size_t len = 0;
+                for (int l = 0; l < 32; ++l) len = std::max(len, out[l].size());
+                len = (len + G - 1) / G;
+                const size_t g0 = ru_tok.size() / G;
+                ru_goff.push_back((int32_t)g0);
+                ru_tok.resize(ru_tok.size() + len * 32 * G, (uint16_t)CH);
+                for (int l = 0; l < 32; ++l)
+                    for (size_t k = 0; k < out[l].size(); ++k) ru_tok[(g0 + (k / G) * 32 + l) * G + (k % G)] = out[l][k];
+                if (ru_tok.size() / G > (size_t)INT32_MAX / 2) return "automaton too large";
+            }
+        }
+    }
+    ru_goff.push_back((int32_t)(ru_tok.size() / FA_GROUP_ENTRIES));
+    // the reweight reads up to eight groups per lane past a stream's end
+    ru_tok.resize(ru_tok.size() + 8 * 32 * FA_GROUP_ENTRIES, (uint16_t)CH);
+    for (int c = 0; c < n_cells; ++c) {
+        crun_off[c] = (int32_t)crun_slot.size();
+        crun_slot.insert(crun_slot.end(), cell_slots[c].begin(), cell_slots[c].end());
+    }
+    crun_off[n_cells] = (int32_t)crun_slot.size();
+
+    // reweight blocks: whole row groups, at most FA_RW_MAX_UNITS >> p units per block in partition p
+    std::vector<int32_t> &rbm = out.rbm;
+    for (int p = 0;; ++p) {
+        const int cap = FA_RW_MAX_UNITS >> p;
+        out.part_first.push_back((int32_t)(rbm.size() / 8));
+        int count = 0, maxu = 1, maxr = 1;
+        for (size_t gi = 0; gi < groups.size();) {
+            size_t gj = gi;
+            int nu = 0;
+            while (gj < groups.size() && (gj == gi || nu + groups[gj].nu <= cap)) nu += groups[gj++].nu;
+            const Group &A = groups[gi], &Z = groups[gj - 1];
+            rbm.insert(rbm.end(), {A.r0, Z.r1, A.u0, Z.u0 + Z.nu, A.c0, Z.c1, 0, 0});
+            maxu = std::max(maxu, nu);
+            maxr = std::max(maxr, Z.r1 - A.r0);
+            ++count;
+            gi = gj;
+        }
+        out.part_count.push_back(count);
+        out.part_max_units.push_back(maxu);
+        out.part_max_rows.push_back(maxr);
+        if (cap == 1 || count == (int)groups.size()) break;
+    }
+    return std::string();
 }
 
 }  // namespace
@@ -132,7 +421,6 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     std::vector<int64_t> cell_off(1, 0);
     std::vector<int32_t> cell_tok;
     cell_tok.reserve((size_t)I);
-    std::vector<int64_t> row_cost(S, 0);
     int32_t max_cell_len = 0;
     for (int q = 0; q < E;) {
         int e0 = src_edges[q];
@@ -150,142 +438,27 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
         cell_src.push_back(s);
         cell_off.push_back((int64_t)cell_tok.size());
         row_cell_off[s + 1]++;
-        row_cost[s] += len + 16;  // a cell's gather length plus a fixed per-cell cost
     }
     for (int s = 0; s < S; ++s) row_cell_off[s + 1] += row_cell_off[s];
     a->n_cells = (int32_t)cell_dst.size();
     a->max_cell_len = max_cell_len;
 
-    // Reweight layout (sliced, ELL-like).  The vocabulary is read in chunks of CH tokens
-    // staged in shared memory.  Every cell's tokens in a chunk are cut into pieces of at most
-    // FA_PIECE_TOKENS; piece ids are cell-major (cell c owns pieces [pc[c], pc[c+1])).  For
-    // each (chunk, row) the row's pieces, longest first, form slices of 32: lane l of a slice
-    // sums piece l, reading 16-byte groups of 8 in-chunk token indices stored interleaved
-    // (group k of lane l at slice_start + 32 k + l, padded with the index CH, a zero slot).
-    const int CH = (V <= FA_REWEIGHT_MAX_CHUNK) ? V : FA_REWEIGHT_MAX_CHUNK;
-    const int nch = (V + CH - 1) / CH;
-    a->chunk_tokens = CH;
-    a->n_chunks = nch;
-    struct Piece { int32_t cell, chunk; int64_t first; int32_t len; };
-    std::vector<Piece> pieces;
-    std::vector<int32_t> pc(a->n_cells + 1, 0);
-    for (int c = 0; c < a->n_cells; ++c) {
-        pc[c] = (int32_t)pieces.size();
-        const int32_t *b0 = cell_tok.data() + cell_off[c], *b1 = cell_tok.data() + cell_off[c + 1];
-        for (int ch = 0; ch < nch; ++ch) {
-            const int32_t lo = ch * CH, hi = (int32_t)std::min<int64_t>((int64_t)(ch + 1) * CH, V);
-            const int32_t *q0 = std::lower_bound(b0, b1, lo), *q1 = std::lower_bound(b0, b1, hi);
-            for (const int32_t *q = q0; q < q1; q += FA_PIECE_TOKENS)
-                pieces.push_back({c, ch, (int64_t)(q - cell_tok.data()), (int32_t)std::min<int64_t>(FA_PIECE_TOKENS, q1 - q)});
-        }
-    }
-    pc[a->n_cells] = (int32_t)pieces.size();
-    std::vector<int32_t> row_pieces(S, 0);
-    for (auto &pz : pieces) row_pieces[cell_src[pz.cell]]++;
+    RunLayout rl;
     {
-        // dynamic shared memory of the reweight: staged chunk, per-piece sums, per-row maxima
-        const long budget = 232448L - 256 - 4L * (CH + 4) - 4L * S;
-        a->max_unit_pieces = (int32_t)std::min<long>(1 << 20, budget / 4);
-        int32_t mx = 0;
-        for (int r = 0; r < S; ++r) mx = std::max(mx, row_pieces[r]);
-        if (mx > a->max_unit_pieces) { delete a; fa_set_error("fa_compile: a state has too many token pieces for one block"); return FA_ERR_UNSUPPORTED; }
+        const std::string why = build_run_layout(S, V, a->n_cells, row_cell_off, cell_off, cell_tok, rl);
+        if (!why.empty()) {
+            delete a;
+            fa_set_error("fa_compile: " + why);
+            return why == "automaton too large" ? FA_ERR_INVALID_ARG : FA_ERR_UNSUPPORTED;
+        }
     }
-    std::vector<int32_t> sl_row_off((size_t)nch * (S + 1)), sl_goff(1, 0), sl_piece;
-    std::vector<uint16_t> tok8;
-    {
-        std::vector<std::vector<int32_t>> by_row(S);
-        for (int ch = 0; ch < nch; ++ch) {
-            for (auto &v : by_row) v.clear();
-            for (int32_t pid = 0; pid < (int32_t)pieces.size(); ++pid)
-                if (pieces[pid].chunk == ch) by_row[cell_src[pieces[pid].cell]].push_back(pid);
-            for (int r = 0; r < S; ++r) {
-                sl_row_off[(size_t)ch * (S + 1) + r] = (int32_t)(sl_goff.size() - 1);
-                auto &v = by_row[r];
-                std::stable_sort(v.begin(), v.end(), [&](int32_t x, int32_t y) { return pieces[x].len > pieces[y].len; });
-                for (size_t s0 = 0; s0 < v.size(); s0 += 32) {
-                    const size_t n = std::min<size_t>(32, v.size() - s0);
-                    int32_t len = 0;
-                    for (size_t l = 0; l < n; ++l) len = std::max(len, (pieces[v[s0 + l]].len + 7) / 8);
-                    const size_t g0 = tok8.size() / 8;
-                    tok8.resize(tok8.size() + (size_t)len * 32 * 8, (uint16_t)CH);
-                    for (size_t l = 0; l < 32; ++l) {
-                        sl_piece.push_back(l < n ? v[s0 + l] : -1);
-                        if (l >= n) continue;
-                        const Piece &pz = pieces[v[s0 + l]];
-                        for (int32_t j = 0; j < pz.len; ++j)
-                            tok8[(g0 + (size_t)(j / 8) * 32 + l) * 8 + (j % 8)] =
-                                (uint16_t)(cell_tok[pz.first + j] - (int32_t)ch * CH);
-                    }
-                    // spread the 32 lanes' gathers of each group position over distinct banks:
-                    // permute the 8 entries of every group (their sum is order-free)
-                    for (int32_t k = 0; k < len; ++k) {
-                        uint16_t rem[32][8];
-                        int nrem[32];
-                        for (int l = 0; l < 32; ++l) {
-                            nrem[l] = 8;
-                            for (int h = 0; h < 8; ++h) rem[l][h] = tok8[(g0 + (size_t)k * 32 + l) * 8 + h];
-                        }
-                        for (int h = 0; h < 8; ++h) {
-                            int used[33] = {0};
-                            for (int l = 0; l < 32; ++l) {
-                                int best = 0, bc = 1 << 30;
-                                for (int x = 0; x < nrem[l]; ++x) {
-                                    const int cost = (rem[l][x] == (uint16_t)CH) ? used[32] : used[rem[l][x] & 31];
-                                    if (cost < bc) { bc = cost; best = x; }
-                                }
-                                const uint16_t tk = rem[l][best];
-                                rem[l][best] = rem[l][--nrem[l]];
-                                used[tk == (uint16_t)CH ? 32 : (tk & 31)]++;
-                                tok8[(g0 + (size_t)k * 32 + l) * 8 + h] = tk;
-                            }
-                        }
-                    }
-                    sl_goff.push_back((int32_t)(tok8.size() / 8));
-                }
-            }
-            sl_row_off[(size_t)ch * (S + 1) + S] = (int32_t)(sl_goff.size() - 1);
-        }
-        if (tok8.size() / 8 > (size_t)INT32_MAX) { delete a; fa_set_error("fa_compile: automaton too large"); return FA_ERR_INVALID_ARG; }
-        tok8.resize(tok8.size() + 64, (uint16_t)CH);
-    }
-    a->n_slices = (int32_t)(sl_goff.size() - 1);
-
-    // row blocks of balanced gather cost with at most max_unit_pieces pieces each, for target
-    // block counts 1, 2, 4, ...
-    int64_t total_cost = 0;
-    for (int r = 0; r < S; ++r) total_cost += row_cost[r] + 1;
-    std::vector<int32_t> rb, rbm;  // rbm: per block {r0, r1, first cell, end cell, first piece, pad}
-    for (int target = 1; ; target *= 2) {
-        const int64_t cap = std::max<int64_t>(1, (total_cost + target - 1) / target);
-        a->part_first.push_back((int32_t)rb.size());
-        rb.push_back(0);
-        int64_t cost = 0;
-        int32_t np = 0;
-        for (int r = 0; r < S; ++r) {
-            const int64_t rc = row_cost[r] + 1;
-            if (r > rb.back() && (cost + rc > cap || np + row_pieces[r] > a->max_unit_pieces)) {
-                rb.push_back(r);
-                cost = 0;
-                np = 0;
-            }
-            cost += rc;
-            np += row_pieces[r];
-        }
-        rb.push_back(S);
-        a->part_count.push_back((int32_t)(rb.size() - a->part_first.back() - 1));
-        int32_t mp = 0, mr = 0;
-        for (size_t q = a->part_first.back(); q + 1 < rb.size(); ++q) {
-            mp = std::max(mp, pc[row_cell_off[rb[q + 1]]] - pc[row_cell_off[rb[q]]]);
-            mr = std::max(mr, rb[q + 1] - rb[q]);
-        }
-        a->part_max_pieces.push_back(mp);
-        a->part_max_rows.push_back(mr);
-        for (size_t q = a->part_first.back(); q + 1 < rb.size(); ++q) {
-            const int32_t c0 = row_cell_off[rb[q]], c1 = row_cell_off[rb[q + 1]];
-            rbm.insert(rbm.end(), {rb[q], rb[q + 1], c0, c1, pc[c0], 0, 0, 0});
-        }
-        if (a->part_count.back() >= S || target >= 4096) break;
-    }
+    a->chunk_tokens = rl.chunk_tokens;
+    a->n_chunks = rl.n_chunks;
+    a->n_units = rl.n_units;
+    a->part_first = rl.part_first;
+    a->part_count = rl.part_count;
+    a->part_max_units = rl.part_max_units;
+    a->part_max_rows = rl.part_max_rows;
 
     std::vector<int32_t> esrc(edge_src, edge_src + E), edst(edge_dst, edge_dst + E);
 
@@ -307,13 +480,12 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     bb.add(&a->cell_src, cell_src);
     bb.add(&a->cell_off, cell_off);
     bb.add(&a->cell_tok, cell_tok);
-    bb.add(&a->rb_bounds, rb);
-    bb.add(&a->rb_meta, rbm);
-    bb.add(&a->tok8, tok8);
-    bb.add(&a->piece_cell_off, pc);
-    bb.add(&a->sl_row_off, sl_row_off);
-    bb.add(&a->sl_goff, sl_goff);
-    bb.add(&a->sl_piece, sl_piece);
+    bb.add(&a->rb_meta, rl.rbm);
+    bb.add(&a->ru_tok, rl.ru_tok);
+    bb.add(&a->ru_goff, rl.ru_goff);
+    bb.add(&a->row_unit0, rl.row_unit0);
+    bb.add(&a->crun_off, rl.crun_off);
+    bb.add(&a->crun_slot, rl.crun_slot);
 
     cudaError_t err = cudaMalloc(&a->blob, bb.total);
     if (err != cudaSuccess) { delete a; return cuda_fail("fa_compile: cudaMalloc", err); }

@@ -36,23 +36,28 @@ struct fa_automaton {
     int32_t *cell_src = nullptr;      // [n_cells]
     int64_t *cell_off = nullptr;      // [n_cells+1]
     int32_t *cell_tok = nullptr;      // [I]
-    // reweight layout (sliced, ELL-like; built in fa_compile): chunk_tokens-token vocabulary
-    // chunks; piece ids are cell-major, cell x owning pieces [piece_cell_off[x],
-    // piece_cell_off[x+1]); slices of (chunk c, row r) are sl_row_off[c*(S+1)+r] ..
-    // sl_row_off[c*(S+1)+r+1]; slice q has its 16-byte groups at tok8 + 8*sl_goff[q] ..
-    // 8*sl_goff[q+1], lane l reading groups sl_goff[q] + 32 k + l, and sums piece
-    // sl_piece[32 q + l] (-1 = none).
-    int32_t chunk_tokens = 0, n_chunks = 1, max_unit_pieces = 0, n_slices = 0;
-    uint16_t *tok8 = nullptr;
-    int32_t *piece_cell_off = nullptr, *sl_row_off = nullptr, *sl_goff = nullptr, *sl_piece = nullptr;
-    // row blocks for the reweight grid: partition p (p = 0..n_parts-1) splits the rows into
-    // part_count[p] contiguous blocks of balanced gather cost, each with at most
-    // max_unit_pieces pieces; its bounds are rb_bounds[part_first[p] .. + part_count[p]].
-    int32_t *rb_bounds = nullptr;
-    // per row block of every partition (same order, part_first[p] - p + i for block i of
-    // partition p): {r0, r1, first cell, end cell, first piece, 0, 0, 0}
+    // reweight layout ("runs", built in fa_compile).  The vocabulary is read in chunks of
+    // chunk_tokens tokens staged in shared memory.  Every cell's sorted token list is cut
+    // into runs (run q of nr takes tokens q, q + nr, ...); a run belongs to one lane of one
+    // warp unit and owns one accumulator slot.  Unit u's entries for chunk c are 8-byte
+    // groups of FA_GROUP_ENTRIES uint16 entries at ru_goff[u*n_chunks+c] + 32 k + lane
+    // (k = 0, 1, ...): bits 0-14 give the in-chunk token index (chunk_tokens = a zero pad
+    // slot); a run's entries fill whole groups, and bit 15 of a group's last entry ends the
+    // lane's current run (every run ends exactly once per chunk, so slot j of a lane is its
+    // j-th run).  A
+    // lane's slot j is at FA_UNIT_SLOTS * (unit - row_unit0[row]) + 32 j + lane relative to the first
+    // unit of the row's group; cell x adds the slots crun_slot[crun_off[x] .. crun_off[x+1]]
+    // in order.
+    int32_t chunk_tokens = 0, n_chunks = 1, n_units = 0;
+    uint16_t *ru_tok = nullptr;
+    int32_t *ru_goff = nullptr, *row_unit0 = nullptr, *crun_off = nullptr;
+    uint16_t *crun_slot = nullptr;
+    // row blocks for the reweight grid: partition p holds part_count[p] blocks of whole rows
+    // (at most FA_RW_MAX_UNITS >> p units each, unless one row group needs more); block i of partition p
+    // is rb_meta[8 * (part_first[p] + i) ..] = {r0, r1, u0, u1, c0, c1, 0, 0}, launched with
+    // 32 * part_max_units[p] threads.
     int32_t *rb_meta = nullptr;
-    std::vector<int32_t> part_first, part_count, part_max_pieces, part_max_rows;
+    std::vector<int32_t> part_first, part_count, part_max_units, part_max_rows;
     void *blob = nullptr;  // one device allocation holding every array above
     size_t blob_bytes = 0;
 };
@@ -62,8 +67,16 @@ void fa_set_error(const std::string &msg);
 // ----------------------------------------------------------------------------- device side
 
 #define FA_INT_NONE (-2147483647 - 1)
-#define FA_REWEIGHT_MAX_CHUNK 32767  // in-chunk indices and the pad index fit in 16 bits
-#define FA_PIECE_TOKENS 64          // tokens one lane sums per slice
+#ifndef FA_REWEIGHT_MAX_CHUNK
+#define FA_REWEIGHT_MAX_CHUNK 24576  // tokens per staged vocabulary chunk
+#endif
+#define FA_RUN_END 0x8000u           // entry flag: last entry of the lane's current run
+#define FA_GROUP_ENTRIES 4           // entries per 8-byte group; runs end only at group ends
+#ifndef FA_RUN_SLOTS
+#define FA_RUN_SLOTS 8               // runs (accumulator slots) per lane
+#endif
+#define FA_UNIT_SLOTS (32 * FA_RUN_SLOTS)
+#define FA_RW_MAX_UNITS 16           // warp units per reweight block (two blocks per SM)
 
 // floor(log2 x) of a positive normal float from its exponent field (subnormals give -127).
 __device__ __forceinline__ int fa_exponent(float x) {

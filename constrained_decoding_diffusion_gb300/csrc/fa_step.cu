@@ -23,8 +23,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRwThreads = 1024;
-constexpr int kRwWarps = kRwThreads / 32;
 
 // ----------------------------------------------------------------------------- workspace plan
 
@@ -92,8 +90,8 @@ struct DevFA {
     const int32_t *row_cell_off, *cell_dst, *cell_src;
     const int64_t *cell_off;
     const int32_t *cell_tok;
-    const uint16_t *tok8;
-    const int32_t *piece_cell_off, *sl_row_off, *sl_goff, *sl_piece;
+    const uint16_t *ru_tok, *crun_slot;
+    const int32_t *ru_goff, *row_unit0, *crun_off;
     int chunk_tokens, n_chunks, n_cells;
 };
 
@@ -104,8 +102,8 @@ DevFA dev_view(const fa_automaton *a) {
     d.tok_off = a->tok_off; d.tok_edges = a->tok_edges;
     d.row_cell_off = a->row_cell_off; d.cell_dst = a->cell_dst; d.cell_src = a->cell_src;
     d.cell_off = a->cell_off; d.cell_tok = a->cell_tok;
-    d.tok8 = a->tok8; d.piece_cell_off = a->piece_cell_off; d.sl_row_off = a->sl_row_off;
-    d.sl_goff = a->sl_goff; d.sl_piece = a->sl_piece;
+    d.ru_tok = a->ru_tok; d.crun_slot = a->crun_slot; d.ru_goff = a->ru_goff;
+    d.row_unit0 = a->row_unit0; d.crun_off = a->crun_off;
     d.chunk_tokens = a->chunk_tokens; d.n_chunks = a->n_chunks; d.n_cells = a->n_cells;
     return d;
 }
@@ -154,110 +152,148 @@ __device__ int warp_categorical(int n, float u, WF w) {
 // position counts the edges s -> s' that carry its token.
 //
 // The probability row is staged in shared memory one vocabulary chunk at a time (the whole
-// row when |V| <= 32767) by asynchronous copies.  The block's token indices are stored as
-// slices of 32 pieces (sliced ELL, see fa_automaton): one warp per slice, lane l sums piece l
-// from coalesced 16-byte groups of 8 in-chunk indices, with the entries of every group
-// ordered at compile time so the 32 lanes' gathers fall into distinct banks.  Each piece's
-// sum lands in its own shared-memory slot; after the last chunk every cell adds its pieces
+// row when |V| <= 32767) by asynchronous copies.  Warp w walks the entry stream of warp unit
+// u0 + w (see fa_automaton): lane l adds the staged probabilities of its entries and, at
+// each run end, moves the running sum into the run's slot, so every run's slots collect
+// one sum per chunk in chunk order.  After the last chunk every cell adds its runs' slots
 // in a fixed order, so the result is deterministic.
-__global__ void __launch_bounds__(kRwThreads) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
-                                                       const int32_t *__restrict__ committed,
-                                                       const int4 *__restrict__ rbm, int nrb, int max_pieces,
-                                                       float *mant, int32_t *rho, int32_t *rmax, int32_t *zero,
-                                                       long n_zero) {
+__global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
+                                                                    const int32_t *__restrict__ committed,
+                                                                    const int4 *__restrict__ rbm, int nrb, int max_units,
+                                                                    float *mant, int32_t *rho, int32_t *rmax,
+                                                                    int32_t *zero, long n_zero) {
     extern __shared__ float smem_f[];
+    const int nthr = blockDim.x;
     // clear the row maxima of the higher tree levels (their products accumulate with atomicMax)
     {
         const long nb = (long)gridDim.x * gridDim.y;
         const long bid = (long)blockIdx.y * gridDim.x + blockIdx.x;
-        for (long i = bid * kRwThreads + threadIdx.x; i < n_zero; i += nb * kRwThreads) zero[i] = 0;
+        for (long i = bid * nthr + threadIdx.x; i < n_zero; i += nb * nthr) zero[i] = 0;
     }
     const int S = fa.S, CH = fa.chunk_tokens, nch = fa.n_chunks;
-    float *sp = smem_f;                                  // [CH + 1] staged chunk, sp[CH] = 0
-    float *part = sp + ((CH + 4) & ~3);                  // [max_pieces] per-piece sums
-    int *smax = (int *)(part + max_pieces);              // [rows] row maxima (bits)
+    const int CHS = (CH + 4) & ~3;                         // the staged chunk, [CH] = 0
+    float *slots = smem_f + CHS;                           // [max_units * FA_UNIT_SLOTS] run sums
+    int *smax = (int *)smem_f;                             // [rows] row maxima (bits), once the chunks are done
     const int t = blockIdx.x / nrb, r = blockIdx.x % nrb, b = blockIdx.y;
     const size_t pos = (size_t)b * L + t;
     // the block's metadata and the committed token, loaded together
     const int4 m0 = __ldg(rbm + 2 * r), m1 = __ldg(rbm + 2 * r + 1);
     const int c = committed[pos];
-    const int r0 = m0.x, r1 = m0.y, cb = m0.z, ce = m0.w, nc = ce - cb;
-    if (r0 >= r1) return;
+    const int r0 = m0.x, r1 = m0.y, u0 = m0.z, nu = m0.w - m0.z, c0 = m1.x, c1 = m1.y;
     float *M = mant + pos * (size_t)S * S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < r1 - r0; i += kRwThreads) smax[i] = 0;
-    for (size_t i = (size_t)r0 * S + tid; i < (size_t)r1 * S; i += kRwThreads) M[i] = 0.0f;
+    for (size_t i = (size_t)r0 * S + tid; i < (size_t)r1 * S; i += nthr) M[i] = 0.0f;
     if (c < 0) {
-        const int pbase = m1.x;
+        for (int i = tid; i < nu * FA_UNIT_SLOTS; i += nthr) slots[i] = 0.0f;
         const float *prow = probs + pos * (size_t)fa.V;
-        const uint4 *g8 = reinterpret_cast<const uint4 *>(fa.tok8);
+        const bool aligned = (reinterpret_cast<uintptr_t>(prow) & 15) == 0 && (CH & 3) == 0;
+        const uint2 *g4 = reinterpret_cast<const uint2 *>(fa.ru_tok);
+        // a run's sum for the current chunk is stored (not added) into the lane's slot at its
+        // end; after each chunk the lane folds its slots into register totals, in chunk order
+        float *my = slots + warp * FA_UNIT_SLOTS + lane;
+        const uint32_t my_addr = (uint32_t)__cvta_generic_to_shared(my);
+        float tot[FA_RUN_SLOTS];
+#pragma unroll
+        for (int q = 0; q < FA_RUN_SLOTS; ++q) tot[q] = 0.0f;
         for (int ch = 0; ch < nch; ++ch) {
-            const int base = ch * CH;
-            const int n = min(CH, fa.V - base);
-            __syncthreads();
-            if ((reinterpret_cast<uintptr_t>(prow + base) & 15) == 0) {
+            const int base = ch * CH, n = min(CH, fa.V - base);
+            __syncthreads();  // every warp is done with the previous chunk
+            if (aligned) {
                 // asynchronous 16-byte global->shared copies, all in flight before one wait
                 const char *src = reinterpret_cast<const char *>(prow + base);
-                const unsigned dst = (unsigned)__cvta_generic_to_shared(sp);
-                for (int i = tid; i < (n >> 2); i += kRwThreads)
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + 16u * i), "l"(src + 16 * (size_t)i)
+                const unsigned d = (unsigned)__cvta_generic_to_shared(smem_f);
+                for (int i = tid; i < (n >> 2); i += nthr)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d + 16u * i), "l"(src + 16 * (size_t)i)
                                  : "memory");
                 asm volatile("cp.async.commit_group;\n" ::: "memory");
-                for (int i = (n & ~3) + tid; i < n; i += kRwThreads) sp[i] = __ldg(prow + base + i);
+                for (int i = (n & ~3) + tid; i < n; i += nthr) smem_f[i] = __ldg(prow + base + i);
             } else {
-                for (int i = tid; i < n; i += kRwThreads) sp[i] = __ldg(prow + base + i);
+                for (int i = tid; i < n; i += nthr) smem_f[i] = __ldg(prow + base + i);
             }
-            if (tid == 0) sp[CH] = 0.0f;
+            if (tid == 0) smem_f[CH] = 0.0f;
             asm volatile("cp.async.wait_all;\n" ::: "memory");
             __syncthreads();
-            const int s0 = fa.sl_row_off[(size_t)ch * (S + 1) + r0], s1 = fa.sl_row_off[(size_t)ch * (S + 1) + r1];
-            for (int sl = s0 + warp; sl < s1; sl += kRwWarps) {
-                const int g0 = fa.sl_goff[sl];
-                const int len = (fa.sl_goff[sl + 1] - g0) >> 5;
-                const int pid = fa.sl_piece[(size_t)sl * 32 + lane];
+            const int boff = 0;
+            if (warp < nu) {
+                const size_t ui = (size_t)(u0 + warp) * nch + ch;
+                const int gb = fa.ru_goff[ui];
+                const int ng = (fa.ru_goff[ui + 1] - gb) >> 5;
+                const uint2 *gp = g4 + gb + lane;
                 float acc = 0.0f;
-                for (int k0 = 0; k0 < len; k0 += 4) {
-                    uint4 v[4];
+                uint32_t slot_addr = my_addr;  // shared address of the current run's slot
+                // one group of four entries: add their staged probabilities; at a run end
+                // (bit 15 of the last entry) store the sum into the run's slot, clear it and
+                // step to the next slot, all predicated (no branch)
+#define FA_RW_GROUP(V)                                                                                 \
+    {                                                                                                  \
+        const uint32_t x_ = (V).x, y_ = (V).y;                                                         \
+        const float p0_ = smem_f[boff + (int)(x_ & 0x7fffu)] + smem_f[boff + (int)((x_ >> 16) & 0x7fffu)]; \
+        const float p1_ = smem_f[boff + (int)(y_ & 0x7fffu)] + smem_f[boff + (int)((y_ >> 16) & 0x7fffu)]; \
+        acc += p0_ + p1_;                                                                              \
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.shared.f32 [%1], %0;\n\t"  \
+                     "@p mov.f32 %0, 0f00000000;\n\t@p add.u32 %1, %1, 128;\n\t}"                   \
+                     : "+f"(acc), "+r"(slot_addr)                                                      \
+                     : "r"(y_ & 0x80000000u)                                                           \
+                     : "memory");                                                                      \
+    }
+                // whole steps of four groups, the next four loaded (unconditionally: the
+                // stream array is padded past its end) while these are summed; then the tail
+                uint2 cv[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        v[u] = (k0 + u < len) ? __ldg(g8 + g0 + (k0 + u) * 32 + lane) : make_uint4(0, 0, 0, 0);
+                for (int q = 0; q < 4; ++q) cv[q] = __ldg(gp + (size_t)q * 32);
+                int k = 0;
+                for (; k + 4 <= ng; k += 4) {
+                    uint2 nv[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        if (k0 + u < len) {
-                            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                            float a0 = 0.0f, a1 = 0.0f;
+                    for (int q = 0; q < 4; ++q) nv[q] = __ldg(gp + (size_t)(k + 4 + q) * 32);
 #pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                a0 += sp[wv[h] & 0xffffu];
-                                a1 += sp[wv[h] >> 16];
-                            }
-                            acc += a0 + a1;
-                        }
-                    }
+                    for (int q = 0; q < 4; ++q) FA_RW_GROUP(cv[q]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) cv[q] = nv[q];
                 }
-                if (pid >= 0) part[pid - pbase] = acc;
+                for (int q = 0; k < ng; ++k, ++q) {
+                    const uint2 v = q == 0 ? cv[0] : q == 1 ? cv[1] : cv[2];
+                    FA_RW_GROUP(v);
+                }
+#undef FA_RW_GROUP
+                // runs of this lane = run ends seen in the chunk; fold the warp's used slots
+                const int nrun = __reduce_max_sync(0xffffffffu, (int)((slot_addr - my_addr) >> 7));
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < FA_RUN_SLOTS; ++q) {
+                    if (q >= nrun) break;
+                    tot[q] += my[q * 32];
+                }
             }
         }
+        if (warp < nu) {
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < FA_RUN_SLOTS; ++q) my[q * 32] = tot[q];
+        }
         __syncthreads();
-        for (int i = tid; i < nc; i += kRwThreads) {
-            const int cell = cb + i;
-            float v = 0.0f;
-            for (int q = fa.piece_cell_off[cell]; q < fa.piece_cell_off[cell + 1]; ++q) v += part[q - pbase];
+        for (int i = tid; i < r1 - r0; i += nthr) smax[i] = 0;  // the chunk buffer is free now
+        __syncthreads();
+        for (int cell = c0 + tid; cell < c1; cell += nthr) {
             const int s = fa.cell_src[cell];
+            const float *sb = slots + (size_t)(fa.row_unit0[s] - u0) * FA_UNIT_SLOTS;
+            float v = 0.0f;
+            for (int q = fa.crun_off[cell]; q < fa.crun_off[cell + 1]; ++q) v += sb[fa.crun_slot[q]];
             M[(size_t)s * S + fa.cell_dst[cell]] = v;
             atomicMax(&smax[s - r0], __float_as_int(v));
         }
     } else {
+        for (int i = tid; i < r1 - r0; i += nthr) smax[i] = 0;
         __syncthreads();
         if (c < fa.V) {
             const int64_t a0 = fa.tok_off[c], a1 = fa.tok_off[c + 1];
-            for (int64_t j = a0 + tid; j < a1; j += kRwThreads) {
+            for (int64_t j = a0 + tid; j < a1; j += nthr) {
                 const int e = fa.tok_edges[j];
                 const int s = fa.edge_src[e];
                 if (s >= r0 && s < r1) atomicAdd(&M[(size_t)s * S + fa.edge_dst[e]], 1.0f);
             }
             __syncthreads();
-            for (int64_t j = a0 + tid; j < a1; j += kRwThreads) {
+            for (int64_t j = a0 + tid; j < a1; j += nthr) {
                 const int e = fa.tok_edges[j];
                 const int s = fa.edge_src[e];
                 if (s >= r0 && s < r1) atomicMax(&smax[s - r0], __float_as_int(M[(size_t)s * S + fa.edge_dst[e]]));
@@ -265,7 +301,7 @@ __global__ void __launch_bounds__(kRwThreads) k_reweight(DevFA fa, int L, const 
         }
     }
     __syncthreads();
-    for (int i = tid; i < r1 - r0; i += kRwThreads) {
+    for (int i = tid; i < r1 - r0; i += nthr) {
         rho[pos * S + r0 + i] = 0;
         if (rmax) rmax[pos * S + r0 + i] = smax[i];
     }
@@ -1094,16 +1130,19 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
                           long n_zero = 0) {
     const int p = pick_partition(a, (long)B * L);
     const int nrb = a->part_count[p];
-    const int4 *rbm = reinterpret_cast<const int4 *>(a->rb_meta) + 2 * (a->part_first[p] - p);
-    const int max_pieces = a->part_max_pieces[p];
-    const size_t smem = sizeof(float) * (size_t)(((a->chunk_tokens + 4) & ~3) + max_pieces + a->part_max_rows[p]);
+    const int4 *rbm = reinterpret_cast<const int4 *>(a->rb_meta) + 2 * a->part_first[p];
+    const int max_units = a->part_max_units[p];
+    const int threads = std::min(32 * FA_RW_MAX_UNITS, std::max(256, 32 * max_units));
+    // the staged chunk (whose space takes the row maxima at the end) and the run slots
+    const size_t smem = sizeof(float) * (std::max((size_t)((a->chunk_tokens + 4) & ~3), (size_t)a->part_max_rows[p]) +
+                                         (size_t)max_units * FA_UNIT_SLOTS);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k_reweight, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) { fa_set_error(std::string("reweight smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     }
     dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
-    k_reweight<<<grid, kRwThreads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, max_pieces, mant, rho, rmax,
-                                               zero, n_zero);
+    k_reweight<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, max_units, mant, rho, rmax,
+                                            zero, n_zero);
     return launch_check("reweight");
 }
 
