@@ -218,6 +218,9 @@ def cpu_baseline(w, probs, seconds: float):
     o = oracle.OracleFA(w.fa)
     reps, t0 = 0, time.perf_counter()
     nb = probs.shape[0]
+    if o.posterior(probs[0], w.committed[0])["empty"]:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "none: the constrained distribution of %s at L=%d is empty" % (w.name, w.L)}
     while True:
         for b in range(nb):
             x = o.sample(probs[b], w.committed[b], 1, seed=reps)[0]
