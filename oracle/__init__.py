@@ -155,6 +155,41 @@ class OracleFA:
         return self.path_count(tokens) > 0.0
 
 
+def entropy(marg_all: np.ndarray) -> np.ndarray:
+    """Entropy in nats of each position's token distribution, H_t = -sum_v p_t(v) ln p_t(v)
+    with 0 ln 0 = 0.  Applied to the exact constrained marginals (posterior(want_all=True))
+    it is the Dream-style confidence (lowest entropy first) computed from the constrained
+    distribution instead of the mean-field one (paperfeed.app summary, "Constrained remasking
+    confidence"; papernotes.org notes, key design 3)."""
+    p = np.asarray(marg_all, np.float64)
+    out = np.zeros(p.shape[:-1], np.float64)
+    pos = p > 0.0
+    terms = np.zeros_like(p)
+    terms[pos] = p[pos] * np.log(p[pos])
+    out[...] = -terms.sum(axis=-1)
+    return out
+
+
+def confidence(mode: str, probs: np.ndarray, tokens: np.ndarray, marg_tokens: np.ndarray,
+               marg_all: Optional[np.ndarray] = None) -> np.ndarray:
+    """Remasking confidence per position of one sequence, larger = commit first:
+    "marginal": the constrained marginal of the sampled token (the "Mar" rule);
+    "neg_entropy": minus the entropy of the full constrained marginal (Dream's lowest
+    entropy, on the constrained distribution);
+    "unconstrained": the mean-field probability p_t(x_t) of the sampled token (the "Mf"
+    ablation: constrained samples, unconstrained confidence).
+    (paperfeed.app summary, "Constrained remasking confidence" and the ablation of Table 2.)"""
+    if mode == "marginal":
+        return np.asarray(marg_tokens, np.float64)
+    if mode == "neg_entropy":
+        return -entropy(marg_all)
+    if mode == "unconstrained":
+        t = np.arange(probs.shape[0])
+        tok = np.where(np.asarray(tokens) >= 0, tokens, 0)
+        return np.asarray(probs, np.float64)[t, tok]
+    raise ValueError(mode)
+
+
 def topk(marg: np.ndarray, committed: np.ndarray, k: int, lo: int, hi: int) -> np.ndarray:
     lib = _load()
     m = np.ascontiguousarray(marg, np.float64)

@@ -169,6 +169,49 @@ def test_single_state_is_unconstrained():
     np.testing.assert_allclose(r["marg_all"], p64 / p64.sum(axis=1, keepdims=True), atol=1e-14)
 
 
+def test_entropy_closed_forms_real_number_language():
+    """Uniform probabilities over the real-number DFA: at L=1 the accepted strings are the
+    ten digits (entropy ln 10); at L=2 they are "-d" and "dd'" (110 strings), so position
+    0 is uniform over '-' and the ten digits (ln 11) and position 1 over the ten digits
+    (each digit ends 1 + 10 strings: ln 10)."""
+    o = oracle.OracleFA(synth.real_number_dfa())
+    for L, want in ((1, [math.log(10)]), (2, [math.log(11), math.log(10)])):
+        probs = np.full((L, 12), 1.0 / 12, np.float32)
+        r = o.posterior(probs, want_all=True)
+        np.testing.assert_allclose(oracle.entropy(r["marg_all"]), want, rtol=0, atol=1e-12)
+        bf = brute.posterior(synth.real_number_dfa(), probs)
+        np.testing.assert_allclose(oracle.entropy(bf["marg"]), want, rtol=0, atol=1e-12)
+
+
+def test_entropy_unconstrained_is_row_entropy():
+    """Single state, self-loop over V: the constrained marginal is p_t itself, so the
+    entropy is each row's entropy (scipy.stats.entropy, natural log)."""
+    rng = np.random.default_rng(4)
+    V, L = 40, 7
+    o = oracle.OracleFA(synth.single_state_fa(V))
+    probs = synth.gaussian_probs(rng, 1, L, V, 2.0)[0]
+    r = o.posterior(probs, want_all=True)
+    want = [stats.entropy(probs[t].astype(np.float64)) for t in range(L)]
+    np.testing.assert_allclose(oracle.entropy(r["marg_all"]), want, rtol=1e-12, atol=1e-12)
+
+
+def test_confidence_modes():
+    """The three remasking scores: constrained marginal of the sample ("Mar"), minus the
+    constrained entropy (Dream), the mean-field probability of the sample ("Mf")."""
+    rng = np.random.default_rng(6)
+    fa = synth.real_number_dfa()
+    o = oracle.OracleFA(fa)
+    probs = synth.gaussian_probs(rng, 1, 5, 12, 2.0)[0]
+    x = o.sample(probs, None, 1, seed=1)[0]
+    r = o.posterior(probs, tokens=x, want_all=True)
+    np.testing.assert_array_equal(oracle.confidence("marginal", probs, x, r["marg_tokens"]), r["marg_tokens"])
+    np.testing.assert_array_equal(oracle.confidence("unconstrained", probs, x, r["marg_tokens"]),
+                                  probs[np.arange(5), x].astype(np.float64))
+    h = oracle.confidence("neg_entropy", probs, x, r["marg_tokens"], r["marg_all"])
+    assert (h <= 0).all() and (-h <= math.log(12) + 1e-12).all()
+    assert (r["marg_tokens"] <= 1 + 1e-12).all()
+
+
 def test_duplicated_edges_double_every_path():
     """NFA path counting (page 1, "Arbitrary schedules and NFAs"): duplicating every edge
     multiplies each accepted string's path count by 2^L, so logZ grows by L ln 2 and
