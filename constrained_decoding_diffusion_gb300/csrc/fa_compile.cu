@@ -461,6 +461,10 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     a->part_max_rows = rl.part_max_rows;
 
     std::vector<int32_t> esrc(edge_src, edge_src + E), edst(edge_dst, edge_dst + E);
+    // the (src, dst) pair of every token-edge incidence, in token order (|S| <= 4096 fits 16 bits)
+    std::vector<uint32_t> tok_sd(I);
+    for (int64_t j = 0; j < I; ++j)
+        tok_sd[j] = ((uint32_t)edge_src[tok_edges[j]] << 16) | (uint32_t)edge_dst[tok_edges[j]];
 
     BlobBuilder bb;
     bb.add(&a->lab_off, lab_off);
@@ -475,6 +479,7 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     bb.add(&a->accept_mask, acc_mask);
     bb.add(&a->edge_src, esrc);
     bb.add(&a->edge_dst, edst);
+    bb.add(&a->tok_sd, tok_sd);
     bb.add(&a->row_cell_off, row_cell_off);
     bb.add(&a->cell_dst, cell_dst);
     bb.add(&a->cell_src, cell_src);

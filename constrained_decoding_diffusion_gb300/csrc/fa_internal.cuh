@@ -30,6 +30,7 @@ struct fa_automaton {
     int32_t *accept = nullptr;       // [n_accept] ascending
     int32_t *accept_mask = nullptr;  // [S] 0/1
     int32_t *edge_src = nullptr, *edge_dst = nullptr;
+    uint32_t *tok_sd = nullptr;      // [I] (src << 16) | dst of incidence j of the token->edge CSR
     // cells (device), sorted by (src, dst)
     int32_t *row_cell_off = nullptr;  // [S+1]
     int32_t *cell_dst = nullptr;      // [n_cells]

@@ -30,7 +30,7 @@ struct Plan {
     int B = 0, L = 0, S = 0, V = 0, K = 0, Lp = 1;
     int nk[18] = {0};
     size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, mu[18] = {0};
-    size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, zsum = 0, zexp = 0;
+    size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, conf = 0, zsum = 0, zexp = 0;
     size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0, img = 0;
     size_t total = 0;
 };
@@ -73,6 +73,7 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
     p.bm = take(bnd * S * sizeof(float));
     p.be = take(bnd * S * sizeof(int32_t));
     p.keys = take((size_t)B * (size_t)L * sizeof(unsigned long long));
+    p.conf = take((size_t)B * (size_t)L * sizeof(float));   // remasking confidence the commit ranks by
     // tensor-core operand images, sized for the level with the most node slots (level 1)
     if (fa_span_tc_supported(a->S) && p.K >= 1) p.img = take(fa_span_tc_image_bytes(a->S, (long)B * p.nk[1]));
     p.zsum = take((size_t)B * sizeof(float));
@@ -85,6 +86,7 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
 struct DevFA {
     int S, V, start, n_accept;
     const int32_t *accept, *accept_mask, *edge_src, *edge_dst;
+    const uint32_t *tok_sd;
     const int64_t *tok_off;
     const int32_t *tok_edges;
     const int32_t *row_cell_off, *cell_dst, *cell_src;
@@ -99,6 +101,7 @@ DevFA dev_view(const fa_automaton *a) {
     DevFA d;
     d.S = a->S; d.V = a->V; d.start = a->start; d.n_accept = a->n_accept;
     d.accept = a->accept; d.accept_mask = a->accept_mask; d.edge_src = a->edge_src; d.edge_dst = a->edge_dst;
+    d.tok_sd = a->tok_sd;
     d.tok_off = a->tok_off; d.tok_edges = a->tok_edges;
     d.row_cell_off = a->row_cell_off; d.cell_dst = a->cell_dst; d.cell_src = a->cell_src;
     d.cell_off = a->cell_off; d.cell_tok = a->cell_tok;
@@ -867,7 +870,8 @@ __device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float 
                               const int32_t *__restrict__ z, const float *__restrict__ am,
                               const int32_t *__restrict__ ae, const float *__restrict__ bm,
                               const int32_t *__restrict__ be, int32_t *tokens, float *marg, int32_t *status,
-                              const float *__restrict__ leaf, LeafShared &sh, float *stage) {
+                              const float *__restrict__ leaf, LeafShared &sh, float *stage, int conf_mode,
+                              float *conf) {
     const int tid = threadIdx.x;
     const size_t pos = (size_t)b * L + t;
     const int c = committed[pos];
@@ -983,12 +987,16 @@ __device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float 
         if (sh.xm > 0.0f && den_m > 0.0f)
             mval = ldexp((double)__ldg(prow + v) * (double)sh.xm / (double)den_m, sh.xe - den_e);
         marg[pos] = (float)mval;
+        // the commit's ranking score (the entropy score was written by k_token_marginals)
+        if (conf_mode == FA_CONF_MARGINAL) conf[pos] = (float)mval;
+        else if (conf_mode == FA_CONF_UNCONSTRAINED) conf[pos] = __ldg(prow + v);
     }
     return true;
 }
 
-__device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const int32_t *__restrict__ committed,
-                         const int32_t *status, int32_t *out, int32_t *tokens, unsigned long long *skey);
+__device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const float *conf,
+                         const int32_t *__restrict__ committed, const int32_t *status, int32_t *out, int32_t *tokens,
+                         unsigned long long *skey);
 
 // Leaves, then the commit: every block takes its sequence's ticket after its position is
 // written; the last block of a sequence sees all of its marginals and runs its top-k.
@@ -1001,12 +1009,13 @@ __global__ void __launch_bounds__(kLeafThreads) k_leaf_commit(DevFA fa, int B, i
                                                             const int32_t *__restrict__ be, int32_t *tokens,
                                                             float *marg, int32_t *status, int k, int lo, int hi,
                                                             int32_t *commit_idx, unsigned long long *keys,
-                                                            int32_t *done, const float *__restrict__ leaf) {
+                                                            int32_t *done, const float *__restrict__ leaf,
+                                                            int conf_mode, float *conf) {
     extern __shared__ float leaf_stage[];
     __shared__ LeafShared sh;
     const int b = (int)(blockIdx.x / (unsigned)L), t = (int)(blockIdx.x % (unsigned)L);
     leaf_position(fa, b, t, L, probs, committed, seed, offset, z, am, ae, bm, be, tokens, marg, status, leaf, sh,
-                  fa.S <= kLeafStageStates ? leaf_stage : nullptr);
+                  fa.S <= kLeafStageStates ? leaf_stage : nullptr, conf_mode, conf);
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -1015,7 +1024,112 @@ __global__ void __launch_bounds__(kLeafThreads) k_leaf_commit(DevFA fa, int B, i
     __syncthreads();
     if (!sh.last) return;
     __threadfence();
-    topk_row(b, L, k, lo, hi, marg, committed, status, commit_idx, tokens, keys + (size_t)b * L);
+    topk_row(b, L, k, lo, hi, marg, conf, committed, status, commit_idx, tokens, keys + (size_t)b * L);
+}
+
+// ----------------------------------------------------------------------------- 5b. all-token marginals
+
+// Full constrained marginal of a masked position t (papernotes.org key design 3):
+//   u(v) = w_t(v) sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e),   p(x_t = v) = u(v) / D,
+// D = sum_v u(v), and its entropy H_t = ln D - (sum_v u ln u) / D.  The messages' per-state
+// exponents are brought to E, the exponent of the largest cell term alpha(s) M_t(s, d)
+// beta(d), so terms more than about 2^-126 below it vanish.  One block per position; token v
+// is summed by thread v mod T over its incidences in CSR order (deterministic), the partial
+// sums in compensated fp32 and the block sum in double.
+constexpr int kTmThreads = 256;
+constexpr int kTmWarps = kTmThreads / 32;
+
+__global__ void __launch_bounds__(kTmThreads) k_token_marginals(DevFA fa, int L, const float *__restrict__ probs,
+                                                               const int32_t *__restrict__ committed,
+                                                               const int32_t *__restrict__ status,
+                                                               const float *__restrict__ am,
+                                                               const int32_t *__restrict__ ae,
+                                                               const float *__restrict__ bm,
+                                                               const int32_t *__restrict__ be,
+                                                               const float *__restrict__ leaf, float *marg_all,
+                                                               float *entropy, float *conf) {
+    extern __shared__ float tm_s[];  // [4 S]: alpha and beta mantissas, then their exponents
+    __shared__ int emax_w[kTmWarps];
+    __shared__ double red[2 * kTmWarps];
+    const int S = fa.S, V = fa.V;
+    const size_t pos = blockIdx.x;
+    const int b = (int)(pos / (size_t)L), t = (int)(pos % (size_t)L);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = committed[pos];
+    float *out = marg_all ? marg_all + pos * (size_t)V : nullptr;
+    if (c >= 0 || status[b] != FA_ROW_OK) {
+        if (out)
+            for (int v = tid; v < V; v += kTmThreads) out[v] = (c >= 0 && v == c) ? 1.0f : 0.0f;
+        if (tid == 0) {
+            if (entropy) entropy[pos] = 0.0f;
+            if (conf) conf[pos] = 0.0f;
+        }
+        return;
+    }
+    float *sam = tm_s, *sbm = tm_s + S;
+    int *sae = reinterpret_cast<int *>(tm_s + 2 * S), *sbe = sae + S;
+    const size_t ba = ((size_t)b * (L + 1) + t) * S, bb = ba + S;
+    for (int s = tid; s < S; s += kTmThreads) {
+        sam[s] = am[ba + s]; sae[s] = ae[ba + s];
+        sbm[s] = bm[bb + s]; sbe[s] = be[bb + s];
+    }
+    __syncthreads();
+    const float *Mt = leaf + pos * (size_t)S * S;
+    int e = FA_INT_NONE;
+    for (int q = tid; q < fa.n_cells; q += kTmThreads) {
+        const int s = fa.cell_src[q], d = fa.cell_dst[q];
+        const float mv = __ldg(Mt + (size_t)s * S + d);
+        if (sam[s] > 0.0f && sbm[d] > 0.0f && mv > 0.0f) e = max(e, sae[s] + sbe[d] + fa_exponent(mv));
+    }
+    e = fa_warp_max_int(e);
+    if (lane == 0) emax_w[warp] = e;
+    __syncthreads();
+    int E = FA_INT_NONE;
+    for (int w = 0; w < kTmWarps; ++w) E = max(E, emax_w[w]);
+    const float *prow = probs + pos * (size_t)V;
+    float su = 0.0f, cu = 0.0f, sl = 0.0f, cl = 0.0f;  // compensated sums of u and u ln u
+    if (E != FA_INT_NONE)
+        for (int v = tid; v < V; v += kTmThreads) {
+            const float w = __ldg(prow + v);
+            float acc = 0.0f;
+            if (w > 0.0f)
+                for (int64_t j = fa.tok_off[v]; j < fa.tok_off[v + 1]; ++j) {
+                    const uint32_t sd = __ldg(fa.tok_sd + j);
+                    const int s = (int)(sd >> 16), d = (int)(sd & 0xffffu);
+                    const float a = sam[s], bq = sbm[d];
+                    if (a > 0.0f && bq > 0.0f) acc += a * bq * fa_pow2(sae[s] + sbe[d] - E);
+                }
+            const float u = w * acc;
+            if (out) out[v] = u;
+            if (u > 0.0f) {
+                float y = u - cu, tt = su + y;
+                cu = (tt - su) - y;
+                su = tt;
+                y = u * logf(u) - cl;
+                tt = sl + y;
+                cl = (tt - sl) - y;
+                sl = tt;
+            }
+        }
+    double du = (double)su - (double)cu, dl = (double)sl - (double)cl;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        du += __shfl_xor_sync(0xffffffffu, du, o);
+        dl += __shfl_xor_sync(0xffffffffu, dl, o);
+    }
+    if (lane == 0) { red[warp] = du; red[kTmWarps + warp] = dl; }
+    __syncthreads();
+    double D = 0.0, SL = 0.0;
+    for (int w = 0; w < kTmWarps; ++w) { D += red[w]; SL += red[kTmWarps + w]; }
+    const double H = D > 0.0 ? log(D) - SL / D : 0.0;
+    if (tid == 0) {
+        if (entropy) entropy[pos] = (float)H;
+        if (conf) conf[pos] = (float)-H;
+    }
+    if (out) {
+        const float inv = D > 0.0 ? (float)(1.0 / D) : 0.0f;
+        for (int v = tid; v < V; v += kTmThreads) out[v] *= inv;  // this thread's own writes
+    }
 }
 
 // ----------------------------------------------------------------------------- 6. commit
@@ -1026,8 +1140,15 @@ __global__ void __launch_bounds__(kLeafThreads) k_leaf_commit(DevFA fa, int B, i
 // A sequence whose status is not OK gets no commits and -1 tokens / 0 marginals at every
 // masked position (some leaves may have been drawn before the failure was recorded).
 // Executed by one whole block; skey holds hi - lo keys.
-__device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const int32_t *__restrict__ committed,
-                         const int32_t *status, int32_t *out, int32_t *tokens, unsigned long long *skey) {
+// Order-preserving bits of a float (any sign): larger float, larger key.
+__device__ __forceinline__ uint32_t fa_order_bits(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const float *conf,
+                         const int32_t *__restrict__ committed, const int32_t *status, int32_t *out, int32_t *tokens,
+                         unsigned long long *skey) {
     int32_t *o = out + (size_t)b * k;
     for (int i = threadIdx.x; i < k; i += blockDim.x) o[i] = -1;
     if (status[b] != FA_ROW_OK) {
@@ -1035,14 +1156,14 @@ __device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const
             if (committed[(size_t)b * L + t] < 0) { tokens[(size_t)b * L + t] = -1; marg[(size_t)b * L + t] = 0.0f; }
         return;
     }
-    const float *mg = marg + (size_t)b * L;
+    const float *cf = conf + (size_t)b * L;
     const int32_t *cm = committed + (size_t)b * L;
     const int t0 = max(lo, 0), t1 = min(hi, L), n = t1 - t0;
-    // key = (marginal bits, ~t): larger marginal first, then lower position; 0 = not eligible
+    // key = (confidence bits, ~t): larger confidence first, then lower position; 0 = not eligible
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         const int t = t0 + i;
         skey[i] = (cm[t] >= 0) ? 0ull
-                               : (((unsigned long long)(unsigned)__float_as_int(mg[t]) << 32) |
+                               : (((unsigned long long)fa_order_bits(cf[t]) << 32) |
                                   (unsigned long long)(0xFFFFFFFFu - (unsigned)t));
     }
     __syncthreads();
@@ -1146,7 +1267,47 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     return launch_check("reweight");
 }
 
+fa_status launch_token_marginals(const fa_automaton *aut, int B, int L, const float *probs, const int32_t *committed,
+                                 const Plan &p, const char *ws, const int32_t *row_status, float *marg_all,
+                                 float *entropy, float *conf, cudaStream_t st) {
+    const size_t smem = (size_t)aut->S * 16;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_token_marginals, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) { fa_set_error(std::string("token marginals smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    }
+    auto F = [&](size_t off) { return (const float *)(ws + off); };
+    auto I = [&](size_t off) { return (const int32_t *)(ws + off); };
+    k_token_marginals<<<(unsigned)((long)B * L), kTmThreads, smem, st>>>(
+        dev_view(aut), L, probs, committed, row_status, F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.mant[0]), marg_all,
+        entropy, conf);
+    return launch_check("token marginals");
+}
+
 }  // namespace
+
+extern "C" fa_status fa_token_marginals(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                        const int32_t *committed, const void *workspace, size_t ws_bytes,
+                                        const int32_t *row_status, float *marg_all, float *entropy,
+                                        fa_stream stream) {
+    if (!aut) { fa_set_error("fa_token_marginals: NULL automaton"); return FA_ERR_INVALID_ARG; }
+    if (B < 0 || B > 65535 || L < 0 || L > FA_MAX_LENGTH) {
+        fa_set_error("fa_token_marginals: B or L out of range"); return FA_ERR_INVALID_ARG;
+    }
+    if ((long)B * L == 0 || (!marg_all && !entropy)) return FA_OK;
+    if (!probs || !committed || !workspace || !row_status) {
+        fa_set_error("fa_token_marginals: NULL buffer"); return FA_ERR_INVALID_ARG;
+    }
+    fa_status st = check_device(aut, "fa_token_marginals");
+    if (st != FA_OK) return st;
+    const Plan p = make_plan(aut, B, L);
+    if (ws_bytes < p.total) {
+        fa_set_error("fa_token_marginals: workspace needs " + std::to_string(p.total) + " bytes");
+        return FA_ERR_WORKSPACE_TOO_SMALL;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { fa_set_error("fa_token_marginals: workspace not 256-byte aligned"); return FA_ERR_INVALID_ARG; }
+    return launch_token_marginals(aut, B, L, probs, committed, p, (const char *)workspace, row_status, marg_all, entropy,
+                                  nullptr, (cudaStream_t)stream);
+}
 
 extern "C" fa_status fa_step_workspace_bytes(const fa_automaton *aut, int32_t B, int32_t L, size_t *bytes) {
     if (!aut || !bytes) { fa_set_error("fa_step_workspace_bytes: NULL argument"); return FA_ERR_INVALID_ARG; }
@@ -1172,7 +1333,21 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
                                          int32_t k, int32_t commit_lo, int32_t commit_hi, void *workspace,
                                          size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
                                          int32_t *commit_idx, int32_t *row_status, fa_stream stream) {
+    return fa_constrained_step_ex(aut, B, L, probs, committed, philox_seed, philox_offset, k, commit_lo, commit_hi,
+                                  FA_CONF_MARGINAL, workspace, ws_bytes, tokens, logZ, marg, nullptr, commit_idx,
+                                  row_status, stream);
+}
+
+extern "C" fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                            const int32_t *committed, uint64_t philox_seed, uint64_t philox_offset,
+                                            int32_t k, int32_t commit_lo, int32_t commit_hi, int32_t confidence,
+                                            void *workspace, size_t ws_bytes, int32_t *tokens, double *logZ,
+                                            float *marg, float *entropy, int32_t *commit_idx, int32_t *row_status,
+                                            fa_stream stream) {
     if (!aut) { fa_set_error("fa_constrained_step: NULL automaton"); return FA_ERR_INVALID_ARG; }
+    if (confidence != FA_CONF_MARGINAL && confidence != FA_CONF_NEG_ENTROPY && confidence != FA_CONF_UNCONSTRAINED) {
+        fa_set_error("fa_constrained_step: unknown confidence"); return FA_ERR_INVALID_ARG;
+    }
     if (B < 0 || B > 65535 || L < 0 || L > FA_MAX_LENGTH || k < 0) {
         fa_set_error("fa_constrained_step: B, L or k out of range"); return FA_ERR_INVALID_ARG;
     }
@@ -1261,13 +1436,19 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
         if ((st = launch_check("top-down level")) != FA_OK) return st;
     }
 
-    // 5. leaves: tokens and marginals, then the commit (one launch)
+    // 5. leaves: tokens and marginals, then the commit (one launch); before them, when asked,
+    //    the entropy of every position's full constrained distribution
     stage_mark(3, s);
+    if (confidence == FA_CONF_NEG_ENTROPY || entropy) {
+        st = launch_token_marginals(aut, B, L, probs, committed, p, ws, row_status, nullptr, entropy,
+                                    confidence == FA_CONF_NEG_ENTROPY ? F(p.conf) : nullptr, s);
+        if (st != FA_OK) return st;
+    }
     const size_t leaf_smem = S <= kLeafStageStates ? (size_t)S * 16 : 0;
     k_leaf_commit<<<(unsigned)((long)B * L), kLeafThreads, leaf_smem, s>>>(
         dev_view(aut), B, L, probs, committed, philox_seed, philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be),
         tokens, marg, row_status, k, commit_lo, commit_hi, commit_idx, (unsigned long long *)(ws + p.keys),
-        I(p.leaf_done), F(p.mant[0]));
+        I(p.leaf_done), F(p.mant[0]), confidence, F(p.conf));
     st = launch_check("leaf and commit");
     stage_mark(4, s);
     return st;

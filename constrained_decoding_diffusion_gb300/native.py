@@ -23,10 +23,14 @@ FA_ERR_OOM = 3
 FA_ERR_WORKSPACE_TOO_SMALL = 4
 FA_ERR_UNSUPPORTED = 5
 FA_ROW_OK, FA_ROW_EMPTY, FA_ROW_UNDERFLOW, FA_ROW_TIMEOUT = 0, 1, 2, 3
+FA_CONF_MARGINAL, FA_CONF_NEG_ENTROPY, FA_CONF_UNCONSTRAINED = 0, 1, 2
+CONFIDENCE = {"marginal": FA_CONF_MARGINAL, "neg_entropy": FA_CONF_NEG_ENTROPY,
+              "unconstrained": FA_CONF_UNCONSTRAINED}
 
 # every entry point include/fa.h declares
 EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_workspace_bytes",
-           "fa_transition_matrices", "fa_constrained_step", "fa_apply_commits", "fa_constrained_step_noalloc",
+           "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_ex", "fa_token_marginals",
+           "fa_apply_commits", "fa_constrained_step_noalloc",
            "fa_profile_enable", "fa_profile_read",
            "fa_launch_count", "fa_last_error")
 N_STAGES = 4
@@ -66,6 +70,10 @@ def load(path: str = LIB_PATH):
     lib.fa_transition_matrices.restype = st
     lib.fa_constrained_step.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, sz, P, P, P, P, P, P]
     lib.fa_constrained_step.restype = st
+    lib.fa_constrained_step_ex.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, i32, P, sz, P, P, P, P, P, P, P]
+    lib.fa_constrained_step_ex.restype = st
+    lib.fa_token_marginals.argtypes = [P, i32, i32, P, P, P, sz, P, P, P, P]
+    lib.fa_token_marginals.restype = st
     lib.fa_apply_commits.argtypes = [i32, i32, i32, P, P, P, P]
     lib.fa_apply_commits.restype = st
     lib.fa_constrained_step_noalloc.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, P, P, P, P, P]
@@ -196,6 +204,41 @@ def fa_constrained_step(aut: CompiledAutomaton, probs, committed, philox_seed: i
         _dev(row_status, torch.int32, "row_status", (B,)), _stream_ptr(stream)))
 
 
+def fa_constrained_step_ex(aut: CompiledAutomaton, probs, committed, philox_seed: int, philox_offset: int, k: int,
+                           commit_lo: int, commit_hi: int, confidence: str, workspace, tokens, logZ, marg, entropy,
+                           commit_idx, row_status, stream=None):
+    """fa_constrained_step with a remasking confidence ("marginal", "neg_entropy" or
+    "unconstrained") and an optional entropy output [B, L] (None to skip)."""
+    import torch
+    B, L, V = probs.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.fa_constrained_step_ex(
+        aut.handle, B, L, _dev(probs, torch.float32, "probs", (B, L, aut.vocab)),
+        _dev(committed, torch.int32, "committed", (B, L)), ctypes.c_uint64(philox_seed & (2 ** 64 - 1)),
+        ctypes.c_uint64(philox_offset & (2 ** 64 - 1)), int(k), int(commit_lo), int(commit_hi),
+        CONFIDENCE[confidence], _dev(workspace, workspace.dtype, "workspace"), ws_bytes,
+        _dev(tokens, torch.int32, "tokens", (B, L)), _dev(logZ, torch.float64, "logZ", (B,)),
+        _dev(marg, torch.float32, "marg", (B, L)),
+        _dev(entropy, torch.float32, "entropy", (B, L)) if entropy is not None else None,
+        _dev(commit_idx, torch.int32, "commit_idx", (B, k)) if k > 0 else None,
+        _dev(row_status, torch.int32, "row_status", (B,)), _stream_ptr(stream)))
+
+
+def fa_token_marginals(aut: CompiledAutomaton, probs, committed, workspace, row_status, marg_all=None, entropy=None,
+                       stream=None):
+    """Full constrained marginals [B, L, V] and/or entropies [B, L] from the messages of the
+    step that last used `workspace` (same inputs)."""
+    import torch
+    B, L, V = probs.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.fa_token_marginals(
+        aut.handle, B, L, _dev(probs, torch.float32, "probs", (B, L, aut.vocab)),
+        _dev(committed, torch.int32, "committed", (B, L)), _dev(workspace, workspace.dtype, "workspace"), ws_bytes,
+        _dev(row_status, torch.int32, "row_status", (B,)),
+        _dev(marg_all, torch.float32, "marg_all", (B, L, aut.vocab)) if marg_all is not None else None,
+        _dev(entropy, torch.float32, "entropy", (B, L)) if entropy is not None else None, _stream_ptr(stream)))
+
+
 def fa_apply_commits(commit_idx, tokens, committed, stream=None):
     """committed[b, t] = tokens[b, t] for every t in commit_idx[b] (t >= 0), on the device."""
     import torch
@@ -209,9 +252,14 @@ def fa_apply_commits(commit_idx, tokens, committed, stream=None):
 class ConstrainedStep:
     """Convenience owner of the workspace and output tensors for a fixed (B, L, k)."""
 
-    def __init__(self, aut: CompiledAutomaton, B: int, L: int, k: int, device="cuda"):
+    def __init__(self, aut: CompiledAutomaton, B: int, L: int, k: int, device="cuda", confidence: str = "marginal",
+                 want_entropy: bool = False):
         import torch
+        if confidence not in CONFIDENCE:
+            raise ValueError("confidence must be one of %s" % sorted(CONFIDENCE))
         self.aut, self.B, self.L, self.k = aut, B, L, k
+        self.confidence = confidence
+        self.entropy = torch.empty((B, L), dtype=torch.float32, device=device) if want_entropy else None
         nbytes = fa_step_workspace_bytes(aut, B, L)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         self.tokens = torch.empty((B, L), dtype=torch.int32, device=device)
@@ -222,10 +270,23 @@ class ConstrainedStep:
 
     def __call__(self, probs, committed, seed: int, offset: int = 0, lo: int = 0, hi: Optional[int] = None,
                  stream=None):
-        fa_constrained_step(self.aut, probs, committed, seed, offset, self.k, lo, self.L if hi is None else hi,
-                            self.workspace, self.tokens, self.logZ, self.marg, self.commit_idx, self.row_status,
-                            stream)
+        hi = self.L if hi is None else hi
+        if self.confidence == "marginal" and self.entropy is None:
+            fa_constrained_step(self.aut, probs, committed, seed, offset, self.k, lo, hi, self.workspace, self.tokens,
+                                self.logZ, self.marg, self.commit_idx, self.row_status, stream)
+        else:
+            fa_constrained_step_ex(self.aut, probs, committed, seed, offset, self.k, lo, hi, self.confidence,
+                                   self.workspace, self.tokens, self.logZ, self.marg, self.entropy, self.commit_idx,
+                                   self.row_status, stream)
         return self.tokens, self.logZ, self.marg, self.commit_idx, self.row_status
+
+    def token_marginals(self, probs, committed, stream=None):
+        """Full constrained marginals [B, L, V] and entropies [B, L] of the last call's inputs."""
+        import torch
+        marg_all = torch.empty((self.B, self.L, self.aut.vocab), dtype=torch.float32, device=self.tokens.device)
+        ent = torch.empty((self.B, self.L), dtype=torch.float32, device=self.tokens.device)
+        fa_token_marginals(self.aut, probs, committed, self.workspace, self.row_status, marg_all, ent, stream)
+        return marg_all, ent
 
 
 def fa_profile_enable(enable: bool):

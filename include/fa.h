@@ -188,6 +188,58 @@ fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int32_t L, con
                               int32_t *commit_idx, int32_t *row_status, fa_stream stream);
 
 /*
+ * Remasking confidence: what the commit ranks masked positions by, larger first.  The
+ * paperfeed.app summary ("Constrained remasking confidence" and the ablation of its
+ * Table 2) and key design 3 of the papernotes.org notes: a dLLM commits the positions with
+ * the best confidence (LLaDA: highest probability, Dream: lowest entropy), and the method
+ * computes it from the constrained distribution ("Mar") instead of the mean-field one ("Mf").
+ */
+enum {
+    FA_CONF_MARGINAL = 0,      /* constrained marginal of the sampled token ("Mar"; the default) */
+    FA_CONF_NEG_ENTROPY = 1,   /* minus the entropy of the position's full constrained token distribution */
+    FA_CONF_UNCONSTRAINED = 2  /* the mean-field probability p_t(x^_t) of the sampled token ("Mf") */
+};
+
+/*
+ * fa_constrained_step_ex -- fa_constrained_step with a choice of remasking confidence.
+ *
+ *   confidence  FA_CONF_*: the commit takes the k masked positions of [commit_lo, commit_hi)
+ *               with the largest confidence, descending, ties to the lower position
+ *   entropy     [B, L] fp32 device out, or NULL: entropy in nats of every position's full
+ *               constrained token distribution (see fa_token_marginals); 0 for committed
+ *               positions and for sequences whose status is not FA_ROW_OK
+ * FA_CONF_NEG_ENTROPY or a non-NULL entropy costs one more pass over the token-edge
+ * incidences of every masked position (about the work of the reweight).  Every other
+ * argument is as for fa_constrained_step, which is this call with FA_CONF_MARGINAL and
+ * entropy = NULL.
+ * Errors: as fa_constrained_step; FA_ERR_INVALID_ARG for an unknown confidence.
+ */
+fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                 const int32_t *committed, uint64_t philox_seed, uint64_t philox_offset,
+                                 int32_t k, int32_t commit_lo, int32_t commit_hi, int32_t confidence,
+                                 void *workspace, size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
+                                 float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream);
+
+/*
+ * fa_token_marginals -- the full constrained marginal of every token at every position,
+ *     p(x_t = v) = w_t(v) * sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / (same summed over v)
+ * (key design 3 of the papernotes.org notes), from the prefix/suffix messages that the
+ * preceding fa_constrained_step or fa_constrained_step_ex left in its workspace.  Call it on
+ * the same stream after that step, with the same automaton, B, L, probs, committed and
+ * workspace, before the workspace is used again.
+ *
+ *   row_status  [B] int32 device: that step's status
+ *   marg_all    [B, L, V] fp32 device out, or NULL; one-hot at committed positions, zero
+ *               at the masked positions of sequences whose status is not FA_ROW_OK
+ *   entropy     [B, L] fp32 device out, or NULL: -sum_v p ln p (nats), 0 where marg_all is
+ *               one-hot or zero
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_WORKSPACE_TOO_SMALL, FA_ERR_CUDA (launch).
+ */
+fa_status fa_token_marginals(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                             const int32_t *committed, const void *workspace, size_t ws_bytes,
+                             const int32_t *row_status, float *marg_all, float *entropy, fa_stream stream);
+
+/*
  * fa_apply_commits -- the commit of a remasking schedule: committed[b, t] = tokens[b, t] for
  * every t = commit_idx[b, i] >= 0 (i < k).  With fa_constrained_step this gives any
  * schedule of the papernotes.org notes (key design 3) or the paperfeed.app summary
