@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--length", type=int, default=None, help="override L (smaller profiling cases)")
+    ap.add_argument("--method", default="tree", choices=["tree", "chain"],
+                    help="log-depth tree (default) or the O(L) chain form of the same step")
+    ap.add_argument("--confidence", default="marginal", choices=["marginal", "neg_entropy", "unconstrained"],
+                    help="remasking confidence the commit ranks by")
     return ap.parse_args()
 
 
@@ -156,10 +160,19 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- roofline model
 
-def algorithmic(w, masked: int):
+def algorithmic(w, masked: int, method: str = "tree"):
     """Algorithmic bytes and FLOPs per step of each stage (the per-unit figures of the design
-    notes times the units one step processes)."""
+    notes times the units one step processes).  For the chain form the second and third
+    stages are the forward pass and the backward pass with the state draws: each reads every
+    M_t once and does one vector-matrix product per position."""
     B, L, S, V = w.B, w.L, w.S, w.V
+    if method == "chain":
+        span = 4 * S * S + 8 * S
+        msg = 8 * S
+        return {"reweight": {"bytes": 4 * masked * V + B * L * span, "flops": 2 * masked * w.fa.n_incidences},
+                "upsweep": {"bytes": B * L * (4 * S * S + msg), "flops": 2 * B * L * S * S},
+                "topdown": {"bytes": B * L * (4 * S * S + 2 * msg), "flops": 2 * B * L * S * S},
+                "leaf_commit": {"bytes": 4 * B * L * 4 + 8 * B * L, "flops": 0}}
     K = max(0, math.ceil(math.log2(L))) if L > 1 else 0
     nk = [(L + (1 << k) - 1) >> k for k in range(K + 1)]
     span = 4 * S * S + 8 * S                      # mantissas + row exponent + row max
@@ -300,7 +313,7 @@ def run_native(args, rank, world, local):
         probs = synth.gaussian_probs_torch(w.seed, w.B, w.L, w.V, w.sigma)
         probs_np = None
     committed = torch.from_numpy(w.committed).cuda()
-    step = native.ConstrainedStep(aut, w.B, w.L, w.k)
+    step = native.ConstrainedStep(aut, w.B, w.L, w.k, method=args.method, confidence=args.confidence)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
     seed = 1234 + rank
@@ -405,7 +418,7 @@ def run_native(args, rank, world, local):
     if rank != 0:
         return
     value = replica_value(w.B * w.L, world, ms_max)
-    alg = algorithmic(w, masked)
+    alg = algorithmic(w, masked, args.method)
     hbm, tc, src = peaks()
     per_stage = {k: stage_ms[k] / n_prof for k in stage_ms}
     dom = max(per_stage, key=per_stage.get)
@@ -425,6 +438,7 @@ def run_native(args, rank, world, local):
             "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "V": w.V, "masked": masked,
                        "k": w.k, "l2": "flushed between steps (256 MiB write)",
                        "launch": "cuda_graph" if graph is not None else "eager",
+                       "method": args.method, "confidence": args.confidence,
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roof,
             "step_roofline": {"ms_at_roofline": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_max,

@@ -1132,6 +1132,195 @@ __global__ void __launch_bounds__(kTmThreads) k_token_marginals(DevFA fa, int L,
     }
 }
 
+// ----------------------------------------------------------------------------- chain variant
+
+// The chain form of the same computation (paperfeed.app summary, "The scan trick": the O(L)
+// chain that the tree shortens to O(log L) depth): forward messages alpha_t = alpha_{t-1} M_t
+// for t = 1..L, then backward messages beta_{t-1} = M_t beta_t together with forward-filtering
+// backward-sampling of the states, z_L ~ alpha_L restricted to F and
+// z_{t-1} ~ alpha_{t-1}(s) M_t(s, z_t).  One block per sequence.  The vectors keep the tree
+// messages' format (mantissa in [1, 2) and an exponent per state) and land in the same
+// workspace arrays, so leaves, marginals and the commit are the tree path's kernels.  Every
+// sum is one pass with a running exponent (fa_xacc).
+constexpr int kChThreads = 512;
+constexpr int kChWarps = kChThreads / 32;
+
+__device__ __forceinline__ int chain_cb(int S) { return S >= 64 ? 64 : 32; }
+
+// Shared memory: two (mantissa, exponent) vectors, and in the forward kernel the partials of
+// the row splits (one mantissa and one exponent per thread).
+size_t chain_smem(int S, bool forward) { return (size_t)S * 16 + (forward ? (size_t)kChThreads * 8 : 0); }
+
+__global__ void __launch_bounds__(kChThreads) k_chain_forward(DevFA fa, int L, const float *__restrict__ leaf,
+                                                             float *am, int32_t *ae) {
+    extern __shared__ float ch_s[];
+    const int S = fa.S, b = blockIdx.x, tid = threadIdx.x;
+    float *va[2] = {ch_s, ch_s + S};
+    int *ve[2] = {reinterpret_cast<int *>(ch_s + 2 * S), reinterpret_cast<int *>(ch_s + 3 * S)};
+    const int CB = chain_cb(S), QS = kChThreads / CB;
+    float *pm = ch_s + 4 * S;
+    int *pe = reinterpret_cast<int *>(pm + kChThreads);
+    const size_t base = (size_t)b * (L + 1) * S;
+    for (int q = tid; q < S; q += kChThreads) {
+        const float a0 = q == fa.start ? 1.0f : 0.0f;
+        am[base + q] = a0; ae[base + q] = 0;
+        va[0][q] = a0; ve[0][q] = 0;
+    }
+    __syncthreads();
+    const int c = tid % CB, qs = tid / CB;
+    for (int t = 1; t <= L; ++t) {
+        const int in = (t - 1) & 1, out = t & 1;
+        const float *M = leaf + ((size_t)b * L + (t - 1)) * (size_t)S * S;
+        for (int c0 = 0; c0 < S; c0 += CB) {
+            const int col = c0 + c;
+            fa_xacc x;
+            x.init();
+            if (col < S)
+                for (int q = qs; q < S; q += QS) {
+                    const float a = va[in][q], v = __ldg(M + (size_t)q * S + col);
+                    if (a > 0.0f && v > 0.0f) {
+                        float mv;
+                        int ev;
+                        fa_split(v, mv, ev);
+                        x.add(a * mv, ve[in][q] + ev);
+                    }
+                }
+            pm[qs * CB + c] = x.acc;
+            pe[qs * CB + c] = x.E;
+            __syncthreads();
+            if (qs == 0 && col < S) {
+                fa_xacc y;
+                y.init();
+                for (int r = 0; r < QS; ++r) y.merge(pm[r * CB + c], pe[r * CB + c]);
+                float mo;
+                int eo;
+                y.normalised(mo, eo);
+                va[out][col] = mo; ve[out][col] = eo;
+                am[base + (size_t)t * S + col] = mo; ae[base + (size_t)t * S + col] = eo;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kChThreads) k_chain_backward(DevFA fa, int L, const float *__restrict__ leaf,
+                                                              const float *__restrict__ am,
+                                                              const int32_t *__restrict__ ae, float *bm, int32_t *be,
+                                                              int32_t *z, uint64_t seed, uint64_t offset, double *logZ,
+                                                              int32_t *status, float *zsum_ws, int32_t *zexp_ws) {
+    extern __shared__ float ch_s[];
+    __shared__ int zcur, alive;
+    const int S = fa.S, b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float *vb[2] = {ch_s, ch_s + S};
+    int *vbe[2] = {reinterpret_cast<int *>(ch_s + 2 * S), reinterpret_cast<int *>(ch_s + 3 * S)};
+    const size_t base = (size_t)b * (L + 1) * S;
+    int32_t *zb = z + (size_t)b * (L + 1);
+    for (int q = tid; q < S; q += kChThreads) {
+        const float b0 = fa.accept_mask[q] ? 1.0f : 0.0f;
+        bm[base + (size_t)L * S + q] = b0; be[base + (size_t)L * S + q] = 0;
+        vb[L & 1][q] = b0; vbe[L & 1][q] = 0;
+    }
+    // the end state and logZ from alpha_L over the accepting states
+    if (warp == 0) {
+        const float *aL = am + base + (size_t)L * S;
+        const int32_t *eL = ae + base + (size_t)L * S;
+        int emax = FA_INT_NONE;
+        for (int i = lane; i < fa.n_accept; i += 32) {
+            const int f = fa.accept[i];
+            if (aL[f] > 0.0f) emax = max(emax, eL[f]);
+        }
+        emax = fa_warp_max_int(emax);
+        int pick = -1;
+        float tot = 0.0f;
+        if (emax != FA_INT_NONE) {
+            auto w = [&](int i) { const int f = fa.accept[i]; return aL[f] > 0.0f ? aL[f] * fa_pow2(eL[f] - emax) : 0.0f; };
+            const float u = fa_uniform(seed, offset, 0u, (uint32_t)b, FA_RNG_ROOT);
+            pick = warp_categorical(fa.n_accept, u, w);
+            for (int i = lane; i < fa.n_accept; i += 32) tot += w(i);
+            tot = fa_warp_sum(tot);
+        }
+        if (lane == 0) {
+            zb[0] = fa.start;
+            if (pick < 0 || !(tot > 0.0f)) {
+                status[b] = FA_ROW_EMPTY;
+                logZ[b] = -INFINITY;
+                zsum_ws[b] = 0.0f;
+                zexp_ws[b] = 0;
+                alive = 0;
+            } else {
+                status[b] = FA_ROW_OK;
+                logZ[b] = (double)emax * 0.69314718055994530942 + log((double)tot);
+                zsum_ws[b] = tot;
+                zexp_ws[b] = emax;
+                zcur = fa.accept[pick];
+                zb[L] = zcur;
+                alive = 1;
+            }
+        }
+    }
+    __syncthreads();
+    if (!alive) {
+        for (int t = tid; t <= L; t += kChThreads) zb[t] = fa.start;   // keep every state in range
+        return;
+    }
+    for (int t = L; t >= 1; --t) {
+        const int in = t & 1, out = (t - 1) & 1;
+        const float *M = leaf + ((size_t)b * L + (t - 1)) * (size_t)S * S;
+        // beta_{t-1}(s) = sum_d M_t(s, d) beta_t(d), one warp per row
+        for (int r = warp; r < S; r += kChWarps) {
+            fa_xacc x;
+            x.init();
+            for (int d = lane; d < S; d += 32) {
+                const float v = __ldg(M + (size_t)r * S + d), bq = vb[in][d];
+                if (v > 0.0f && bq > 0.0f) {
+                    float mv;
+                    int ev;
+                    fa_split(v, mv, ev);
+                    x.add(bq * mv, vbe[in][d] + ev);
+                }
+            }
+            x.warp_reduce();
+            if (lane == 0) {
+                float mo;
+                int eo;
+                x.normalised(mo, eo);
+                vb[out][r] = mo; vbe[out][r] = eo;
+                bm[base + (size_t)(t - 1) * S + r] = mo; be[base + (size_t)(t - 1) * S + r] = eo;
+            }
+        }
+        // z_{t-1} ~ alpha_{t-1}(s) M_t(s, z_t) (warp 0; the other warps' rows do not need it)
+        if (warp == 0 && t > 1) {
+            const int zt = zcur;
+            const float *a = am + base + (size_t)(t - 1) * S;
+            const int32_t *ea = ae + base + (size_t)(t - 1) * S;
+            int emax = FA_INT_NONE;
+            for (int q = lane; q < S; q += 32) {
+                const float v = __ldg(M + (size_t)q * S + zt);
+                if (a[q] > 0.0f && v > 0.0f) emax = max(emax, ea[q] + fa_exponent(v));
+            }
+            emax = fa_warp_max_int(emax);
+            int pick = -1;
+            if (emax != FA_INT_NONE) {
+                const float u = fa_uniform(seed, offset, (uint32_t)(t - 1), (uint32_t)b, FA_RNG_MID);
+                pick = warp_categorical(S, u, [&](int q) {
+                    const float v = __ldg(M + (size_t)q * S + zt);
+                    if (!(a[q] > 0.0f && v > 0.0f)) return 0.0f;
+                    float mv;
+                    int ev;
+                    fa_split(v, mv, ev);
+                    return a[q] * mv * fa_pow2(ea[q] + ev - emax);
+                });
+            }
+            if (lane == 0) {
+                if (pick < 0) { status[b] = FA_ROW_UNDERFLOW; pick = fa.start; }
+                zb[t - 1] = pick;
+                zcur = pick;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // ----------------------------------------------------------------------------- 6. commit
 
 // Per sequence, the k masked positions of [lo, hi) with the largest marginal, descending,
@@ -1338,12 +1527,39 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
                                   row_status, stream);
 }
 
+namespace {
+fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *probs, const int32_t *committed,
+                    uint64_t philox_seed, uint64_t philox_offset, int32_t k, int32_t commit_lo, int32_t commit_hi,
+                    int32_t confidence, void *workspace, size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
+                    float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream, bool chain);
+}
+
 extern "C" fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
                                             const int32_t *committed, uint64_t philox_seed, uint64_t philox_offset,
                                             int32_t k, int32_t commit_lo, int32_t commit_hi, int32_t confidence,
                                             void *workspace, size_t ws_bytes, int32_t *tokens, double *logZ,
                                             float *marg, float *entropy, int32_t *commit_idx, int32_t *row_status,
                                             fa_stream stream) {
+    return step_impl(aut, B, L, probs, committed, philox_seed, philox_offset, k, commit_lo, commit_hi, confidence,
+                     workspace, ws_bytes, tokens, logZ, marg, entropy, commit_idx, row_status, stream, false);
+}
+
+extern "C" fa_status fa_constrained_step_chain(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                               const int32_t *committed, uint64_t philox_seed,
+                                               uint64_t philox_offset, int32_t k, int32_t commit_lo,
+                                               int32_t commit_hi, int32_t confidence, void *workspace,
+                                               size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
+                                               float *entropy, int32_t *commit_idx, int32_t *row_status,
+                                               fa_stream stream) {
+    return step_impl(aut, B, L, probs, committed, philox_seed, philox_offset, k, commit_lo, commit_hi, confidence,
+                     workspace, ws_bytes, tokens, logZ, marg, entropy, commit_idx, row_status, stream, true);
+}
+
+namespace {
+fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *probs, const int32_t *committed,
+                    uint64_t philox_seed, uint64_t philox_offset, int32_t k, int32_t commit_lo, int32_t commit_hi,
+                    int32_t confidence, void *workspace, size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
+                    float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream, bool chain) {
     if (!aut) { fa_set_error("fa_constrained_step: NULL automaton"); return FA_ERR_INVALID_ARG; }
     if (confidence != FA_CONF_MARGINAL && confidence != FA_CONF_NEG_ENTROPY && confidence != FA_CONF_UNCONSTRAINED) {
         fa_set_error("fa_constrained_step: unknown confidence"); return FA_ERR_INVALID_ARG;
@@ -1381,9 +1597,28 @@ extern "C" fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, 
                          (long)(p.rmax_hi_bytes / sizeof(int32_t)));
     if (st != FA_OK) return st;
 
+    if (chain) {
+        // 2-4, chain form: forward messages, then backward messages with the state draws
+        stage_mark(1, s);
+        const size_t fsm = chain_smem(S, true), bsm = chain_smem(S, false);
+        if (fsm > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(k_chain_forward, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_chain_backward, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsm);
+            if (e != cudaSuccess) { fa_set_error(std::string("chain smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+        }
+        k_chain_forward<<<B, kChThreads, fsm, s>>>(dev_view(aut), L, F(p.mant[0]), F(p.am), I(p.ae));
+        if ((st = launch_check("chain forward")) != FA_OK) return st;
+        stage_mark(2, s);
+        k_chain_backward<<<B, kChThreads, bsm, s>>>(dev_view(aut), L, F(p.mant[0]), F(p.am), I(p.ae), F(p.bm),
+                                                    I(p.be), I(p.z), philox_seed, philox_offset, logZ, row_status,
+                                                    F(p.zsum), I(p.zexp));
+        if ((st = launch_check("chain backward")) != FA_OK) return st;
+    }
+
     // 2. up-sweep: level k from level k-1
-    stage_mark(1, s);
-    for (int kk = 1; kk <= p.K; ++kk) {
+    if (!chain) stage_mark(1, s);
+    for (int kk = 1; kk <= p.K && !chain; ++kk) {
         if (S <= SMALL_S) {
             const long tpd = (S + ST - 1) / ST;
             k_span_small<<<(unsigned)((long)B * p.nk[kk] * tpd * tpd), kThreads, 0, s>>>(
@@ -1412,14 +1647,14 @@ extern "C" fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, 
     }
 
     // 3. root: logZ, end state, boundary messages
-    stage_mark(2, s);
-    k_root<<<B, kThreads, 0, s>>>(dev_view(aut), L, p.K, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), philox_seed,
+    if (!chain) stage_mark(2, s);
+    if (!chain) k_root<<<B, kThreads, 0, s>>>(dev_view(aut), L, p.K, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), philox_seed,
                                   philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.zsum), I(p.zexp),
                                   logZ, row_status, I(p.tc_err));
-    if ((st = launch_check("root")) != FA_OK) return st;
+    if (!chain && (st = launch_check("root")) != FA_OK) return st;
 
     // 4. top-down: midpoints and prefix/suffix messages, level K-1 .. 0
-    for (int kk = p.K - 1; kk >= 0; --kk) {
+    for (int kk = p.K - 1; kk >= 0 && !chain; --kk) {
         TopdownArgs ta;
         ta.S = S; ta.B = B; ta.L = L; ta.k = kk; ta.nc = p.nk[kk]; ta.np = p.nk[kk + 1];
         ta.CB = S >= 64 ? 64 : ((S + 31) / 32) * 32;
@@ -1453,6 +1688,7 @@ extern "C" fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, 
     stage_mark(4, s);
     return st;
 }
+}  // namespace
 
 extern "C" fa_status fa_profile_enable(int32_t enable) {
     if (enable && !g_stage.created) {

@@ -29,7 +29,8 @@ CONFIDENCE = {"marginal": FA_CONF_MARGINAL, "neg_entropy": FA_CONF_NEG_ENTROPY,
 
 # every entry point include/fa.h declares
 EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_workspace_bytes",
-           "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_ex", "fa_token_marginals",
+           "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_ex", "fa_constrained_step_chain",
+           "fa_token_marginals",
            "fa_apply_commits", "fa_constrained_step_noalloc",
            "fa_profile_enable", "fa_profile_read",
            "fa_launch_count", "fa_last_error")
@@ -72,6 +73,8 @@ def load(path: str = LIB_PATH):
     lib.fa_constrained_step.restype = st
     lib.fa_constrained_step_ex.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, i32, P, sz, P, P, P, P, P, P, P]
     lib.fa_constrained_step_ex.restype = st
+    lib.fa_constrained_step_chain.argtypes = lib.fa_constrained_step_ex.argtypes
+    lib.fa_constrained_step_chain.restype = st
     lib.fa_token_marginals.argtypes = [P, i32, i32, P, P, P, sz, P, P, P, P]
     lib.fa_token_marginals.restype = st
     lib.fa_apply_commits.argtypes = [i32, i32, i32, P, P, P, P]
@@ -206,13 +209,15 @@ def fa_constrained_step(aut: CompiledAutomaton, probs, committed, philox_seed: i
 
 def fa_constrained_step_ex(aut: CompiledAutomaton, probs, committed, philox_seed: int, philox_offset: int, k: int,
                            commit_lo: int, commit_hi: int, confidence: str, workspace, tokens, logZ, marg, entropy,
-                           commit_idx, row_status, stream=None):
+                           commit_idx, row_status, stream=None, method: str = "tree"):
     """fa_constrained_step with a remasking confidence ("marginal", "neg_entropy" or
-    "unconstrained") and an optional entropy output [B, L] (None to skip)."""
+    "unconstrained"), an optional entropy output [B, L] (None to skip), and the tree
+    (fa_constrained_step_ex) or chain (fa_constrained_step_chain) form of the step."""
     import torch
     B, L, V = probs.shape
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(_lib.fa_constrained_step_ex(
+    fn = {"tree": _lib.fa_constrained_step_ex, "chain": _lib.fa_constrained_step_chain}[method]
+    _check(fn(
         aut.handle, B, L, _dev(probs, torch.float32, "probs", (B, L, aut.vocab)),
         _dev(committed, torch.int32, "committed", (B, L)), ctypes.c_uint64(philox_seed & (2 ** 64 - 1)),
         ctypes.c_uint64(philox_offset & (2 ** 64 - 1)), int(k), int(commit_lo), int(commit_hi),
@@ -253,10 +258,13 @@ class ConstrainedStep:
     """Convenience owner of the workspace and output tensors for a fixed (B, L, k)."""
 
     def __init__(self, aut: CompiledAutomaton, B: int, L: int, k: int, device="cuda", confidence: str = "marginal",
-                 want_entropy: bool = False):
+                 want_entropy: bool = False, method: str = "tree"):
         import torch
         if confidence not in CONFIDENCE:
             raise ValueError("confidence must be one of %s" % sorted(CONFIDENCE))
+        if method not in ("tree", "chain"):
+            raise ValueError("method must be 'tree' or 'chain'")
+        self.method = method
         self.aut, self.B, self.L, self.k = aut, B, L, k
         self.confidence = confidence
         self.entropy = torch.empty((B, L), dtype=torch.float32, device=device) if want_entropy else None
@@ -271,13 +279,13 @@ class ConstrainedStep:
     def __call__(self, probs, committed, seed: int, offset: int = 0, lo: int = 0, hi: Optional[int] = None,
                  stream=None):
         hi = self.L if hi is None else hi
-        if self.confidence == "marginal" and self.entropy is None:
+        if self.method == "tree" and self.confidence == "marginal" and self.entropy is None:
             fa_constrained_step(self.aut, probs, committed, seed, offset, self.k, lo, hi, self.workspace, self.tokens,
                                 self.logZ, self.marg, self.commit_idx, self.row_status, stream)
         else:
             fa_constrained_step_ex(self.aut, probs, committed, seed, offset, self.k, lo, hi, self.confidence,
                                    self.workspace, self.tokens, self.logZ, self.marg, self.entropy, self.commit_idx,
-                                   self.row_status, stream)
+                                   self.row_status, stream, method=self.method)
         return self.tokens, self.logZ, self.marg, self.commit_idx, self.row_status
 
     def token_marginals(self, probs, committed, stream=None):

@@ -221,6 +221,23 @@ fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, int32_t L, 
                                  float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream);
 
 /*
+ * fa_constrained_step_chain -- the same step computed in chain form: forward messages
+ * alpha_t = alpha_{t-1} M_t for t = 1..L, then backward messages beta_{t-1} = M_t beta_t with
+ * forward-filtering backward-sampling of the states (z_L ~ alpha_L restricted to F,
+ * z_{t-1} ~ alpha_{t-1}(s) M_t(s, z_t)).  This is the O(L)-depth chain that the paperfeed.app
+ * summary ("The scan trick") and key design 2 of the papernotes.org notes replace by the
+ * log-depth tree; it samples the same distribution with O(L S^2) instead of O(L S^3) work,
+ * one sequence per thread block.  Arguments, workspace size and outputs are those of
+ * fa_constrained_step_ex; the draws differ from the tree's for the same seed (another
+ * sequence of Philox counters), the distribution does not.
+ */
+fa_status fa_constrained_step_chain(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                    const int32_t *committed, uint64_t philox_seed, uint64_t philox_offset,
+                                    int32_t k, int32_t commit_lo, int32_t commit_hi, int32_t confidence,
+                                    void *workspace, size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
+                                    float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream);
+
+/*
  * fa_token_marginals -- the full constrained marginal of every token at every position,
  *     p(x_t = v) = w_t(v) * sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / (same summed over v)
  * (key design 3 of the papernotes.org notes), from the prefix/suffix messages that the
