@@ -11,6 +11,7 @@ string for tiny cases.  Citations are in the C file's header.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 from typing import Optional
@@ -188,6 +189,80 @@ def confidence(mode: str, probs: np.ndarray, tokens: np.ndarray, marg_tokens: np
         tok = np.where(np.asarray(tokens) >= 0, tokens, 0)
         return np.asarray(probs, np.float64)[t, tok]
     raise ValueError(mode)
+
+
+def viterbi(fa, probs: np.ndarray, committed: Optional[np.ndarray] = None):
+    """Greedy (T = 0) constrained decoding of one sequence: the accepted string with the
+    largest mean-field product, argmax over x in C of prod_t w_t(x_t), by max-product over
+    (state path, string) along the chain (paperfeed.app summary: greedy decoding with the
+    constraint; the "greedy / MAP" variant of the same HMM).  Because the product depends
+    only on the string, the best (path, string) pair carries the best accepted string; NFA
+    path counts weight sampling and play no part here.  w_t is probs[t] at masked positions
+    and one-hot at committed ones.
+
+    Returns (score, tokens): score = ln of the maximum in float64 (-inf and tokens None when
+    no accepted string has positive weight)."""
+    probs = np.asarray(probs, np.float64)
+    L, V = probs.shape
+    S = fa.n_states
+    src = np.asarray(fa.edge_src, np.int64)
+    dst = np.asarray(fa.edge_dst, np.int64)
+    off = np.asarray(fa.label_offsets, np.int64)
+    lab = np.asarray(fa.label_tokens, np.int64)
+    E = src.shape[0]
+    with np.errstate(divide="ignore"):
+        logw = np.log(probs)
+    if committed is not None:
+        for t in range(L):
+            if committed[t] >= 0:
+                logw[t] = -np.inf
+                if committed[t] < V:
+                    logw[t, committed[t]] = 0.0
+    delta = np.full(S, -np.inf)
+    delta[fa.start] = 0.0
+    back_edge = np.zeros((L, S), np.int64)
+    back_tok = np.zeros((L, E), np.int64)
+    for t in range(L):
+        # the best token of every edge at position t
+        best = np.full(E, -np.inf)
+        for e in range(E):
+            toks = lab[off[e]:off[e + 1]]
+            if toks.shape[0]:
+                j = int(np.argmax(logw[t, toks]))
+                best[e] = logw[t, toks[j]]
+                back_tok[t, e] = toks[j]
+        cand = delta[src] + best
+        new = np.full(S, -np.inf)
+        for e in range(E):
+            if cand[e] > new[dst[e]]:
+                new[dst[e]] = cand[e]
+                back_edge[t, dst[e]] = e
+        delta = new
+    acc = np.asarray(fa.accept, np.int64)
+    f = int(acc[np.argmax(delta[acc])])
+    score = float(delta[f])
+    if score == -np.inf:
+        return score, None
+    out = np.zeros(L, np.int32)
+    s = f
+    for t in range(L - 1, -1, -1):
+        e = int(back_edge[t, s])
+        out[t] = back_tok[t, e]
+        s = int(src[e])
+    return score, out
+
+
+def string_log_weight(probs: np.ndarray, tokens: np.ndarray, committed: Optional[np.ndarray] = None) -> float:
+    """ln prod_t w_t(x_t) of a given string (w_t one-hot at committed positions)."""
+    probs = np.asarray(probs, np.float64)
+    tot = 0.0
+    for t, v in enumerate(tokens):
+        if committed is not None and committed[t] >= 0:
+            if v != committed[t]:
+                return -np.inf
+            continue
+        tot += math.log(probs[t, v]) if probs[t, v] > 0 else -np.inf
+    return tot
 
 
 def topk(marg: np.ndarray, committed: np.ndarray, k: int, lo: int, hi: int) -> np.ndarray:

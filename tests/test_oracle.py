@@ -212,6 +212,54 @@ def test_confidence_modes():
     assert (r["marg_tokens"] <= 1 + 1e-12).all()
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_viterbi_matches_brute_force(seed):
+    """The greedy score is the largest mean-field product over the accepted strings, found
+    by enumerating V^L; the returned string is accepted and attains it."""
+    rng = np.random.default_rng(100 + seed)
+    S, V, L = int(rng.integers(2, 6)), int(rng.integers(2, 6)), int(rng.integers(1, 6))
+    fa = synth.tiny_random_fa(rng, S, V, n_edges=int(rng.integers(S, 3 * S + 1)), max_label=V,
+                              n_accept=int(rng.integers(1, S + 1)))
+    probs = synth.gaussian_probs(rng, 1, L, V, 1.5)[0]
+    committed = np.full(L, -1, np.int32)
+    if seed % 2:
+        committed[rng.choice(L, size=(L + 1) // 2, replace=False)] = rng.integers(0, V, size=(L + 1) // 2)
+    strings = brute.all_strings(V, L)
+    ok = brute.path_counts(fa, strings) > 0
+    for t in range(L):
+        if committed[t] >= 0:
+            ok &= strings[:, t] == committed[t]
+    lw = np.array([oracle.string_log_weight(probs, x, committed) for x in strings])
+    score, x = oracle.viterbi(fa, probs, committed)
+    if not ok.any() or not np.isfinite(lw[ok]).any():
+        assert score == -np.inf and x is None
+        return
+    best = lw[ok].max()
+    assert abs(score - best) <= 1e-12 * max(1.0, abs(best))
+    assert oracle.OracleFA(fa).accepts(x)
+    assert abs(oracle.string_log_weight(probs, x, committed) - best) <= 1e-12 * max(1.0, abs(best))
+
+
+def test_viterbi_unconstrained_is_per_position_argmax():
+    rng = np.random.default_rng(8)
+    V, L = 30, 6
+    probs = synth.gaussian_probs(rng, 1, L, V, 2.0)[0]
+    score, x = oracle.viterbi(synth.single_state_fa(V), probs)
+    np.testing.assert_array_equal(x, probs.argmax(axis=1))
+    assert abs(score - np.log(probs.max(axis=1).astype(np.float64)).sum()) < 1e-12
+
+
+def test_viterbi_avoids_dotdot():
+    """Real-number DFA, L=2, both positions preferring '.' then '1': "1." and ".." are not
+    numbers, so the greedy constrained string is "11"."""
+    probs = np.full((2, 12), 0.01, np.float32)
+    probs[:, synth.DOT] = 0.5
+    probs[:, 1] = 0.4
+    score, x = oracle.viterbi(synth.real_number_dfa(), probs)
+    assert x.tolist() == [1, 1]
+    assert abs(score - 2 * math.log(np.float32(0.4))) < 1e-12
+
+
 def test_duplicated_edges_double_every_path():
     """NFA path counting (page 1, "Arbitrary schedules and NFAs"): duplicating every edge
     multiplies each accepted string's path count by 2^L, so logZ grows by L ln 2 and
