@@ -160,6 +160,9 @@ __device__ int warp_categorical(int n, float u, WF w) {
 // each run end, moves the running sum into the run's slot, so every run's slots collect
 // one sum per chunk in chunk order.  After the last chunk every cell adds its runs' slots
 // in a fixed order, so the result is deterministic.
+// MAX = true: the max-product variant for greedy decoding, M_t(s, s') = max over the tokens of
+// the edges s -> s' of w_t(v) (a committed position: 1 where an edge carries its token).
+template <bool MAX>
 __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
                                                                     const int32_t *__restrict__ committed,
                                                                     const int4 *__restrict__ rbm, int nrb, int max_units,
@@ -230,9 +233,11 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
 #define FA_RW_GROUP(V)                                                                                 \
     {                                                                                                  \
         const uint32_t x_ = (V).x, y_ = (V).y;                                                         \
-        const float p0_ = smem_f[boff + (int)(x_ & 0x7fffu)] + smem_f[boff + (int)((x_ >> 16) & 0x7fffu)]; \
-        const float p1_ = smem_f[boff + (int)(y_ & 0x7fffu)] + smem_f[boff + (int)((y_ >> 16) & 0x7fffu)]; \
-        acc += p0_ + p1_;                                                                              \
+        const float q0_ = smem_f[boff + (int)(x_ & 0x7fffu)], q1_ = smem_f[boff + (int)((x_ >> 16) & 0x7fffu)]; \
+        const float q2_ = smem_f[boff + (int)(y_ & 0x7fffu)], q3_ = smem_f[boff + (int)((y_ >> 16) & 0x7fffu)]; \
+        const float p0_ = MAX ? fmaxf(q0_, q1_) : q0_ + q1_;                                           \
+        const float p1_ = MAX ? fmaxf(q2_, q3_) : q2_ + q3_;                                           \
+        if constexpr (MAX) acc = fmaxf(acc, fmaxf(p0_, p1_)); else acc += p0_ + p1_;                   \
         asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.shared.f32 [%1], %0;\n\t"  \
                      "@p mov.f32 %0, 0f00000000;\n\t@p add.u32 %1, %1, 128;\n\t}"                   \
                      : "+f"(acc), "+r"(slot_addr)                                                      \
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
 #pragma unroll
                 for (int q = 0; q < FA_RUN_SLOTS; ++q) {
                     if (q >= nrun) break;
-                    tot[q] += my[q * 32];
+                    if constexpr (MAX) tot[q] = fmaxf(tot[q], my[q * 32]); else tot[q] += my[q * 32];
                 }
             }
         }
@@ -281,7 +286,9 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
             const int s = fa.cell_src[cell];
             const float *sb = slots + (size_t)(fa.row_unit0[s] - u0) * FA_UNIT_SLOTS;
             float v = 0.0f;
-            for (int q = fa.crun_off[cell]; q < fa.crun_off[cell + 1]; ++q) v += sb[fa.crun_slot[q]];
+            for (int q = fa.crun_off[cell]; q < fa.crun_off[cell + 1]; ++q) {
+                if constexpr (MAX) v = fmaxf(v, sb[fa.crun_slot[q]]); else v += sb[fa.crun_slot[q]];
+            }
             M[(size_t)s * S + fa.cell_dst[cell]] = v;
             atomicMax(&smax[s - r0], __float_as_int(v));
         }
@@ -293,7 +300,10 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
             for (int64_t j = a0 + tid; j < a1; j += nthr) {
                 const int e = fa.tok_edges[j];
                 const int s = fa.edge_src[e];
-                if (s >= r0 && s < r1) atomicAdd(&M[(size_t)s * S + fa.edge_dst[e]], 1.0f);
+                if (s >= r0 && s < r1) {
+                    if constexpr (MAX) M[(size_t)s * S + fa.edge_dst[e]] = 1.0f;
+                    else atomicAdd(&M[(size_t)s * S + fa.edge_dst[e]], 1.0f);
+                }
             }
             __syncthreads();
             for (int64_t j = a0 + tid; j < a1; j += nthr) {
@@ -351,6 +361,7 @@ __global__ void __launch_bounds__(kThreads) k_rowshift(int S, int L, int k, int 
 constexpr int SMALL_S = 64;
 constexpr int ST = 32;
 
+template <bool MAX>
 __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                        const int32_t *__restrict__ rho_c,
                                                        const int32_t *__restrict__ rmax_c, int nc, float *mant_p,
@@ -431,8 +442,13 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
     for (int m = 0; m < S; ++m) {
         const float a0 = As[2 * ty][m], a1 = As[2 * ty + 1][m];
         const float b0 = Bs[m][2 * tx], b1 = Bs[m][2 * tx + 1];
-        c00 = fmaf(a0, b0, c00); c01 = fmaf(a0, b1, c01);
-        c10 = fmaf(a1, b0, c10); c11 = fmaf(a1, b1, c11);
+        if constexpr (MAX) {
+            c00 = fmaxf(c00, a0 * b0); c01 = fmaxf(c01, a0 * b1);
+            c10 = fmaxf(c10, a1 * b0); c11 = fmaxf(c11, a1 * b1);
+        } else {
+            c00 = fmaf(a0, b0, c00); c01 = fmaf(a0, b1, c01);
+            c10 = fmaf(a1, b0, c10); c11 = fmaf(a1, b1, c11);
+        }
     }
     const float cv[2][2] = {{c00, c01}, {c10, c11}};
 #pragma unroll
@@ -463,6 +479,7 @@ constexpr int GBM = 64, GBN = 64, GBK = 16;
 
 // C̃ = (Ã_L prescaled per (row, m)) x Ã_R in fp32 FMA, 64x64 tiles, 4x4 per thread.  A
 // product whose right child lies wholly in the padding beyond L is a copy of the left child.
+template <bool MAX>
 __global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                       const int32_t *__restrict__ rho_c,
                                                       const int32_t *__restrict__ rmax_c, int nc,
@@ -533,7 +550,10 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int
 #pragma unroll
             for (int p = 0; p < 4; ++p)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(a[p], bb[q], acc[p][q]);
+                for (int q = 0; q < 4; ++q) {
+                    if constexpr (MAX) acc[p][q] = fmaxf(acc[p][q], a[p] * bb[q]);
+                    else acc[p][q] = fmaf(a[p], bb[q], acc[p][q]);
+                }
         }
         __syncthreads();
     }
@@ -1321,6 +1341,150 @@ __global__ void __launch_bounds__(kChThreads) k_chain_backward(DevFA fa, int L, 
     }
 }
 
+// ----------------------------------------------------------------------------- greedy (MAP) decoding
+
+// Greedy (T = 0) decoding by max-product over the same tree (the max-product reweight and span
+// products above; paperfeed.app summary, greedy decoding under the constraint): the root takes
+// the best accepting end state, every midpoint the best state given its segment's ends, every
+// leaf the best token of the chosen edge set.  Ties go to the lowest index everywhere.
+
+// Warp argmax of w(i) > 0 over i < n, the lowest index among equal values; -1 if none is
+// positive.  *best gets the maximum.
+template <class WF>
+__device__ int warp_argmax(int n, WF w, float *best) {
+    float bv = 0.0f;
+    int bi = -1;
+    for (int i = (threadIdx.x & 31); i < n; i += 32) {
+        const float x = w(i);
+        if (x > bv) { bv = x; bi = i; }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) { bv = ov; bi = oi; }
+    }
+    *best = bv;
+    return bi;
+}
+
+__global__ void __launch_bounds__(32) k_map_root(DevFA fa, int L, int nK, const float *__restrict__ mant_root,
+                                                 const int32_t *__restrict__ rho_root, int32_t *z, double *score,
+                                                 int32_t *status) {
+    const int b = blockIdx.x, S = fa.S, s0 = fa.start;
+    const float *row = mant_root + (size_t)b * nK * S * S + (size_t)s0 * S;
+    float best;
+    const int pick = warp_argmax(fa.n_accept, [&](int i) { return row[fa.accept[i]]; }, &best);
+    if (threadIdx.x == 0) {
+        const size_t bnd0 = (size_t)b * (L + 1);
+        z[bnd0] = s0;
+        if (pick < 0) {
+            status[b] = FA_ROW_EMPTY;
+            score[b] = -INFINITY;
+            z[bnd0 + L] = s0;
+        } else {
+            status[b] = FA_ROW_OK;
+            score[b] = (double)rho_root[(size_t)b * nK * S + s0] * 0.69314718055994530942 + log((double)best);
+            z[bnd0 + L] = fa.accept[pick];
+        }
+    }
+}
+
+// Level k: the midpoint m of every node [l, r) takes argmax_s A[l, m)[z_l, s] A[m, r)[s, z_r].
+__global__ void __launch_bounds__(kThreads) k_map_midpoints(int S, int B, int L, int k, int nc, int np,
+                                                          const float *__restrict__ mant,
+                                                          const int32_t *__restrict__ rho, int32_t *z,
+                                                          int32_t *status) {
+    const long gw = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (gw >= (long)B * np) return;
+    const int b = (int)(gw / np), j = (int)(gw % np);
+    const int l = j << (k + 1), m = l + (1 << k);
+    if (m >= L) return;
+    const int r = min(l + (1 << (k + 1)), L);
+    if (__shfl_sync(0xffffffffu, status[b], 0) != FA_ROW_OK) return;
+    const int32_t *zb = z + (size_t)b * (L + 1);
+    const int zl = zb[l], zr = zb[r];
+    const size_t lnode = (size_t)b * nc + 2 * j, rnode = lnode + 1;
+    const float *Lrow = mant + lnode * (size_t)S * S + (size_t)zl * S;
+    const float *R = mant + rnode * (size_t)S * S;
+    const int32_t *rhoR = rho + rnode * S;
+    const int lane = threadIdx.x & 31;
+    int emax = FA_INT_NONE;
+    for (int q = lane; q < S; q += 32) {
+        const float x = Lrow[q], y = R[(size_t)q * S + zr];
+        if (x > 0.0f && y > 0.0f) emax = max(emax, rhoR[q] + fa_exponent(x) + fa_exponent(y));
+    }
+    emax = fa_warp_max_int(emax);
+    int pick = -1;
+    if (emax != FA_INT_NONE) {
+        float best;
+        pick = warp_argmax(S, [&](int q) {
+            const float x = Lrow[q], y = R[(size_t)q * S + zr];
+            if (!(x > 0.0f && y > 0.0f)) return 0.0f;
+            float mx, my;
+            int ex, ey;
+            fa_split(x, mx, ex);
+            fa_split(y, my, ey);
+            return mx * my * fa_pow2(rhoR[q] + ex + ey - emax);
+        }, &best);
+    }
+    if (lane == 0) {
+        if (pick < 0) status[b] = FA_ROW_UNDERFLOW;
+        else z[(size_t)b * (L + 1) + m] = pick;
+    }
+}
+
+// Leaves: the best token of the cell z_{t-1} -> z_t (committed positions echo their token).
+__global__ void __launch_bounds__(kThreads) k_map_leaf(DevFA fa, int B, int L, const float *__restrict__ probs,
+                                                     const int32_t *__restrict__ committed,
+                                                     const int32_t *__restrict__ z, int32_t *tokens,
+                                                     int32_t *status) {
+    const long gw = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (gw >= (long)B * L) return;
+    const int b = (int)(gw / L), t = (int)(gw % L), lane = threadIdx.x & 31;
+    const size_t pos = (size_t)b * L + t;
+    const int c = committed[pos];
+    if (c >= 0) {
+        if (lane == 0) tokens[pos] = c;
+        return;
+    }
+    if (__shfl_sync(0xffffffffu, status[b], 0) != FA_ROW_OK) {
+        if (lane == 0) tokens[pos] = -1;
+        return;
+    }
+    const int32_t *zb = z + (size_t)b * (L + 1);
+    const int zp = zb[t], zn = zb[t + 1];
+    int lo = fa.row_cell_off[zp], hi = fa.row_cell_off[zp + 1];
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (fa.cell_dst[mid] < zn) lo = mid + 1; else hi = mid;
+    }
+    int v = -1;
+    if (lo < fa.row_cell_off[zp + 1] && fa.cell_dst[lo] == zn) {
+        const int64_t a0 = fa.cell_off[lo];
+        const int n = (int)(fa.cell_off[lo + 1] - a0);
+        const float *prow = probs + pos * (size_t)fa.V;
+        float best;
+        const int pick = warp_argmax(n, [&](int i) { return __ldg(prow + fa.cell_tok[a0 + i]); }, &best);
+        if (pick >= 0) v = fa.cell_tok[a0 + pick];
+    }
+    if (lane == 0) {
+        tokens[pos] = v;
+        if (v < 0) status[b] = FA_ROW_UNDERFLOW;
+    }
+}
+
+// Sequences that failed: -1 at every masked position and a score of -inf.
+__global__ void k_map_fix(int B, int L, const int32_t *__restrict__ committed, const int32_t *__restrict__ status,
+                          int32_t *tokens, double *score) {
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long)B * L) return;
+    const int b = (int)(i / L), t = (int)(i % L);
+    if (status[b] == FA_ROW_OK) return;
+    if (committed[i] < 0) tokens[i] = -1;
+    if (t == 0) score[b] = -INFINITY;
+}
+
 // ----------------------------------------------------------------------------- 6. commit
 
 // Per sequence, the k masked positions of [lo, hi) with the largest marginal, descending,
@@ -1437,7 +1601,7 @@ fa_status check_device(const fa_automaton *a, const char *fn) {
 
 fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *probs, const int32_t *committed,
                           float *mant, int32_t *rho, int32_t *rmax, cudaStream_t st, int32_t *zero = nullptr,
-                          long n_zero = 0) {
+                          long n_zero = 0, bool use_max = false) {
     const int p = pick_partition(a, (long)B * L);
     const int nrb = a->part_count[p];
     const int4 *rbm = reinterpret_cast<const int4 *>(a->rb_meta) + 2 * a->part_first[p];
@@ -1447,11 +1611,13 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     const size_t smem = sizeof(float) * (std::max((size_t)((a->chunk_tokens + 4) & ~3), (size_t)a->part_max_rows[p]) +
                                          (size_t)max_units * FA_UNIT_SLOTS);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_reweight, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(k_reweight<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_reweight<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) { fa_set_error(std::string("reweight smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     }
     dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
-    k_reweight<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, max_units, mant, rho, rmax,
+    (use_max ? k_reweight<true> : k_reweight<false>)<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, max_units, mant, rho, rmax,
                                             zero, n_zero);
     return launch_check("reweight");
 }
@@ -1496,6 +1662,69 @@ extern "C" fa_status fa_token_marginals(const fa_automaton *aut, int32_t B, int3
     if (((uintptr_t)workspace & 255) != 0) { fa_set_error("fa_token_marginals: workspace not 256-byte aligned"); return FA_ERR_INVALID_ARG; }
     return launch_token_marginals(aut, B, L, probs, committed, p, (const char *)workspace, row_status, marg_all, entropy,
                                   nullptr, (cudaStream_t)stream);
+}
+
+extern "C" fa_status fa_map_step(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
+                                 const int32_t *committed, void *workspace, size_t ws_bytes, int32_t *tokens,
+                                 double *score, int32_t *row_status, fa_stream stream) {
+    if (!aut) { fa_set_error("fa_map_step: NULL automaton"); return FA_ERR_INVALID_ARG; }
+    if (B < 0 || B > 65535 || L < 0 || L > FA_MAX_LENGTH) { fa_set_error("fa_map_step: B or L out of range"); return FA_ERR_INVALID_ARG; }
+    if (B == 0) return FA_OK;
+    if (!score || !row_status || (L > 0 && (!probs || !committed || !tokens))) {
+        fa_set_error("fa_map_step: NULL buffer"); return FA_ERR_INVALID_ARG;
+    }
+    fa_status st = check_device(aut, "fa_map_step");
+    if (st != FA_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (L == 0) {
+        k_empty_length<<<(B + 255) / 256, 256, 0, s>>>(aut->start, aut->accept_mask, B, 0, score, row_status, nullptr);
+        return launch_check("empty length");
+    }
+    const Plan p = make_plan(aut, B, L);
+    if (!workspace || ws_bytes < p.total) {
+        fa_set_error("fa_map_step: workspace needs " + std::to_string(p.total) + " bytes");
+        return FA_ERR_WORKSPACE_TOO_SMALL;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { fa_set_error("fa_map_step: workspace not 256-byte aligned"); return FA_ERR_INVALID_ARG; }
+    char *ws = (char *)workspace;
+    auto F = [&](size_t off) { return (float *)(ws + off); };
+    auto I = [&](size_t off) { return (int32_t *)(ws + off); };
+    const int S = aut->S;
+    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), s, I(p.rmax_hi),
+                         (long)(p.rmax_hi_bytes / sizeof(int32_t)), true);
+    if (st != FA_OK) return st;
+    for (int kk = 1; kk <= p.K; ++kk) {
+        if (S <= SMALL_S) {
+            const long tpd = (S + ST - 1) / ST;
+            k_span_small<true><<<(unsigned)((long)B * p.nk[kk] * tpd * tpd), kThreads, 0, s>>>(
+                S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), p.nk[kk - 1], F(p.mant[kk]),
+                I(p.rho[kk]), I(p.rmax[kk]));
+            if ((st = launch_check("span product (small, max)")) != FA_OK) return st;
+            continue;
+        }
+        dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
+        k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
+                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
+        if ((st = launch_check("rowshift")) != FA_OK) return st;
+        const long tiles = (S + GBN - 1) / GBN;
+        k_gemm_simt<true><<<(unsigned)((long)B * p.nk[kk] * tiles * tiles), kThreads, 0, s>>>(
+            S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), p.nk[kk - 1], I(p.mu[kk]),
+            F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]));
+        if ((st = launch_check("span product (max)")) != FA_OK) return st;
+    }
+    k_map_root<<<B, 32, 0, s>>>(dev_view(aut), L, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), I(p.z), score, row_status);
+    if ((st = launch_check("greedy root")) != FA_OK) return st;
+    for (int kk = p.K - 1; kk >= 0; --kk) {
+        const int np = p.nk[kk + 1];
+        k_map_midpoints<<<(unsigned)(((long)B * np + kWarps - 1) / kWarps), kThreads, 0, s>>>(
+            S, B, L, kk, p.nk[kk], np, F(p.mant[kk]), I(p.rho[kk]), I(p.z), row_status);
+        if ((st = launch_check("greedy midpoints")) != FA_OK) return st;
+    }
+    k_map_leaf<<<(unsigned)(((long)B * L + kWarps - 1) / kWarps), kThreads, 0, s>>>(dev_view(aut), B, L, probs, committed,
+                                                                              I(p.z), tokens, row_status);
+    if ((st = launch_check("greedy leaves")) != FA_OK) return st;
+    k_map_fix<<<(unsigned)(((long)B * L + 255) / 256), 256, 0, s>>>(B, L, committed, row_status, tokens, score);
+    return launch_check("greedy fix-up");
 }
 
 extern "C" fa_status fa_step_workspace_bytes(const fa_automaton *aut, int32_t B, int32_t L, size_t *bytes) {
@@ -1621,7 +1850,7 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
     for (int kk = 1; kk <= p.K && !chain; ++kk) {
         if (S <= SMALL_S) {
             const long tpd = (S + ST - 1) / ST;
-            k_span_small<<<(unsigned)((long)B * p.nk[kk] * tpd * tpd), kThreads, 0, s>>>(
+            k_span_small<false><<<(unsigned)((long)B * p.nk[kk] * tpd * tpd), kThreads, 0, s>>>(
                 S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), p.nk[kk - 1], F(p.mant[kk]),
                 I(p.rho[kk]), I(p.rmax[kk]));
             if ((st = launch_check("span product (small)")) != FA_OK) return st;
@@ -1641,7 +1870,7 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
         }
         const long tiles = (S + GBN - 1) / GBN;
         const long g2 = (long)B * p.nk[kk] * tiles * tiles;
-        k_gemm_simt<<<(unsigned)g2, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
+        k_gemm_simt<false><<<(unsigned)g2, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
                                             p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]));
         if ((st = launch_check("span product")) != FA_OK) return st;
     }

@@ -30,7 +30,7 @@ CONFIDENCE = {"marginal": FA_CONF_MARGINAL, "neg_entropy": FA_CONF_NEG_ENTROPY,
 # every entry point include/fa.h declares
 EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_workspace_bytes",
            "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_ex", "fa_constrained_step_chain",
-           "fa_token_marginals",
+           "fa_token_marginals", "fa_map_step",
            "fa_apply_commits", "fa_constrained_step_noalloc",
            "fa_profile_enable", "fa_profile_read",
            "fa_launch_count", "fa_last_error")
@@ -75,6 +75,8 @@ def load(path: str = LIB_PATH):
     lib.fa_constrained_step_ex.restype = st
     lib.fa_constrained_step_chain.argtypes = lib.fa_constrained_step_ex.argtypes
     lib.fa_constrained_step_chain.restype = st
+    lib.fa_map_step.argtypes = [P, i32, i32, P, P, P, sz, P, P, P, P]
+    lib.fa_map_step.restype = st
     lib.fa_token_marginals.argtypes = [P, i32, i32, P, P, P, sz, P, P, P, P]
     lib.fa_token_marginals.restype = st
     lib.fa_apply_commits.argtypes = [i32, i32, i32, P, P, P, P]
@@ -242,6 +244,36 @@ def fa_token_marginals(aut: CompiledAutomaton, probs, committed, workspace, row_
         _dev(row_status, torch.int32, "row_status", (B,)),
         _dev(marg_all, torch.float32, "marg_all", (B, L, aut.vocab)) if marg_all is not None else None,
         _dev(entropy, torch.float32, "entropy", (B, L)) if entropy is not None else None, _stream_ptr(stream)))
+
+
+def fa_map_step(aut: CompiledAutomaton, probs, committed, workspace, tokens, score, row_status, stream=None):
+    """Greedy (T = 0) constrained decoding: the accepted string with the largest mean-field
+    product (include/fa.h); all tensors on the current device."""
+    import torch
+    B, L, V = probs.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.fa_map_step(
+        aut.handle, B, L, _dev(probs, torch.float32, "probs", (B, L, aut.vocab)),
+        _dev(committed, torch.int32, "committed", (B, L)), _dev(workspace, workspace.dtype, "workspace"), ws_bytes,
+        _dev(tokens, torch.int32, "tokens", (B, L)), _dev(score, torch.float64, "score", (B,)),
+        _dev(row_status, torch.int32, "row_status", (B,)), _stream_ptr(stream)))
+
+
+class GreedyStep:
+    """Owner of the workspace and outputs of fa_map_step for a fixed (B, L)."""
+
+    def __init__(self, aut: CompiledAutomaton, B: int, L: int, device="cuda"):
+        import torch
+        self.aut, self.B, self.L = aut, B, L
+        nbytes = fa_step_workspace_bytes(aut, B, L)
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        self.tokens = torch.empty((B, L), dtype=torch.int32, device=device)
+        self.score = torch.empty((B,), dtype=torch.float64, device=device)
+        self.row_status = torch.empty((B,), dtype=torch.int32, device=device)
+
+    def __call__(self, probs, committed, stream=None):
+        fa_map_step(self.aut, probs, committed, self.workspace, self.tokens, self.score, self.row_status, stream)
+        return self.tokens, self.score, self.row_status
 
 
 def fa_apply_commits(commit_idx, tokens, committed, stream=None):

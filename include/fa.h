@@ -238,6 +238,28 @@ fa_status fa_constrained_step_chain(const fa_automaton *aut, int32_t B, int32_t 
                                     float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream);
 
 /*
+ * fa_map_step -- greedy (T = 0) constrained decoding: the accepted string with the largest
+ * mean-field product, argmax over x in the language of prod_t w_t(x_t) (w_t one-hot at
+ * committed positions), by max-product over the same log-depth tree (paperfeed.app summary,
+ * greedy decoding with the constraint; key design 2 of the papernotes.org notes with max in
+ * place of sum).  The product of a string does not depend on its accepting path, so the
+ * best (path, string) pair carries the best accepted string; NFA path counts play no part.
+ * Ties go to the lowest state and token index.  Span products run on the CUDA cores (the
+ * tensor cores have no max).
+ *
+ *   workspace   as for fa_constrained_step (fa_step_workspace_bytes(B, L))
+ *   tokens      [B, L] int32 out (committed positions echoed; -1 where masked when
+ *               row_status[b] != FA_ROW_OK)
+ *   score       [B] double out: ln of the best product (-inf when no accepted string has a
+ *               positive product)
+ *   row_status  [B] int32 out: FA_ROW_*
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_WORKSPACE_TOO_SMALL, FA_ERR_CUDA (launch).
+ */
+fa_status fa_map_step(const fa_automaton *aut, int32_t B, int32_t L, const float *probs, const int32_t *committed,
+                      void *workspace, size_t ws_bytes, int32_t *tokens, double *score, int32_t *row_status,
+                      fa_stream stream);
+
+/*
  * fa_token_marginals -- the full constrained marginal of every token at every position,
  *     p(x_t = v) = w_t(v) * sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / (same summed over v)
  * (key design 3 of the papernotes.org notes), from the prefix/suffix messages that the
