@@ -51,8 +51,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--length", type=int, default=None, help="override L (smaller profiling cases)")
-    ap.add_argument("--method", default="tree", choices=["tree", "chain"],
-                    help="log-depth tree (default) or the O(L) chain form of the same step")
+    ap.add_argument("--method", default="tree", choices=["tree", "chain", "greedy"],
+                    help="log-depth tree (default), the O(L) chain form of the same step, or greedy (T=0) "
+                         "decoding by max-product over the tree")
     ap.add_argument("--confidence", default="marginal", choices=["marginal", "neg_entropy", "unconstrained"],
                     help="remasking confidence the commit ranks by")
     return ap.parse_args()
@@ -166,6 +167,14 @@ def algorithmic(w, masked: int, method: str = "tree"):
     stages are the forward pass and the backward pass with the state draws: each reads every
     M_t once and does one vector-matrix product per position."""
     B, L, S, V = w.B, w.L, w.S, w.V
+    if method == "greedy":
+        K = max(0, math.ceil(math.log2(L))) if L > 1 else 0
+        nk = [(L + (1 << k) - 1) >> k for k in range(K + 1)]
+        alg = algorithmic(w, masked, "tree")
+        alg["upsweep"]["flops"] = 0          # max-product span products run on the CUDA cores
+        alg["topdown"] = {"bytes": sum(B * n * 8 * S for n in nk[:K]), "flops": 0}  # two vectors per midpoint
+        alg["leaf_commit"] = {"bytes": 4 * B * L * 2, "flops": 0}
+        return alg
     if method == "chain":
         span = 4 * S * S + 8 * S
         msg = 8 * S
@@ -224,13 +233,26 @@ def recorded_traffic(stage: str, workload: str):
 
 # ----------------------------------------------------------------------------- CPU baseline
 
-def cpu_baseline(w, probs, seconds: float):
+def cpu_baseline(w, probs, seconds: float, greedy: bool = False):
     """The float64 oracle as it stands, single-threaded on a host core: sample, posterior
-    (logZ and marginals of the sample) and commit, repeated for about `seconds`."""
+    (logZ and marginals of the sample) and commit, repeated for about `seconds` (greedy:
+    the oracle's max-product chain)."""
     import oracle
     o = oracle.OracleFA(w.fa)
     reps, t0 = 0, time.perf_counter()
     nb = probs.shape[0]
+    if greedy:
+        while True:
+            for b in range(nb):
+                oracle.viterbi(w.fa, probs[b], w.committed[b])
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        return {"value": reps * nb * w.L / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "%d greedy passes over %d of the %d sequences of %s (L=%d) in %.1f s, one thread"
+                          % (reps, nb, w.B, w.name, w.L, el),
+                "ms_per_step": 1e3 * el / reps * w.B / nb}
     if o.posterior(probs[0], w.committed[0])["empty"]:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
                 "sample": "none: the constrained distribution of %s at L=%d is empty" % (w.name, w.L)}
@@ -313,13 +335,21 @@ def run_native(args, rank, world, local):
         probs = synth.gaussian_probs_torch(w.seed, w.B, w.L, w.V, w.sigma)
         probs_np = None
     committed = torch.from_numpy(w.committed).cuda()
-    step = native.ConstrainedStep(aut, w.B, w.L, w.k, method=args.method, confidence=args.confidence)
+    if args.method == "greedy":
+        step = native.GreedyStep(aut, w.B, w.L)
+        step_outputs = [step.tokens, step.score, step.row_status]
+    else:
+        step = native.ConstrainedStep(aut, w.B, w.L, w.k, method=args.method, confidence=args.confidence)
+        step_outputs = [step.tokens, step.logZ, step.marg, step.commit_idx, step.row_status]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
     seed = 1234 + rank
 
     def call(offset):
-        step(probs, committed, seed, offset, 0, w.window)
+        if args.method == "greedy":
+            step(probs, committed)
+        else:
+            step(probs, committed, seed, offset, 0, w.window)
 
     # launches per step (counted by the library)
     with torch.cuda.stream(stream):
@@ -393,7 +423,7 @@ def run_native(args, rank, world, local):
     # pinned memory, the step, D2H of every output, all inside the events
     h_probs = probs.cpu().pin_memory()
     h_com = torch.from_numpy(w.committed).pin_memory()
-    outs = [step.tokens, step.logZ, step.marg, step.commit_idx, step.row_status]
+    outs = step_outputs
     h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     n_e2e = max(1, min(args.e2e_steps, args.steps))
     e2e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
@@ -451,7 +481,7 @@ def run_native(args, rank, world, local):
             "clocks": clocks.summary()}
     if world == 1:
         host_probs = probs_np if probs_np is not None else probs[:1].cpu().numpy()
-        line["cpu_baseline"] = cpu_baseline(w, host_probs, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, host_probs, args.cpu_seconds, greedy=args.method == "greedy")
     print(json.dumps(line), flush=True)
 
 

@@ -22,6 +22,7 @@
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kTmChunk = 4096;   // tokens per block of the all-token marginals
 constexpr int kWarps = kThreads / 32;
 
 // ----------------------------------------------------------------------------- workspace plan
@@ -30,7 +31,8 @@ struct Plan {
     int B = 0, L = 0, S = 0, V = 0, K = 0, Lp = 1;
     int nk[18] = {0};
     size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, mu[18] = {0};
-    size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, conf = 0, zsum = 0, zexp = 0;
+    size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, conf = 0, den_m = 0, den_e = 0, tm_part = 0, zsum = 0, zexp = 0;
+    int tm_chunks = 1;
     size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0, img = 0;
     size_t total = 0;
 };
@@ -74,6 +76,12 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
     p.be = take(bnd * S * sizeof(int32_t));
     p.keys = take((size_t)B * (size_t)L * sizeof(unsigned long long));
     p.conf = take((size_t)B * (size_t)L * sizeof(float));   // remasking confidence the commit ranks by
+    // the local normaliser D_t of every position (mantissa, exponent), from the leaves
+    p.den_m = take((size_t)B * (size_t)L * sizeof(float));
+    p.den_e = take((size_t)B * (size_t)L * sizeof(int32_t));
+    // per (position, vocabulary chunk) partial sums of p ln p for the entropies
+    p.tm_chunks = (a->V + kTmChunk - 1) / kTmChunk;
+    p.tm_part = take((size_t)B * (size_t)L * (size_t)p.tm_chunks * sizeof(double));
     // tensor-core operand images, sized for the level with the most node slots (level 1)
     if (fa_span_tc_supported(a->S) && p.K >= 1) p.img = take(fa_span_tc_image_bytes(a->S, (long)B * p.nk[1]));
     p.zsum = take((size_t)B * sizeof(float));
@@ -891,7 +899,7 @@ __device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float 
                               const int32_t *__restrict__ ae, const float *__restrict__ bm,
                               const int32_t *__restrict__ be, int32_t *tokens, float *marg, int32_t *status,
                               const float *__restrict__ leaf, LeafShared &sh, float *stage, int conf_mode,
-                              float *conf) {
+                              float *conf, float *den_mo, int32_t *den_eo) {
     const int tid = threadIdx.x;
     const size_t pos = (size_t)b * L + t;
     const int c = committed[pos];
@@ -1007,7 +1015,9 @@ __device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float 
         if (sh.xm > 0.0f && den_m > 0.0f)
             mval = ldexp((double)__ldg(prow + v) * (double)sh.xm / (double)den_m, sh.xe - den_e);
         marg[pos] = (float)mval;
-        // the commit's ranking score (the entropy score was written by k_token_marginals)
+        den_mo[pos] = den_m;
+        den_eo[pos] = den_e;
+        // the commit's ranking score (the entropy score is written by k_tm_finish)
         if (conf_mode == FA_CONF_MARGINAL) conf[pos] = (float)mval;
         else if (conf_mode == FA_CONF_UNCONSTRAINED) conf[pos] = __ldg(prow + v);
     }
@@ -1030,12 +1040,14 @@ __global__ void __launch_bounds__(kLeafThreads) k_leaf_commit(DevFA fa, int B, i
                                                             float *marg, int32_t *status, int k, int lo, int hi,
                                                             int32_t *commit_idx, unsigned long long *keys,
                                                             int32_t *done, const float *__restrict__ leaf,
-                                                            int conf_mode, float *conf) {
+                                                            int conf_mode, float *conf, float *den_mo,
+                                                            int32_t *den_eo, int do_commit) {
     extern __shared__ float leaf_stage[];
     __shared__ LeafShared sh;
     const int b = (int)(blockIdx.x / (unsigned)L), t = (int)(blockIdx.x % (unsigned)L);
     leaf_position(fa, b, t, L, probs, committed, seed, offset, z, am, ae, bm, be, tokens, marg, status, leaf, sh,
-                  fa.S <= kLeafStageStates ? leaf_stage : nullptr, conf_mode, conf);
+                  fa.S <= kLeafStageStates ? leaf_stage : nullptr, conf_mode, conf, den_mo, den_eo);
+    if (!do_commit) return;
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -1050,42 +1062,42 @@ __global__ void __launch_bounds__(kLeafThreads) k_leaf_commit(DevFA fa, int B, i
 // ----------------------------------------------------------------------------- 5b. all-token marginals
 
 // Full constrained marginal of a masked position t (papernotes.org key design 3):
-//   u(v) = w_t(v) sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e),   p(x_t = v) = u(v) / D,
-// D = sum_v u(v), and its entropy H_t = ln D - (sum_v u ln u) / D.  The messages' per-state
-// exponents are brought to E, the exponent of the largest cell term alpha(s) M_t(s, d)
-// beta(d), so terms more than about 2^-126 below it vanish.  One block per position; token v
-// is summed by thread v mod T over its incidences in CSR order (deterministic), the partial
-// sums in compensated fp32 and the block sum in double.
+//   p(x_t = v) = w_t(v) sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / D_t,
+// D_t = alpha_{t-1}^T M_t beta_t the local normaliser the leaves computed (the same sum taken
+// over the cells), and the entropy H_t = -sum_v p ln p.  One block per (position, chunk of
+// kTmChunk tokens); token v is summed by one thread over its incidences in CSR order, the
+// block's sum of p ln p lands in a per-chunk slot, and k_tm_finish adds the slots in chunk
+// order, so the result is deterministic.
 constexpr int kTmThreads = 256;
 constexpr int kTmWarps = kTmThreads / 32;
 
-__global__ void __launch_bounds__(kTmThreads) k_token_marginals(DevFA fa, int L, const float *__restrict__ probs,
-                                                               const int32_t *__restrict__ committed,
-                                                               const int32_t *__restrict__ status,
-                                                               const float *__restrict__ am,
-                                                               const int32_t *__restrict__ ae,
-                                                               const float *__restrict__ bm,
-                                                               const int32_t *__restrict__ be,
-                                                               const float *__restrict__ leaf, float *marg_all,
-                                                               float *entropy, float *conf) {
+__global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int n_chunks, const float *__restrict__ probs,
+                                                          const int32_t *__restrict__ committed,
+                                                          const int32_t *__restrict__ status,
+                                                          const float *__restrict__ am, const int32_t *__restrict__ ae,
+                                                          const float *__restrict__ bm, const int32_t *__restrict__ be,
+                                                          const float *__restrict__ den_m,
+                                                          const int32_t *__restrict__ den_e, float *marg_all,
+                                                          double *part) {
     extern __shared__ float tm_s[];  // [4 S]: alpha and beta mantissas, then their exponents
-    __shared__ int emax_w[kTmWarps];
-    __shared__ double red[2 * kTmWarps];
+    __shared__ double red[kTmWarps];
     const int S = fa.S, V = fa.V;
-    const size_t pos = blockIdx.x;
+    const size_t pos = blockIdx.x / (unsigned)n_chunks;
+    const int chunk = (int)(blockIdx.x % (unsigned)n_chunks);
     const int b = (int)(pos / (size_t)L), t = (int)(pos % (size_t)L);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int v0 = chunk * kTmChunk, v1 = min(V, v0 + kTmChunk);
     const int c = committed[pos];
     float *out = marg_all ? marg_all + pos * (size_t)V : nullptr;
-    if (c >= 0 || status[b] != FA_ROW_OK) {
+    const float dm = (c >= 0 || status[b] != FA_ROW_OK) ? 0.0f : den_m[pos];
+    if (!(dm > 0.0f)) {
         if (out)
-            for (int v = tid; v < V; v += kTmThreads) out[v] = (c >= 0 && v == c) ? 1.0f : 0.0f;
-        if (tid == 0) {
-            if (entropy) entropy[pos] = 0.0f;
-            if (conf) conf[pos] = 0.0f;
-        }
+            for (int v = v0 + tid; v < v1; v += kTmThreads) out[v] = (c >= 0 && v == c) ? 1.0f : 0.0f;
+        if (tid == 0) part[blockIdx.x] = 0.0;
         return;
     }
+    const int E = den_e[pos];
+    const float inv = 1.0f / dm;
     float *sam = tm_s, *sbm = tm_s + S;
     int *sae = reinterpret_cast<int *>(tm_s + 2 * S), *sbe = sae + S;
     const size_t ba = ((size_t)b * (L + 1) + t) * S, bb = ba + S;
@@ -1094,62 +1106,59 @@ __global__ void __launch_bounds__(kTmThreads) k_token_marginals(DevFA fa, int L,
         sbm[s] = bm[bb + s]; sbe[s] = be[bb + s];
     }
     __syncthreads();
-    const float *Mt = leaf + pos * (size_t)S * S;
-    int e = FA_INT_NONE;
-    for (int q = tid; q < fa.n_cells; q += kTmThreads) {
-        const int s = fa.cell_src[q], d = fa.cell_dst[q];
-        const float mv = __ldg(Mt + (size_t)s * S + d);
-        if (sam[s] > 0.0f && sbm[d] > 0.0f && mv > 0.0f) e = max(e, sae[s] + sbe[d] + fa_exponent(mv));
-    }
-    e = fa_warp_max_int(e);
-    if (lane == 0) emax_w[warp] = e;
-    __syncthreads();
-    int E = FA_INT_NONE;
-    for (int w = 0; w < kTmWarps; ++w) E = max(E, emax_w[w]);
     const float *prow = probs + pos * (size_t)V;
-    float su = 0.0f, cu = 0.0f, sl = 0.0f, cl = 0.0f;  // compensated sums of u and u ln u
-    if (E != FA_INT_NONE)
-        for (int v = tid; v < V; v += kTmThreads) {
-            const float w = __ldg(prow + v);
-            float acc = 0.0f;
-            if (w > 0.0f)
-                for (int64_t j = fa.tok_off[v]; j < fa.tok_off[v + 1]; ++j) {
-                    const uint32_t sd = __ldg(fa.tok_sd + j);
-                    const int s = (int)(sd >> 16), d = (int)(sd & 0xffffu);
-                    const float a = sam[s], bq = sbm[d];
-                    if (a > 0.0f && bq > 0.0f) acc += a * bq * fa_pow2(sae[s] + sbe[d] - E);
-                }
-            const float u = w * acc;
-            if (out) out[v] = u;
-            if (u > 0.0f) {
-                float y = u - cu, tt = su + y;
-                cu = (tt - su) - y;
-                su = tt;
-                y = u * logf(u) - cl;
-                tt = sl + y;
-                cl = (tt - sl) - y;
-                sl = tt;
+    float sl = 0.0f, cl = 0.0f;  // compensated sum of p ln p
+    for (int v = v0 + tid; v < v1; v += kTmThreads) {
+        const float w = __ldg(prow + v);
+        float acc = 0.0f;
+        if (w > 0.0f) {
+            const int64_t j0 = fa.tok_off[v], j1 = fa.tok_off[v + 1];
+#pragma unroll 4
+            for (int64_t j = j0; j < j1; ++j) {
+                const uint32_t sd = __ldg(fa.tok_sd + j);
+                const int s = (int)(sd >> 16), d = (int)(sd & 0xffffu);
+                const float a = sam[s], bq = sbm[d];
+                if (a > 0.0f && bq > 0.0f) acc += a * bq * fa_pow2(sae[s] + sbe[d] - E);
             }
         }
-    double du = (double)su - (double)cu, dl = (double)sl - (double)cl;
+        const float pv = w * acc * inv;
+        if (out) out[v] = pv;
+        if (pv > 0.0f) {
+            const float y = pv * logf(pv) - cl, tt = sl + y;
+            cl = (tt - sl) - y;
+            sl = tt;
+        }
+    }
+    double dl = (double)sl - (double)cl;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        du += __shfl_xor_sync(0xffffffffu, du, o);
-        dl += __shfl_xor_sync(0xffffffffu, dl, o);
-    }
-    if (lane == 0) { red[warp] = du; red[kTmWarps + warp] = dl; }
+    for (int o = 16; o; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+    if (lane == 0) red[warp] = dl;
     __syncthreads();
-    double D = 0.0, SL = 0.0;
-    for (int w = 0; w < kTmWarps; ++w) { D += red[w]; SL += red[kTmWarps + w]; }
-    const double H = D > 0.0 ? log(D) - SL / D : 0.0;
     if (tid == 0) {
-        if (entropy) entropy[pos] = (float)H;
-        if (conf) conf[pos] = (float)-H;
+        double tot = 0.0;
+        for (int w = 0; w < kTmWarps; ++w) tot += red[w];
+        part[blockIdx.x] = tot;
     }
-    if (out) {
-        const float inv = D > 0.0 ? (float)(1.0 / D) : 0.0f;
-        for (int v = tid; v < V; v += kTmThreads) out[v] *= inv;  // this thread's own writes
-    }
+}
+
+// H_t = -(sum of the chunk slots, in chunk order); the commit score is -H_t.
+__global__ void k_tm_finish(long n_pos, int n_chunks, const double *__restrict__ part, float *entropy, float *conf) {
+    const long pos = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (pos >= n_pos) return;
+    double tot = 0.0;
+    for (int q = 0; q < n_chunks; ++q) tot += part[pos * n_chunks + q];
+    const float H = (float)(tot == 0.0 ? 0.0 : -tot);
+    if (entropy) entropy[pos] = H;
+    if (conf) conf[pos] = -H;
+}
+
+// The commit of every sequence as its own block (when it must wait for the entropies).
+__global__ void __launch_bounds__(kThreads) k_commit_rows(int L, int k, int lo, int hi, float *marg,
+                                                        const float *conf, const int32_t *__restrict__ committed,
+                                                        const int32_t *status, int32_t *commit_idx, int32_t *tokens,
+                                                        unsigned long long *keys) {
+    const int b = blockIdx.x;
+    topk_row(b, L, k, lo, hi, marg, conf, committed, status, commit_idx, tokens, keys + (size_t)b * L);
 }
 
 // ----------------------------------------------------------------------------- chain variant
@@ -1627,15 +1636,23 @@ fa_status launch_token_marginals(const fa_automaton *aut, int B, int L, const fl
                                  float *entropy, float *conf, cudaStream_t st) {
     const size_t smem = (size_t)aut->S * 16;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_token_marginals, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(k_tm_partial, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) { fa_set_error(std::string("token marginals smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     }
     auto F = [&](size_t off) { return (const float *)(ws + off); };
     auto I = [&](size_t off) { return (const int32_t *)(ws + off); };
-    k_token_marginals<<<(unsigned)((long)B * L), kTmThreads, smem, st>>>(
-        dev_view(aut), L, probs, committed, row_status, F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.mant[0]), marg_all,
-        entropy, conf);
-    return launch_check("token marginals");
+    double *part = (double *)(ws + p.tm_part);
+    const long n_pos = (long)B * L;
+    k_tm_partial<<<(unsigned)(n_pos * p.tm_chunks), kTmThreads, smem, st>>>(
+        dev_view(aut), L, p.tm_chunks, probs, committed, row_status, F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.den_m),
+        I(p.den_e), marg_all, part);
+    fa_status s = launch_check("token marginals");
+    if (s != FA_OK) return s;
+    if (entropy || conf) {
+        k_tm_finish<<<(unsigned)((n_pos + 255) / 256), 256, 0, st>>>(n_pos, p.tm_chunks, part, entropy, conf);
+        s = launch_check("entropies");
+    }
+    return s;
 }
 
 }  // namespace
@@ -1690,9 +1707,11 @@ extern "C" fa_status fa_map_step(const fa_automaton *aut, int32_t B, int32_t L, 
     auto F = [&](size_t off) { return (float *)(ws + off); };
     auto I = [&](size_t off) { return (int32_t *)(ws + off); };
     const int S = aut->S;
+    stage_mark(0, s);
     st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), s, I(p.rmax_hi),
                          (long)(p.rmax_hi_bytes / sizeof(int32_t)), true);
     if (st != FA_OK) return st;
+    stage_mark(1, s);
     for (int kk = 1; kk <= p.K; ++kk) {
         if (S <= SMALL_S) {
             const long tpd = (S + ST - 1) / ST;
@@ -1712,6 +1731,7 @@ extern "C" fa_status fa_map_step(const fa_automaton *aut, int32_t B, int32_t L, 
             F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]));
         if ((st = launch_check("span product (max)")) != FA_OK) return st;
     }
+    stage_mark(2, s);
     k_map_root<<<B, 32, 0, s>>>(dev_view(aut), L, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), I(p.z), score, row_status);
     if ((st = launch_check("greedy root")) != FA_OK) return st;
     for (int kk = p.K - 1; kk >= 0; --kk) {
@@ -1720,11 +1740,14 @@ extern "C" fa_status fa_map_step(const fa_automaton *aut, int32_t B, int32_t L, 
             S, B, L, kk, p.nk[kk], np, F(p.mant[kk]), I(p.rho[kk]), I(p.z), row_status);
         if ((st = launch_check("greedy midpoints")) != FA_OK) return st;
     }
+    stage_mark(3, s);
     k_map_leaf<<<(unsigned)(((long)B * L + kWarps - 1) / kWarps), kThreads, 0, s>>>(dev_view(aut), B, L, probs, committed,
                                                                               I(p.z), tokens, row_status);
     if ((st = launch_check("greedy leaves")) != FA_OK) return st;
     k_map_fix<<<(unsigned)(((long)B * L + 255) / 256), 256, 0, s>>>(B, L, committed, row_status, tokens, score);
-    return launch_check("greedy fix-up");
+    st = launch_check("greedy fix-up");
+    stage_mark(4, s);
+    return st;
 }
 
 extern "C" fa_status fa_step_workspace_bytes(const fa_automaton *aut, int32_t B, int32_t L, size_t *bytes) {
@@ -1903,17 +1926,23 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
     // 5. leaves: tokens and marginals, then the commit (one launch); before them, when asked,
     //    the entropy of every position's full constrained distribution
     stage_mark(3, s);
-    if (confidence == FA_CONF_NEG_ENTROPY || entropy) {
-        st = launch_token_marginals(aut, B, L, probs, committed, p, ws, row_status, nullptr, entropy,
-                                    confidence == FA_CONF_NEG_ENTROPY ? F(p.conf) : nullptr, s);
-        if (st != FA_OK) return st;
-    }
+    const bool entropies = confidence == FA_CONF_NEG_ENTROPY || entropy;
     const size_t leaf_smem = S <= kLeafStageStates ? (size_t)S * 16 : 0;
     k_leaf_commit<<<(unsigned)((long)B * L), kLeafThreads, leaf_smem, s>>>(
         dev_view(aut), B, L, probs, committed, philox_seed, philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be),
         tokens, marg, row_status, k, commit_lo, commit_hi, commit_idx, (unsigned long long *)(ws + p.keys),
-        I(p.leaf_done), F(p.mant[0]), confidence, F(p.conf));
+        I(p.leaf_done), F(p.mant[0]), confidence, F(p.conf), F(p.den_m), I(p.den_e), entropies ? 0 : 1);
     st = launch_check("leaf and commit");
+    if (st == FA_OK && entropies) {
+        // the entropies need every leaf's normaliser; the commit waits for them
+        st = launch_token_marginals(aut, B, L, probs, committed, p, ws, row_status, nullptr, entropy,
+                                    confidence == FA_CONF_NEG_ENTROPY ? F(p.conf) : nullptr, s);
+        if (st == FA_OK) {
+            k_commit_rows<<<B, kThreads, 0, s>>>(L, k, commit_lo, commit_hi, marg, F(p.conf), committed, row_status,
+                                                 commit_idx, tokens, (unsigned long long *)(ws + p.keys));
+            st = launch_check("commit");
+        }
+    }
     stage_mark(4, s);
     return st;
 }
