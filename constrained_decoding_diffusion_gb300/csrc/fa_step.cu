@@ -374,15 +374,17 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
                                                        const int32_t *__restrict__ rho_c,
                                                        const int32_t *__restrict__ rmax_c, int nc, float *mant_p,
                                                        int32_t *rho_p, int32_t *rmax_p) {
-    __shared__ float As[ST][SMALL_S + 1];
-    __shared__ float Bs[SMALL_S][ST + 1];
+    // the A tile is stored transposed (At[m][row]) and both tiles padded to 16-byte rows, so
+    // the inner loop reads two float2 per step
+    __shared__ __align__(16) float At[SMALL_S][ST + 4];
+    __shared__ __align__(16) float Bs[SMALL_S][ST + 4];
     __shared__ int rhoR_s[SMALL_S], rmaxR_s[SMALL_S], mu_s[ST];
     const int tpd = (S + ST - 1) / ST;
     const int tile = blockIdx.x % (tpd * tpd);
     const long bn = blockIdx.x / (tpd * tpd);
     const int node = (int)(bn % nk), b = (int)(bn / nk);
     const int i0 = (tile / tpd) * ST, j0 = (tile % tpd) * ST;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const size_t pnode = (size_t)b * nk + node;
     const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
     const size_t SS = (size_t)S * S;
@@ -421,43 +423,53 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int q = tid + u * kThreads;
-            As[q / SMALL_S][q % SMALL_S] = va[u];
+            At[q % SMALL_S][q / SMALL_S] = va[u];
             Bs[q / ST][q % ST] = vb[u];
         }
         if (tid < SMALL_S) { rhoR_s[tid] = ra; rmaxR_s[tid] = rr; }
     }
     __syncthreads();
-    for (int r = warp; r < ST; r += kWarps) {
+    {
+        // row shift: eight threads per row, each over every eighth inner index, then three
+        // shuffles (all 32 rows at once)
+        const int r = tid >> 3, seg = tid & 7;
         int best = FA_INT_NONE;
-        for (int m = lane; m < S; m += 32) {
-            const float x = As[r][m];
+        for (int m = seg; m < S; m += 8) {
+            const float x = At[m][r];
             const int q = rmaxR_s[m];
             if (x > 0.0f && q > 0) best = max(best, rhoR_s[m] + fa_exponent(__int_as_float(q)) + fa_exponent(x));
         }
-        best = fa_warp_max_int(best);
-        if (lane == 0) mu_s[r] = best;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+        if (seg == 0) mu_s[r] = best;
     }
     __syncthreads();
     for (int q = tid; q < ST * SMALL_S; q += kThreads) {
-        const int r = q / SMALL_S, m = q % SMALL_S;
-        const float x = As[r][m];
+        const int m = q / ST, r = q % ST;
+        const float x = At[m][r];
         const int mr = mu_s[r];
-        As[r][m] = (x > 0.0f && mr != FA_INT_NONE && m < S && rmaxR_s[m] > 0) ? fa_mul_pow2(x, rhoR_s[m] - mr) : 0.0f;
+        At[m][r] = (x > 0.0f && mr != FA_INT_NONE && m < S && rmaxR_s[m] > 0) ? fa_mul_pow2(x, rhoR_s[m] - mr) : 0.0f;
     }
     __syncthreads();
     const int tx = tid & 15, ty = tid >> 4;          // 2x2 outputs per thread
     float c00 = 0.0f, c01 = 0.0f, c10 = 0.0f, c11 = 0.0f;
-    for (int m = 0; m < S; ++m) {
-        const float a0 = As[2 * ty][m], a1 = As[2 * ty + 1][m];
-        const float b0 = Bs[m][2 * tx], b1 = Bs[m][2 * tx + 1];
+    auto step = [&](int m) {
+        const float2 a = *reinterpret_cast<const float2 *>(&At[m][2 * ty]);
+        const float2 bq = *reinterpret_cast<const float2 *>(&Bs[m][2 * tx]);
         if constexpr (MAX) {
-            c00 = fmaxf(c00, a0 * b0); c01 = fmaxf(c01, a0 * b1);
-            c10 = fmaxf(c10, a1 * b0); c11 = fmaxf(c11, a1 * b1);
+            c00 = fmaxf(c00, a.x * bq.x); c01 = fmaxf(c01, a.x * bq.y);
+            c10 = fmaxf(c10, a.y * bq.x); c11 = fmaxf(c11, a.y * bq.y);
         } else {
-            c00 = fmaf(a0, b0, c00); c01 = fmaf(a0, b1, c01);
-            c10 = fmaf(a1, b0, c10); c11 = fmaf(a1, b1, c11);
+            c00 = fmaf(a.x, bq.x, c00); c01 = fmaf(a.x, bq.y, c01);
+            c10 = fmaf(a.y, bq.x, c10); c11 = fmaf(a.y, bq.y, c11);
         }
+    };
+    int m = 0;
+    for (; m + 8 <= S; m += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) step(m + u);
     }
+    for (; m < S; ++m) step(m);
     const float cv[2][2] = {{c00, c01}, {c10, c11}};
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
