@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--method", default="tree", choices=["tree", "chain", "greedy"],
                     help="log-depth tree (default), the O(L) chain form of the same step, or greedy (T=0) "
                          "decoding by max-product over the tree")
+    ap.add_argument("--schedule", action="store_true",
+                    help="also time the workload's whole remasking schedule (block-wise workload)")
     ap.add_argument("--confidence", default="marginal", choices=["marginal", "neg_entropy", "unconstrained"],
                     help="remasking confidence the commit ranks by")
     return ap.parse_args()
@@ -271,6 +273,43 @@ def cpu_baseline(w, probs, seconds: float, greedy: bool = False):
             "ms_per_step": 1e3 * el / reps * w.B / nb}
 
 
+def run_schedule(w, aut, stream, seed):
+    """The workload's whole block-wise remasking schedule: every step is the constrained step
+    and the commit, timed with CUDA events on the launching stream; the denoiser's fresh
+    probabilities of each step are drawn on the device outside the events."""
+    import torch
+    from constrained_decoding_diffusion_gb300 import native, synth
+    committed = torch.from_numpy(w.committed).cuda()
+    step = native.ConstrainedStep(aut, w.B, w.L, w.k)
+    n_blocks = (w.L + w.window - 1) // w.window
+    per_block = max(1, w.steps // n_blocks)
+    ms, i, ok = [], 0, True
+    for blk in range(n_blocks):
+        lo, hi = blk * w.window, min(w.L, (blk + 1) * w.window)
+        for _ in range(per_block):
+            probs = synth.gaussian_probs_torch(w.seed * 1000 + i, w.B, w.L, w.V, w.sigma)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                step(probs, committed, seed, i, lo, hi, stream)
+                native.fa_apply_commits(step.commit_idx, step.tokens, committed, stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+            ok = ok and bool((step.row_status.cpu().numpy() == 0).all())
+            del probs
+            i += 1
+    final = committed.cpu().numpy()
+    total = float(np.sum(ms))
+    return {"steps": i, "blocks": n_blocks, "steps_per_block": per_block, "k": w.k, "ms_total": total,
+            "ms_first_step": float(ms[0]), "ms_last_step": float(ms[-1]), "ms_mean_step": total / i,
+            "value": w.B * w.L / (total / 1e3), "unit": "committed positions/s",
+            "all_committed": bool((final >= 0).all()), "row_status_ok": ok,
+            "timing": "per step: fa_constrained_step + fa_apply_commits between CUDA events; probabilities "
+                      "drawn on the device outside them"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -479,6 +518,9 @@ def run_native(args, rank, world, local):
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
             "wall_s": wall, "row_status_ok": bool((status == 0).all()),
             "clocks": clocks.summary()}
+    if args.schedule and w.steps > 1:
+        del graph
+        line["schedule"] = run_schedule(w, aut, stream, seed)
     if world == 1:
         host_probs = probs_np if probs_np is not None else probs[:1].cpu().numpy()
         line["cpu_baseline"] = cpu_baseline(w, host_probs, args.cpu_seconds, greedy=args.method == "greedy")
