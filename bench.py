@@ -198,6 +198,22 @@ def algorithmic(w, masked: int, method: str = "tree"):
             "leaf_commit": {"bytes": 4 * B * L * 4 + 8 * B * L, "flops": 0}}
 
 
+def reweight_gather(w, masked: int, ms: float, clocks):
+    """The reweight against its compute limits: one gather-add per token-edge incidence per
+    masked position, against the FP32 issue peak (128 lanes per SM per clock) and the
+    shared-memory gather peak (32 banks per SM per clock), at the sampled SM clock (152 SMs)."""
+    if ms <= 0:
+        return None
+    mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    gathers = masked * w.fa.n_incidences
+    rate = gathers / (ms / 1e3)
+    alu = 152 * 128 * mhz * 1e6
+    smem = 152 * 32 * mhz * 1e6
+    return {"gathers": gathers, "achieved_G_per_s": rate / 1e9, "fp32_issue_peak_G_per_s": alu / 1e9,
+            "frac_fp32_issue": rate / alu, "smem_gather_peak_G_per_s": smem / 1e9, "frac_smem_gather": rate / smem,
+            "sm_mhz": mhz}
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -510,6 +526,7 @@ def run_native(args, rank, world, local):
                        "method": args.method, "confidence": args.confidence,
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roof,
+            "reweight_gather": reweight_gather(w, masked, per_stage.get("reweight", 0.0), clocks.summary()),
             "step_roofline": {"ms_at_roofline": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_max,
                               "bytes": tot_bytes, "span_flops": alg["upsweep"]["flops"]},
             "stage_ms": per_stage,
