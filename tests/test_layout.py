@@ -1,0 +1,54 @@
+"""The reweight's run layout, checked on the host (no GPU): tests/layout_harness.cu builds
+the layout with the library's own build_run_layout, replays the kernel's walk over the
+entry streams and compares every cell sum with float64, on automata covering one and
+several vocabulary chunks, small and large rows, parallel edges and many states."""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+from constrained_decoding_diffusion_gb300 import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def harness(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    out = tmp_path_factory.mktemp("layout") / "layout_harness"
+    subprocess.check_call([nvcc, "-std=c++17", "-O2", "-o", str(out), os.path.join(HERE, "layout_harness.cu")])
+    return str(out)
+
+
+def dump(fa, path):
+    with open(path, "wb") as f:
+        np.array([fa.n_states, fa.vocab, len(fa.edge_src)], np.int64).tofile(f)
+        np.asarray(fa.edge_src, np.int32).tofile(f)
+        np.asarray(fa.edge_dst, np.int32).tofile(f)
+        np.asarray(fa.label_offsets, np.int64).tofile(f)
+        np.asarray(fa.label_tokens, np.int32).tofile(f)
+
+
+CASES = {
+    "real_number": lambda: synth.real_number_dfa(),
+    "tiny_nfa_parallel_edges": lambda: synth.tiny_random_fa(np.random.default_rng(3), 6, 40, 14, 9),
+    "random_dfa_one_chunk": lambda: synth.random_dfa(64, 3000, 0.7, 8, seed=1),
+    "random_dfa_two_chunks": lambda: synth.random_dfa(32, 30000, 0.5, 4, seed=2),
+    "duplicated_edges": lambda: synth.random_dfa(12, 40, 0.5, 3, seed=4).duplicated_edges(),
+    "single_state_three_chunks": lambda: synth.single_state_fa(60000),
+    "layered_chain_two_chunks": lambda: synth.layered_chain(256, 40000, seed=2),
+    "random_nfa": lambda: synth.random_nfa(200, 20000, 8, 100, 4, seed=3),
+    "many_small_rows": lambda: synth.random_nfa(3000, 2000, 2, 3, 5, seed=5),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_run_layout(harness, tmp_path, name):
+    path = tmp_path / "fa.bin"
+    dump(CASES[name](), path)
+    r = subprocess.run([harness, str(path)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "bad=0" in r.stdout, r.stdout + r.stderr
