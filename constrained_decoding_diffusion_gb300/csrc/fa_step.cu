@@ -298,7 +298,11 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
                 if constexpr (MAX) v = fmaxf(v, sb[fa.crun_slot[q]]); else v += sb[fa.crun_slot[q]];
             }
             M[(size_t)s * S + fa.cell_dst[cell]] = v;
-            atomicMax(&smax[s - r0], __float_as_int(v));
+            // consecutive cells mostly share a row: one atomic per row and warp
+            const unsigned act = __activemask();
+            const unsigned same = __match_any_sync(act, s);
+            const int rowmax = (int)__reduce_max_sync(same, (unsigned)__float_as_int(v));
+            if ((threadIdx.x & 31) == __ffs(same) - 1) atomicMax(&smax[s - r0], rowmax);
         }
     } else {
         for (int i = tid; i < r1 - r0; i += nthr) smax[i] = 0;
