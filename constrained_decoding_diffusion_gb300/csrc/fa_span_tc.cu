@@ -12,12 +12,14 @@
 // Two kernels per tree level.  k_tc_prep converts every operand once: the left child, row
 // prescaled, and the right child are split into hi/lo and written as the exact images of the
 // shared-memory tiles the MMAs read (canonical K-major no-swizzle layout: 8-row x 16-byte
-// core matrices, K-direction core stride 128 B, row-group stride 1024 B; 128x32 left tiles,
-// 256x32 right tiles).  k_span_tc then runs a warp-specialised pipeline per 128x256 output
-// tile: one producer thread streams the tile images of each K step (4 bulk copies, 96 KB)
-// into one of two shared-memory stages, tracked by the stage's "full" mbarrier; one thread
-// issues the MMAs (M=128, N=256, K=8; hi*hi, hi*lo, lo*hi) and commits them to the stage's
-// "empty" mbarrier, which releases the stage to the producer.  K steps alternate between two
+// core matrices, K-direction core stride 128 B, row-group stride 512 B; 128x16 left tiles,
+// 256x16 right tiles).  k_span_tc then runs a warp-specialised pipeline per 128x256 output
+// tile: one producer thread streams the tile images of each K step (48 KB) into one of four
+// shared-memory stages, tracked by the stage's "full" mbarrier; one thread issues the MMAs
+// (M=128, N=256, K=8; hi*hi, hi*lo, lo*hi) and commits them to the stage's "empty" mbarrier,
+// which releases the stage to the producer.  Four stages of 16 K-columns rather than two of
+// 32 keep three stages in flight while one is multiplied, so the refill of a stage has three
+// stages' worth of MMA time to cover the L2 latency.  K steps alternate between two
 // tensor-memory accumulators (128 lanes x 256 fp32 columns each): the tensor cores' fp32
 // accumulation truncates, so each chain of additions is kept half as long and the two are
 // added with round-to-nearest in the epilogue, where the 8 warps read tensor memory (each
@@ -31,16 +33,17 @@
 
 namespace {
 
-constexpr int TM = 128, TN = 256, TK = 32, NTHR = 256;
-constexpr int A_BYTES = TM * TK * 4;        // 16 KB per copy (hi or lo)
-constexpr int B_BYTES = TN * TK * 4;        // 32 KB
-constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 96 KB
-constexpr int NSTAGE = 2;
+constexpr int TM = 128, TN = 256, TK = 16, NTHR = 256;
+constexpr int A_BYTES = TM * TK * 4;        // 8 KB per copy (hi or lo)
+constexpr int B_BYTES = TN * TK * 4;        // 16 KB
+constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 48 KB
+constexpr int NSTAGE = 4;                   // three stages in flight while one is multiplied
+constexpr uint32_t KGRP = TK * 32;          // bytes of one 8-row group (8 rows x TK x 4 B)
 constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 constexpr long long kSpinCycles = 2000000000LL;
-constexpr int A_IMG = 2 * A_BYTES;          // hi + lo image of one 128x32 left tile
-constexpr int PREP_KT = 8;                  // K steps converted per k_tc_prep block
-constexpr int B_IMG = 2 * B_BYTES;          // hi + lo image of one 256x32 right tile
+constexpr int A_IMG = 2 * A_BYTES;          // hi + lo image of one 128x16 left tile
+constexpr int PREP_KT = 256 / TK;           // K steps converted per k_tc_prep block (256 columns)
+constexpr int B_IMG = 2 * B_BYTES;          // hi + lo image of one 256x16 right tile
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -127,9 +130,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// byte offset of element (row, k) in a K-major no-swizzle tile with 32 K-columns
+// byte offset of element (row, k) in a K-major no-swizzle tile with TK K-columns
 __device__ __forceinline__ uint32_t kmaj_off(int row, int k) {
-    return (uint32_t)((row >> 3) * 1024 + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4);
+    return (uint32_t)((row >> 3) * KGRP + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4);
 }
 
 __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
@@ -169,8 +172,8 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
         for (int kt = kt0; kt < kt1; ++kt) {
             unsigned char *t = base + (size_t)kt * A_IMG;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int kk = (tid & 1) * 16 + 4 * q, m0 = kt * TK + kk;
+            for (int q = 0; q < TK / 8; ++q) {
+                const int kk = (tid & 1) * (TK / 2) + 4 * q, m0 = kt * TK + kk;
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (gi < S && m0 < S) v = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gi * S + m0));
                 float x[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
@@ -265,6 +268,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
     const uint32_t tmem = tmem_base_s;
     if (tid == 0) {
         // producer: stream the operand images of every K step into the stages
+        int issued = 0;
         for (int kt = 0; kt < nkt; ++kt) {
             const int st = kt % NSTAGE;
             if (kt >= NSTAGE && !mbar_wait(&empty[st], ((kt / NSTAGE) - 1) & 1)) { atomicExch(&fail_s, 1); break; }
@@ -272,6 +276,12 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
             mbar_expect_tx(&full[st], STAGE_BYTES);
             bulk_g2s(stage, a_img + (size_t)kt * A_IMG, A_IMG, &full[st]);
             bulk_g2s(stage + A_IMG, b_img + (size_t)kt * B_IMG, B_IMG, &full[st]);
+            issued = kt + 1;
+        }
+        if (fail_s) {
+            // copies still in flight land in this CTA's stages: wait (bounded) for the last
+            // phase issued on each stage before the CTA may leave
+            for (int kt = max(0, issued - NSTAGE); kt < issued; ++kt) (void)mbar_wait(&full[kt % NSTAGE], (kt / NSTAGE) & 1);
         }
     } else if (tid == 32) {
         // MMA issuer
@@ -288,9 +298,9 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
             for (int ks = 0; ks < TK / 8; ++ks) {
                 const uint32_t o = ks * 256;   // 8 K-columns = two 128-byte core matrices
                 const uint32_t first = (kt < 2 && ks == 0) ? 0u : 1u;
-                umma_tf32(dacc, umma_desc(a_hi + o, 128, 1024), umma_desc(b_hi + o, 128, 1024), idesc, first);
-                umma_tf32(dacc, umma_desc(a_hi + o, 128, 1024), umma_desc(b_lo + o, 128, 1024), idesc, 1u);
-                umma_tf32(dacc, umma_desc(a_lo + o, 128, 1024), umma_desc(b_hi + o, 128, 1024), idesc, 1u);
+                umma_tf32(dacc, umma_desc(a_hi + o, 128, KGRP), umma_desc(b_hi + o, 128, KGRP), idesc, first);
+                umma_tf32(dacc, umma_desc(a_hi + o, 128, KGRP), umma_desc(b_lo + o, 128, KGRP), idesc, 1u);
+                umma_tf32(dacc, umma_desc(a_lo + o, 128, KGRP), umma_desc(b_hi + o, 128, KGRP), idesc, 1u);
             }
             umma_commit(&empty[st]);
         }

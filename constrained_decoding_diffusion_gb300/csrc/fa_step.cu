@@ -196,7 +196,10 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
     const int r0 = m0.x, r1 = m0.y, u0 = m0.z, nu = m0.w - m0.z, c0 = m1.x, c1 = m1.y;
     float *M = mant + pos * (size_t)S * S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (size_t i = (size_t)r0 * S + tid; i < (size_t)r1 * S; i += nthr) M[i] = 0.0f;
+    // a masked position writes every cell of its rows: the rest of the rows is cleared, all
+    // of it unless the cells cover every (s, s') pair of the rows
+    if (c >= 0 || c1 - c0 < (r1 - r0) * S)
+        for (size_t i = (size_t)r0 * S + tid; i < (size_t)r1 * S; i += nthr) M[i] = 0.0f;
     if (c < 0) {
         for (int i = tid; i < nu * FA_UNIT_SLOTS; i += nthr) slots[i] = 0.0f;
         const float *prow = probs + pos * (size_t)fa.V;

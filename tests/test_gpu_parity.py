@@ -372,9 +372,11 @@ def test_step_long_sequence_global_topk(native):
     check_against_oracle(fa, o, probs, committed, res, 40)
 
 
-@pytest.mark.parametrize("S", [128, 300])
+@pytest.mark.parametrize("S", [128, 200, 300, 400, 512])
 def test_step_tensor_core_span_products(native, S):
-    """|S| >= 128 takes the tcgen05 3xTF32 span products; 300 leaves ragged 128x256 tiles."""
+    """|S| >= 128 takes the tcgen05 3xTF32 span products; 200, 300 and 400 leave ragged
+    128x256 tiles.  Row tiles in clusters sharing the right operand: 1 CTA (128, 300),
+    2 CTAs (200) and 4 CTAs (400, 512)."""
     rng = np.random.default_rng(S)
     fa = synth.random_dfa(S, 3000, 0.8, 12, seed=S)
     o = oracle.OracleFA(fa)
