@@ -77,7 +77,8 @@ void fa_set_error(const std::string &msg);
 #define FA_RUN_SLOTS 8               // runs (accumulator slots) per lane
 #endif
 #define FA_UNIT_SLOTS (32 * FA_RUN_SLOTS)
-#define FA_RW_MAX_UNITS 16           // warp units per reweight block (two blocks per SM)
+#define FA_RW_WARPS 16               // warps per reweight block (two blocks per SM)
+#define FA_RW_MAX_UNITS 32           // warp units per reweight block: a warp walks up to two
 
 // floor(log2 x) of a positive normal float from its exponent field (subnormals give -127).
 __device__ __forceinline__ int fa_exponent(float x) {

@@ -171,9 +171,9 @@ __device__ int warp_categorical(int n, float u, WF w) {
 // MAX = true: the max-product variant for greedy decoding, M_t(s, s') = max over the tokens of
 // the edges s -> s' of w_t(v) (a committed position: 1 where an edge carries its token).
 template <bool MAX>
-__global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
-                                                                    const int32_t *__restrict__ committed,
-                                                                    const int4 *__restrict__ rbm, int nrb, int max_units,
+__global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
+                                                                const int32_t *__restrict__ committed,
+                                                                const int4 *__restrict__ rbm, int nrb, int tot_floats,
                                                                     float *mant, int32_t *rho, int32_t *rmax,
                                                                     int32_t *zero, long n_zero) {
     extern __shared__ float smem_f[];
@@ -185,15 +185,18 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
         for (long i = bid * nthr + threadIdx.x; i < n_zero; i += nb * nthr) zero[i] = 0;
     }
     const int S = fa.S, CH = fa.chunk_tokens, nch = fa.n_chunks;
-    const int CHS = (CH + 4) & ~3;                         // the staged chunk, [CH] = 0
-    float *slots = smem_f + CHS;                           // [max_units * FA_UNIT_SLOTS] run sums
-    int *smax = (int *)smem_f;                             // [rows] row maxima (bits), once the chunks are done
+    // shared memory: [0, tot_floats) holds the staged chunk ([CH] = 0) while the chunks are
+    // walked, then every unit's run totals (FA_UNIT_SLOTS per unit) followed by the row maxima;
+    // after it, one slot array per warp for the run sums of the chunk being walked
+    float *utot = smem_f;
+    float *slots = smem_f + tot_floats;                    // [FA_RW_WARPS * FA_UNIT_SLOTS]
     const int t = blockIdx.x / nrb, r = blockIdx.x % nrb, b = blockIdx.y;
     const size_t pos = (size_t)b * L + t;
     // the block's metadata and the committed token, loaded together
     const int4 m0 = __ldg(rbm + 2 * r), m1 = __ldg(rbm + 2 * r + 1);
     const int c = committed[pos];
     const int r0 = m0.x, r1 = m0.y, u0 = m0.z, nu = m0.w - m0.z, c0 = m1.x, c1 = m1.y;
+    int *smax = (int *)(utot + nu * FA_UNIT_SLOTS);        // [rows] row maxima (bits), once the chunks are done
     float *M = mant + pos * (size_t)S * S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // a masked position writes every cell of its rows: the rest of the rows is cleared, all
@@ -201,17 +204,19 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
     if (c >= 0 || c1 - c0 < (r1 - r0) * S)
         for (size_t i = (size_t)r0 * S + tid; i < (size_t)r1 * S; i += nthr) M[i] = 0.0f;
     if (c < 0) {
-        for (int i = tid; i < nu * FA_UNIT_SLOTS; i += nthr) slots[i] = 0.0f;
         const float *prow = probs + pos * (size_t)fa.V;
         const bool aligned = (reinterpret_cast<uintptr_t>(prow) & 15) == 0 && (CH & 3) == 0;
         const uint2 *g4 = reinterpret_cast<const uint2 *>(fa.ru_tok);
         // a run's sum for the current chunk is stored (not added) into the lane's slot at its
-        // end; after each chunk the lane folds its slots into register totals, in chunk order
+        // end; after each walk the lane folds the slots it wrote into register totals, in chunk
+        // order.  Warp w walks units w and w + FA_RW_WARPS of the block (when it has them).
         float *my = slots + warp * FA_UNIT_SLOTS + lane;
         const uint32_t my_addr = (uint32_t)__cvta_generic_to_shared(my);
-        float tot[FA_RUN_SLOTS];
+        float tot[2][FA_RUN_SLOTS];
 #pragma unroll
-        for (int q = 0; q < FA_RUN_SLOTS; ++q) tot[q] = 0.0f;
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int q = 0; q < FA_RUN_SLOTS; ++q) tot[h][q] = 0.0f;
         for (int ch = 0; ch < nch; ++ch) {
             const int base = ch * CH, n = min(CH, fa.V - base);
             __syncthreads();  // every warp is done with the previous chunk
@@ -231,8 +236,11 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
             asm volatile("cp.async.wait_all;\n" ::: "memory");
             __syncthreads();
             const int boff = 0;
-            if (warp < nu) {
-                const size_t ui = (size_t)(u0 + warp) * nch + ch;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int uw = warp + FA_RW_WARPS * h;
+                if (uw >= nu) break;
+                const size_t ui = (size_t)(u0 + uw) * nch + ch;
                 const int gb = fa.ru_goff[ui];
                 const int ng = (fa.ru_goff[ui + 1] - gb) >> 5;
                 const uint2 *gp = g4 + gb + lane;
@@ -275,27 +283,35 @@ __global__ void __launch_bounds__(32 * FA_RW_MAX_UNITS, 2) k_reweight(DevFA fa, 
                     FA_RW_GROUP(v);
                 }
 #undef FA_RW_GROUP
-                // runs of this lane = run ends seen in the chunk; fold the warp's used slots
-                const int nrun = __reduce_max_sync(0xffffffffu, (int)((slot_addr - my_addr) >> 7));
+                // runs of this lane = run ends seen in the walk; fold the slots it wrote (the
+                // others may hold the sums of the warp's other unit)
+                const int mine = (int)((slot_addr - my_addr) >> 7);
+                const int nrun = __reduce_max_sync(0xffffffffu, mine);
                 __syncwarp();
 #pragma unroll
                 for (int q = 0; q < FA_RUN_SLOTS; ++q) {
                     if (q >= nrun) break;
-                    if constexpr (MAX) tot[q] = fmaxf(tot[q], my[q * 32]); else tot[q] += my[q * 32];
+                    if (q < mine) {
+                        if constexpr (MAX) tot[h][q] = fmaxf(tot[h][q], my[q * 32]); else tot[h][q] += my[q * 32];
+                    }
                 }
+                __syncwarp();  // the next walk reuses the slots
             }
         }
-        if (warp < nu) {
-            __syncwarp();
+        __syncthreads();  // the chunk buffer is free now: it takes the units' totals
 #pragma unroll
-            for (int q = 0; q < FA_RUN_SLOTS; ++q) my[q * 32] = tot[q];
+        for (int h = 0; h < 2; ++h) {
+            const int uw = warp + FA_RW_WARPS * h;
+            if (uw < nu) {
+#pragma unroll
+                for (int q = 0; q < FA_RUN_SLOTS; ++q) utot[uw * FA_UNIT_SLOTS + q * 32 + lane] = tot[h][q];
+            }
         }
-        __syncthreads();
-        for (int i = tid; i < r1 - r0; i += nthr) smax[i] = 0;  // the chunk buffer is free now
+        for (int i = tid; i < r1 - r0; i += nthr) smax[i] = 0;
         __syncthreads();
         for (int cell = c0 + tid; cell < c1; cell += nthr) {
             const int s = fa.cell_src[cell];
-            const float *sb = slots + (size_t)(fa.row_unit0[s] - u0) * FA_UNIT_SLOTS;
+            const float *sb = utot + (size_t)(fa.row_unit0[s] - u0) * FA_UNIT_SLOTS;
             float v = 0.0f;
             for (int q = fa.crun_off[cell]; q < fa.crun_off[cell + 1]; ++q) {
                 if constexpr (MAX) v = fmaxf(v, sb[fa.crun_slot[q]]); else v += sb[fa.crun_slot[q]];
@@ -1634,10 +1650,12 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     const int nrb = a->part_count[p];
     const int4 *rbm = reinterpret_cast<const int4 *>(a->rb_meta) + 2 * a->part_first[p];
     const int max_units = a->part_max_units[p];
-    const int threads = std::min(32 * FA_RW_MAX_UNITS, std::max(256, 32 * max_units));
-    // the staged chunk (whose space takes the row maxima at the end) and the run slots
-    const size_t smem = sizeof(float) * (std::max((size_t)((a->chunk_tokens + 4) & ~3), (size_t)a->part_max_rows[p]) +
-                                         (size_t)max_units * FA_UNIT_SLOTS);
+    const int threads = std::min(32 * FA_RW_WARPS, std::max(256, 32 * max_units));
+    // the staged chunk, whose space takes the units' run totals and the row maxima at the
+    // end, then one run-slot array per warp
+    const int tot_floats = (int)std::max((size_t)((a->chunk_tokens + 4) & ~3),
+                                         (size_t)max_units * FA_UNIT_SLOTS + (size_t)a->part_max_rows[p]);
+    const size_t smem = sizeof(float) * ((size_t)tot_floats + (size_t)(threads / 32) * FA_UNIT_SLOTS);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k_reweight<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
@@ -1645,7 +1663,7 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
         if (e != cudaSuccess) { fa_set_error(std::string("reweight smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     }
     dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
-    (use_max ? k_reweight<true> : k_reweight<false>)<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, max_units, mant, rho, rmax,
+    (use_max ? k_reweight<true> : k_reweight<false>)<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, tot_floats, mant, rho, rmax,
                                             zero, n_zero);
     return launch_check("reweight");
 }
