@@ -979,19 +979,53 @@ __device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float 
     float own = 0.0f;
     for (int i = tid; i < n; i += kLeafThreads) own += __ldg(prow + fa.cell_tok[a0 + i]);
 
-    // the normaliser over the cells of M_t
+    // the normaliser over the cells of M_t (zero everywhere else): through the cell lists, or,
+    // when the cells cover a quarter of the (s, s') pairs or more, over M_t read whole as
+    // float4s in address order (coalesced, no index traffic).  Thread tid takes the float4s
+    // tid, tid + T, ...; its (row, column) advances by a fixed step, without divisions.
     const float *Mt = leaf + pos * (size_t)S * S;
     fa_xacc dx;
     dx.init();
-#pragma unroll 4
-    for (int q = tid; q < fa.n_cells; q += kLeafThreads) {
-        const int s = fa.cell_src[q], d = fa.cell_dst[q];
-        const float a = a_m[s], bv = b_m[d], mv = __ldg(Mt + (size_t)s * S + d);
-        if (a > 0.0f && bv > 0.0f && mv > 0.0f) {
+    auto term = [&](float a, int ea, float mv, int d) {
+        const float bv = b_m[d];
+        if (bv > 0.0f && mv > 0.0f) {
             float mm;
             int em;
             fa_split(mv, mm, em);
-            dx.add(a * bv * mm, a_e[s] + b_e[d] + em);
+            dx.add(a * bv * mm, ea + b_e[d] + em);
+        }
+    };
+    if ((long)fa.n_cells * 4 >= (long)S * S && (S & 3) == 0 && (reinterpret_cast<uintptr_t>(Mt) & 15) == 0) {
+        const int S4 = S >> 2, n4 = S * S4;
+        const int dr = kLeafThreads / S4, dc = kLeafThreads % S4;
+        int r = tid / S4, c4 = tid % S4;
+        const float4 *M4 = reinterpret_cast<const float4 *>(Mt);
+#pragma unroll 4
+        for (int i = tid; i < n4; i += kLeafThreads) {
+            const float4 mv = __ldg(M4 + i);
+            const float a = a_m[r];
+            if (a > 0.0f) {
+                const int ea = a_e[r], d = 4 * c4;
+                term(a, ea, mv.x, d);
+                term(a, ea, mv.y, d + 1);
+                term(a, ea, mv.z, d + 2);
+                term(a, ea, mv.w, d + 3);
+            }
+            r += dr;
+            c4 += dc;
+            if (c4 >= S4) { c4 -= S4; ++r; }
+        }
+    } else {
+#pragma unroll 4
+        for (int q = tid; q < fa.n_cells; q += kLeafThreads) {
+            const int s = fa.cell_src[q], d = fa.cell_dst[q];
+            const float a = a_m[s], bv = b_m[d], mv = __ldg(Mt + (size_t)s * S + d);
+            if (a > 0.0f && bv > 0.0f && mv > 0.0f) {
+                float mm;
+                int em;
+                fa_split(mv, mm, em);
+                dx.add(a * bv * mm, a_e[s] + b_e[d] + em);
+            }
         }
     }
 
@@ -1065,7 +1099,7 @@ __device__ void topk_row(int b, int L, int k, int lo, int hi, float *marg, const
 
 // Leaves, then the commit: every block takes its sequence's ticket after its position is
 // written; the last block of a sequence sees all of its marginals and runs its top-k.
-__global__ void __launch_bounds__(kLeafThreads) k_leaf_commit(DevFA fa, int B, int L, const float *__restrict__ probs,
+__global__ void __launch_bounds__(kLeafThreads, 1) k_leaf_commit(DevFA fa, int B, int L, const float *__restrict__ probs,
                                                             const int32_t *__restrict__ committed, uint64_t seed,
                                                             uint64_t offset, const int32_t *__restrict__ z,
                                                             const float *__restrict__ am,
