@@ -304,10 +304,13 @@ std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_
     }
     crun_off[n_cells] = (int32_t)crun_slot.size();
 
-    // reweight blocks: whole row groups, at most FA_RW_MAX_UNITS >> p units per block in partition p
+    // reweight blocks: whole row groups, at most caps[p] units per block in partition p
     std::vector<int32_t> &rbm = out.rbm;
+    std::vector<int> caps{FA_RW_MAX_UNITS};
+    for (int c = 32; c >= 1; c >>= 1)
+        if (c < caps.back()) caps.push_back(c);
     for (int p = 0;; ++p) {
-        const int cap = FA_RW_MAX_UNITS >> p;
+        const int cap = caps[p];
         out.part_first.push_back((int32_t)(rbm.size() / 8));
         int count = 0, maxu = 1, maxr = 1;
         for (size_t gi = 0; gi < groups.size();) {
@@ -324,7 +327,7 @@ std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_
         out.part_count.push_back(count);
         out.part_max_units.push_back(maxu);
         out.part_max_rows.push_back(maxr);
-        if (cap == 1 || count == (int)groups.size()) break;
+        if (p + 1 == (int)caps.size() || count == (int)groups.size()) break;
     }
     return std::string();
 }

@@ -54,7 +54,8 @@ struct fa_automaton {
     int32_t *ru_goff = nullptr, *row_unit0 = nullptr, *crun_off = nullptr;
     uint16_t *crun_slot = nullptr;
     // row blocks for the reweight grid: partition p holds part_count[p] blocks of whole rows
-    // (at most FA_RW_MAX_UNITS >> p units each, unless one row group needs more); block i of partition p
+    // (at most FA_RW_MAX_UNITS, 32, 16, ..., 1 units each for p = 0, 1, 2, ..., unless one row group
+    // needs more); block i of partition p
     // is rb_meta[8 * (part_first[p] + i) ..] = {r0, r1, u0, u1, c0, c1, 0, 0}, launched with
     // 32 * part_max_units[p] threads.
     int32_t *rb_meta = nullptr;
@@ -78,7 +79,7 @@ void fa_set_error(const std::string &msg);
 #endif
 #define FA_UNIT_SLOTS (32 * FA_RUN_SLOTS)
 #define FA_RW_WARPS 16               // warps per reweight block (two blocks per SM)
-#define FA_RW_MAX_UNITS 32           // warp units per reweight block: a warp walks up to two
+#define FA_RW_MAX_UNITS 48           // warp units per reweight block: a warp walks up to three
 
 // floor(log2 x) of a positive normal float from its exponent field (subnormals give -127).
 __device__ __forceinline__ int fa_exponent(float x) {

@@ -170,7 +170,7 @@ __device__ int warp_categorical(int n, float u, WF w) {
 // in a fixed order, so the result is deterministic.
 // MAX = true: the max-product variant for greedy decoding, M_t(s, s') = max over the tokens of
 // the edges s -> s' of w_t(v) (a committed position: 1 where an edge carries its token).
-template <bool MAX>
+template <bool MAX, int UPW>
 __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int L, const float *__restrict__ probs,
                                                                 const int32_t *__restrict__ committed,
                                                                 const int4 *__restrict__ rbm, int nrb, int tot_floats,
@@ -209,12 +209,12 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
         const uint2 *g4 = reinterpret_cast<const uint2 *>(fa.ru_tok);
         // a run's sum for the current chunk is stored (not added) into the lane's slot at its
         // end; after each walk the lane folds the slots it wrote into register totals, in chunk
-        // order.  Warp w walks units w and w + FA_RW_WARPS of the block (when it has them).
+        // order.  Warp w walks units w, w + FA_RW_WARPS, ... of the block (UPW at most).
         float *my = slots + warp * FA_UNIT_SLOTS + lane;
         const uint32_t my_addr = (uint32_t)__cvta_generic_to_shared(my);
-        float tot[2][FA_RUN_SLOTS];
+        float tot[UPW][FA_RUN_SLOTS];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < UPW; ++h)
 #pragma unroll
             for (int q = 0; q < FA_RUN_SLOTS; ++q) tot[h][q] = 0.0f;
         for (int ch = 0; ch < nch; ++ch) {
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
             __syncthreads();
             const int boff = 0;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < UPW; ++h) {
                 const int uw = warp + FA_RW_WARPS * h;
                 if (uw >= nu) break;
                 const size_t ui = (size_t)(u0 + uw) * nch + ch;
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
         }
         __syncthreads();  // the chunk buffer is free now: it takes the units' totals
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < UPW; ++h) {
             const int uw = warp + FA_RW_WARPS * h;
             if (uw < nu) {
 #pragma unroll
@@ -1660,10 +1660,10 @@ void stage_mark(int i, cudaStream_t s) {
 }
 
 int pick_partition(const fa_automaton *a, long positions) {
-    // the first partition giving about two blocks per SM over all positions: every extra
+    // the first partition giving about three blocks per SM over all positions: every extra
     // block re-stages its probability row and repeats its metadata round trips
     int p = 0;
-    while (p + 1 < (int)a->part_count.size() && positions * a->part_count[p] < 152L * 2) ++p;
+    while (p + 1 < (int)a->part_count.size() && positions * a->part_count[p] < 152L * 3) ++p;
     return p;
 }
 
@@ -1690,15 +1690,19 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     const int tot_floats = (int)std::max((size_t)((a->chunk_tokens + 4) & ~3),
                                          (size_t)max_units * FA_UNIT_SLOTS + (size_t)a->part_max_rows[p]);
     const size_t smem = sizeof(float) * ((size_t)tot_floats + (size_t)(threads / 32) * FA_UNIT_SLOTS);
+    // units per warp: the register totals of a third unit cost the smaller layouts ~10%
+    const int upw = (max_units + FA_RW_WARPS - 1) / FA_RW_WARPS;
+    using K = void (*)(DevFA, int, const float *, const int32_t *, const int4 *, int, int, float *, int32_t *, int32_t *,
+                       int32_t *, long);
+    K kern = upw <= 1 ? (use_max ? (K)k_reweight<true, 1> : (K)k_reweight<false, 1>)
+             : upw == 2 ? (use_max ? (K)k_reweight<true, 2> : (K)k_reweight<false, 2>)
+                        : (use_max ? (K)k_reweight<true, 3> : (K)k_reweight<false, 3>);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_reweight<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_reweight<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) { fa_set_error(std::string("reweight smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     }
     dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
-    (use_max ? k_reweight<true> : k_reweight<false>)<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, tot_floats, mant, rho, rmax,
-                                            zero, n_zero);
+    kern<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, tot_floats, mant, rho, rmax, zero, n_zero);
     return launch_check("reweight");
 }
 
