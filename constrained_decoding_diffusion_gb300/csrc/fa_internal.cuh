@@ -30,7 +30,12 @@ struct fa_automaton {
     int32_t *accept = nullptr;       // [n_accept] ascending
     int32_t *accept_mask = nullptr;  // [S] 0/1
     int32_t *edge_src = nullptr, *edge_dst = nullptr;
-    uint32_t *tok_sd = nullptr;      // [I] (src << 16) | dst of incidence j of the token->edge CSR
+    // (src << 16) | dst of every incidence, token-major and interleaved by groups of 32
+    // consecutive tokens: row k of group g (rows tok_goff[g] .. tok_goff[g + 1]) holds incidence
+    // k of tokens 32 g + lane at tok_sd[32 * row + lane], FA_SD_NONE past a token's count, so a
+    // warp reading one row reads 128 contiguous bytes
+    uint32_t *tok_sd = nullptr;
+    int64_t *tok_goff = nullptr;     // [ceil(V / 32) + 1]
     // cells (device), sorted by (src, dst)
     int32_t *row_cell_off = nullptr;  // [S+1]
     int32_t *cell_dst = nullptr;      // [n_cells]
@@ -72,6 +77,7 @@ void fa_set_error(const std::string &msg);
 #ifndef FA_REWEIGHT_MAX_CHUNK
 #define FA_REWEIGHT_MAX_CHUNK 24576  // tokens per staged vocabulary chunk
 #endif
+#define FA_SD_NONE 0xFFFFFFFFu       // tok_sd padding
 #define FA_RUN_END 0x8000u           // entry flag: last entry of the lane's current run
 #define FA_GROUP_ENTRIES 4           // entries per 8-byte group; runs end only at group ends
 #ifndef FA_RUN_SLOTS

@@ -22,7 +22,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTmChunk = 4096;   // tokens per block of the all-token marginals
+constexpr int kTmChunkMax = 4096, kTmChunkMin = 1024;  // tokens per block of the all-token marginals
 constexpr int kWarps = kThreads / 32;
 
 // ----------------------------------------------------------------------------- workspace plan
@@ -32,7 +32,7 @@ struct Plan {
     int nk[18] = {0};
     size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, mu[18] = {0};
     size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, conf = 0, den_m = 0, den_e = 0, tm_part = 0, zsum = 0, zexp = 0;
-    int tm_chunks = 1;
+    int tm_chunks = 1, tm_chunk = kTmChunkMax;
     size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0, img = 0;
     size_t total = 0;
 };
@@ -80,7 +80,11 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
     p.den_m = take((size_t)B * (size_t)L * sizeof(float));
     p.den_e = take((size_t)B * (size_t)L * sizeof(int32_t));
     // per (position, vocabulary chunk) partial sums of p ln p for the entropies
-    p.tm_chunks = (a->V + kTmChunk - 1) / kTmChunk;
+    // (4096 tokens per block, halved down to 1024 while that gives under 4096 blocks in all:
+    //  few positions need the narrower blocks to fill the GPU)
+    p.tm_chunk = kTmChunkMax;
+    while (p.tm_chunk > kTmChunkMin && (long)B * L * ((a->V + p.tm_chunk - 1) / p.tm_chunk) < 4096) p.tm_chunk >>= 1;
+    p.tm_chunks = (a->V + p.tm_chunk - 1) / p.tm_chunk;
     p.tm_part = take((size_t)B * (size_t)L * (size_t)p.tm_chunks * sizeof(double));
     // tensor-core operand images, sized for the level with the most node slots (level 1)
     if (fa_span_tc_supported(a->S) && p.K >= 1) p.img = take(fa_span_tc_image_bytes(a->S, (long)B * p.nk[1]));
@@ -95,6 +99,7 @@ struct DevFA {
     int S, V, start, n_accept;
     const int32_t *accept, *accept_mask, *edge_src, *edge_dst;
     const uint32_t *tok_sd;
+    const int64_t *tok_goff;
     const int64_t *tok_off;
     const int32_t *tok_edges;
     const int32_t *row_cell_off, *cell_dst, *cell_src;
@@ -110,6 +115,7 @@ DevFA dev_view(const fa_automaton *a) {
     d.S = a->S; d.V = a->V; d.start = a->start; d.n_accept = a->n_accept;
     d.accept = a->accept; d.accept_mask = a->accept_mask; d.edge_src = a->edge_src; d.edge_dst = a->edge_dst;
     d.tok_sd = a->tok_sd;
+    d.tok_goff = a->tok_goff;
     d.tok_off = a->tok_off; d.tok_edges = a->tok_edges;
     d.row_cell_off = a->row_cell_off; d.cell_dst = a->cell_dst; d.cell_src = a->cell_src;
     d.cell_off = a->cell_off; d.cell_tok = a->cell_tok;
@@ -1134,13 +1140,15 @@ __global__ void __launch_bounds__(kLeafThreads, 1) k_leaf_commit(DevFA fa, int B
 //   p(x_t = v) = w_t(v) sum_{e carries v} alpha_{t-1}(src e) beta_t(dst e) / D_t,
 // D_t = alpha_{t-1}^T M_t beta_t the local normaliser the leaves computed (the same sum taken
 // over the cells), and the entropy H_t = -sum_v p ln p.  One block per (position, chunk of
-// kTmChunk tokens); token v is summed by one thread over its incidences in CSR order, the
-// block's sum of p ln p lands in a per-chunk slot, and k_tm_finish adds the slots in chunk
-// order, so the result is deterministic.
+// `chunk_tokens` tokens, a multiple of 32); token v is summed by one thread over its
+// incidences (interleaved by groups of 32 tokens, see fa_automaton), the block's sum of
+// p ln p lands in a per-chunk slot, and k_tm_finish adds the slots in chunk order, so the
+// result is deterministic.
 constexpr int kTmThreads = 256;
 constexpr int kTmWarps = kTmThreads / 32;
 
-__global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int n_chunks, const float *__restrict__ probs,
+__global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int n_chunks, int chunk_tokens,
+                                                          const float *__restrict__ probs,
                                                           const int32_t *__restrict__ committed,
                                                           const int32_t *__restrict__ status,
                                                           const float *__restrict__ am, const int32_t *__restrict__ ae,
@@ -1148,14 +1156,14 @@ __global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int 
                                                           const float *__restrict__ den_m,
                                                           const int32_t *__restrict__ den_e, float *marg_all,
                                                           double *part) {
-    extern __shared__ float tm_s[];  // [4 S]: alpha and beta mantissas, then their exponents
+    extern __shared__ float2 tm_s[];  // [2 S]: (mantissa, exponent bits) of alpha, then of beta
     __shared__ double red[kTmWarps];
     const int S = fa.S, V = fa.V;
     const size_t pos = blockIdx.x / (unsigned)n_chunks;
     const int chunk = (int)(blockIdx.x % (unsigned)n_chunks);
     const int b = (int)(pos / (size_t)L), t = (int)(pos % (size_t)L);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int v0 = chunk * kTmChunk, v1 = min(V, v0 + kTmChunk);
+    const int v0 = chunk * chunk_tokens, v1 = min(V, v0 + chunk_tokens);
     const int c = committed[pos];
     float *out = marg_all ? marg_all + pos * (size_t)V : nullptr;
     const float dm = (c >= 0 || status[b] != FA_ROW_OK) ? 0.0f : den_m[pos];
@@ -1167,30 +1175,38 @@ __global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int 
     }
     const int E = den_e[pos];
     const float inv = 1.0f / dm;
-    float *sam = tm_s, *sbm = tm_s + S;
-    int *sae = reinterpret_cast<int *>(tm_s + 2 * S), *sbe = sae + S;
+    float2 *sa = tm_s, *sb = tm_s + S;
     const size_t ba = ((size_t)b * (L + 1) + t) * S, bb = ba + S;
     for (int s = tid; s < S; s += kTmThreads) {
-        sam[s] = am[ba + s]; sae[s] = ae[ba + s];
-        sbm[s] = bm[bb + s]; sbe[s] = be[bb + s];
+        sa[s] = make_float2(am[ba + s], __int_as_float(ae[ba + s]));
+        sb[s] = make_float2(bm[bb + s], __int_as_float(be[bb + s]));
     }
     __syncthreads();
     const float *prow = probs + pos * (size_t)V;
     float sl = 0.0f, cl = 0.0f;  // compensated sum of p ln p
-    for (int v = v0 + tid; v < v1; v += kTmThreads) {
-        const float w = __ldg(prow + v);
+    // warp w takes the token groups g0 + w, g0 + w + kTmWarps, ...; lane l the token 32 g + l,
+    // reading row k of the group's interleaved incidences (one 128-byte line per warp)
+    for (int g = v0 / 32 + warp; g < (v1 + 31) / 32; g += kTmWarps) {
+        const int v = 32 * g + lane;
+        const float w = v < v1 ? __ldg(prow + v) : 0.0f;
+        const int64_t r0 = fa.tok_goff[g], nr = fa.tok_goff[g + 1] - r0;
+        const uint32_t *col = fa.tok_sd + (size_t)r0 * 32 + lane;
         float acc = 0.0f;
-        if (w > 0.0f) {
-            const int64_t j0 = fa.tok_off[v], j1 = fa.tok_off[v + 1];
-#pragma unroll 4
-            for (int64_t j = j0; j < j1; ++j) {
-                const uint32_t sd = __ldg(fa.tok_sd + j);
-                const int s = (int)(sd >> 16), d = (int)(sd & 0xffffu);
-                const float a = sam[s], bq = sbm[d];
-                if (a > 0.0f && bq > 0.0f) acc += a * bq * fa_pow2(sae[s] + sbe[d] - E);
+        for (int64_t k0 = 0; k0 < nr; k0 += 8) {
+            uint32_t sdv[8];  // eight rows' loads in flight before any is used
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sdv[u] = k0 + u < nr ? __ldg(col + (size_t)(k0 + u) * 32) : FA_SD_NONE;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t sd = sdv[u];
+                if (sd != FA_SD_NONE) {
+                    const float2 a = sa[sd >> 16], bq = sb[sd & 0xffffu];
+                    if (a.x > 0.0f && bq.x > 0.0f) acc += a.x * bq.x * fa_pow2(__float_as_int(a.y) + __float_as_int(bq.y) - E);
+                }
             }
         }
-        const float pv = w * acc * inv;
+        if (v >= v1) continue;
+        const float pv = w > 0.0f ? w * acc * inv : 0.0f;
         if (out) out[v] = pv;
         if (pv > 0.0f) {
             const float y = pv * logf(pv) - cl, tt = sl + y;
@@ -1719,7 +1735,7 @@ fa_status launch_token_marginals(const fa_automaton *aut, int B, int L, const fl
     double *part = (double *)(ws + p.tm_part);
     const long n_pos = (long)B * L;
     k_tm_partial<<<(unsigned)(n_pos * p.tm_chunks), kTmThreads, smem, st>>>(
-        dev_view(aut), L, p.tm_chunks, probs, committed, row_status, F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.den_m),
+        dev_view(aut), L, p.tm_chunks, p.tm_chunk, probs, committed, row_status, F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.den_m),
         I(p.den_e), marg_all, part);
     fa_status s = launch_check("token marginals");
     if (s != FA_OK) return s;

@@ -389,3 +389,28 @@ def test_step_tensor_core_span_products(native, S):
     committed[0, idx] = x[idx]
     res = run_step(aut, probs, committed, seed=5, offset=1, k=4)
     check_against_oracle(fa, o, probs, committed, res, 4)
+
+
+def test_sequence_results_do_not_depend_on_the_batch(native):
+    """Sequence b's draws depend only on the seed, the offset, b and its own inputs: the first
+    16 sequences of a batch of 17 and the same 16 run alone give the same midpoints, tokens,
+    logZ and marginals; both checked against the oracle."""
+    rng = np.random.default_rng(40)
+    fa = synth.random_dfa(48, 500, 0.6, 6, seed=40)
+    aut = native.fa_compile(fa)
+    B, L = 17, 37
+    probs = synth.gaussian_probs(rng, B, L, 500, 2.5)
+    committed = np.full((B, L), -1, np.int32)
+    for b in range(B):
+        x = synth.random_accepted_string(fa, L, rng)
+        pos = rng.choice(L, size=8, replace=False)
+        committed[b, pos] = x[pos]
+    whole = run_step(aut, probs, committed, seed=6, offset=2, k=5)
+    part = run_step(aut, probs[:16], committed[:16], seed=6, offset=2, k=5)
+    np.testing.assert_array_equal(part["status"], whole["status"][:16])
+    np.testing.assert_array_equal(part["tokens"], whole["tokens"][:16])
+    np.testing.assert_array_equal(part["logZ"], whole["logZ"][:16])
+    np.testing.assert_allclose(part["marg"], whole["marg"][:16], rtol=0, atol=1e-6)
+    o = oracle.OracleFA(fa)
+    check_against_oracle(fa, o, probs[:16], committed[:16], part, 5, rows=[0, 7, 15])
+    check_against_oracle(fa, o, probs, committed, whole, 5, rows=[16])
