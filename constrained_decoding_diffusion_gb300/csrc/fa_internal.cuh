@@ -50,19 +50,18 @@ struct fa_automaton {
     // (k = 0, 1, ...): bits 0-14 give the in-chunk token index (chunk_tokens = a zero pad
     // slot); a run's entries fill whole groups, and bit 15 of a group's last entry ends the
     // lane's current run (every run ends exactly once per chunk, so slot j of a lane is its
-    // j-th run).  A
-    // lane's slot j is at FA_UNIT_SLOTS * (unit - row_unit0[row]) + 32 j + lane relative to the first
-    // unit of the row's group; cell x adds the slots crun_slot[crun_off[x] .. crun_off[x+1]]
-    // in order.
+    // j-th run).  A lane's slot j is at FA_UNIT_SLOTS * (unit - row_unit0[row]) + 32 j + lane
+    // relative to the first unit of the row's group; cell x adds the slots
+    // crun_slot[crun_off[x] .. crun_off[x+1]] in order.
     int32_t chunk_tokens = 0, n_chunks = 1, n_units = 0;
     uint16_t *ru_tok = nullptr;
     int32_t *ru_goff = nullptr, *row_unit0 = nullptr, *crun_off = nullptr;
     uint16_t *crun_slot = nullptr;
     // row blocks for the reweight grid: partition p holds part_count[p] blocks of whole rows
-    // (at most FA_RW_MAX_UNITS, 32, 16, ..., 1 units each for p = 0, 1, 2, ..., unless one row group
-    // needs more); block i of partition p
-    // is rb_meta[8 * (part_first[p] + i) ..] = {r0, r1, u0, u1, c0, c1, 0, 0}, launched with
-    // 32 * part_max_units[p] threads.
+    // (at most FA_RW_MAX_UNITS, 32, 16, ..., 1 units each for p = 0, 1, 2, ..., unless one row
+    // group needs more); block i of partition p is rb_meta[8 * (part_first[p] + i) ..] =
+    // {r0, r1, u0, u1, c0, c1, 0, 0}, launched with min(32 FA_RW_WARPS, max(256,
+    // 32 part_max_units[p])) threads, a warp walking up to three units.
     int32_t *rb_meta = nullptr;
     std::vector<int32_t> part_first, part_count, part_max_units, part_max_rows;
     void *blob = nullptr;  // one device allocation holding every array above

@@ -169,11 +169,12 @@ __device__ int warp_categorical(int n, float u, WF w) {
 // position counts the edges s -> s' that carry its token.
 //
 // The probability row is staged in shared memory one vocabulary chunk at a time (the whole
-// row when |V| <= 32767) by asynchronous copies.  Warp w walks the entry stream of warp unit
-// u0 + w (see fa_automaton): lane l adds the staged probabilities of its entries and, at
-// each run end, moves the running sum into the run's slot, so every run's slots collect
-// one sum per chunk in chunk order.  After the last chunk every cell adds its runs' slots
-// in a fixed order, so the result is deterministic.
+// row when |V| <= FA_REWEIGHT_MAX_CHUNK) by asynchronous copies.  Warp w walks the entry
+// streams of units u0 + w, u0 + w + FA_RW_WARPS, ... (UPW at most; see fa_automaton): lane l
+// adds the staged probabilities of its entries and, at each run end, stores the run's chunk
+// sum into its slot; after each walk the lane folds those slots into the unit's register
+// totals, in chunk order.  After the last chunk the totals go to the freed chunk buffer and
+// every cell adds its runs' totals in a fixed order, so the result is deterministic.
 // MAX = true: the max-product variant for greedy decoding, M_t(s, s') = max over the tokens of
 // the edges s -> s' of w_t(v) (a committed position: 1 where an edge carries its token).
 template <bool MAX, int UPW>
