@@ -178,3 +178,19 @@ def test_confidence_does_not_change_the_sample(native):
         for key in ("tokens", "logZ", "marg", "status", "entropy"):
             np.testing.assert_array_equal(r[key], outs[0][key])
     check_against_oracle(fa, oracle.OracleFA(fa), probs, committed, outs[0], 4)
+
+
+def test_full_marginals_wide_vocabulary_blocks(native):
+    """4096 positions: the all-token pass takes its widest vocabulary blocks (4096 tokens;
+    the small cases above run 1024-token blocks).  Two sequences against the oracle."""
+    rng = np.random.default_rng(52)
+    fa = synth.random_dfa(16, 5000, 0.6, 4, seed=52)
+    B, L = 16, 256
+    probs = synth.gaussian_probs(rng, B, L, fa.vocab, 3.0)
+    committed = np.full((B, L), -1, np.int32)
+    for b in (0, 9):
+        x = synth.random_accepted_string(fa, L, rng)
+        pos = rng.choice(L, size=40, replace=False)
+        committed[b, pos] = x[pos]
+    res = run(native, fa, probs, committed, 61, 4)
+    check_full(fa, probs, committed, res, rows=[0, 9])
