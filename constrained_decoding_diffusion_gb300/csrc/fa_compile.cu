@@ -464,18 +464,26 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     a->part_max_rows = rl.part_max_rows;
 
     std::vector<int32_t> esrc(edge_src, edge_src + E), edst(edge_dst, edge_dst + E);
-    // the (src, dst) pair of every token-edge incidence (|S| <= 4096 fits 16 bits), interleaved
-    // by groups of 32 consecutive tokens, each group as many rows as its longest token
+    // the (src, dst) pair of every token-edge incidence (|S| <= 4096 fits 16 bits), the tokens
+    // ordered by incidence count (ties by id) and interleaved by groups of 32, each group as
+    // many rows as its longest token: tokens of nearly equal counts share a group, so the
+    // padding stays near one row per incidence however skewed the counts are
     const int64_t n_tg = ((int64_t)V + 31) / 32;
+    std::vector<int32_t> tok_perm(V);
+    std::iota(tok_perm.begin(), tok_perm.end(), 0);
+    std::stable_sort(tok_perm.begin(), tok_perm.end(), [&](int32_t x, int32_t y) {
+        return tok_off[x + 1] - tok_off[x] < tok_off[y + 1] - tok_off[y];
+    });
     std::vector<int64_t> tok_goff(n_tg + 1, 0);
     for (int64_t g = 0; g < n_tg; ++g) {
         int64_t cnt = 0;
-        for (int64_t v = 32 * g; v < std::min<int64_t>(32 * g + 32, V); ++v) cnt = std::max(cnt, tok_off[v + 1] - tok_off[v]);
+        for (int64_t i = 32 * g; i < std::min<int64_t>(32 * g + 32, V); ++i)
+            cnt = std::max(cnt, tok_off[tok_perm[i] + 1] - tok_off[tok_perm[i]]);
         tok_goff[g + 1] = tok_goff[g] + cnt;
     }
     std::vector<uint32_t> tok_sd((size_t)tok_goff[n_tg] * 32, FA_SD_NONE);
-    for (int64_t v = 0; v < V; ++v) {
-        const int64_t g = v / 32, lane = v % 32;
+    for (int64_t i = 0; i < V; ++i) {
+        const int64_t g = i / 32, lane = i % 32, v = tok_perm[i];
         for (int64_t k = 0; k < tok_off[v + 1] - tok_off[v]; ++k) {
             const int e = tok_edges[tok_off[v] + k];
             tok_sd[(size_t)(tok_goff[g] + k) * 32 + lane] = ((uint32_t)edge_src[e] << 16) | (uint32_t)edge_dst[e];
@@ -497,6 +505,7 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     bb.add(&a->edge_dst, edst);
     bb.add(&a->tok_sd, tok_sd);
     bb.add(&a->tok_goff, tok_goff);
+    bb.add(&a->tok_perm, tok_perm);
     bb.add(&a->row_cell_off, row_cell_off);
     bb.add(&a->cell_dst, cell_dst);
     bb.add(&a->cell_src, cell_src);

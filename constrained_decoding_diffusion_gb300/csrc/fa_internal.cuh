@@ -30,12 +30,14 @@ struct fa_automaton {
     int32_t *accept = nullptr;       // [n_accept] ascending
     int32_t *accept_mask = nullptr;  // [S] 0/1
     int32_t *edge_src = nullptr, *edge_dst = nullptr;
-    // (src << 16) | dst of every incidence, token-major and interleaved by groups of 32
-    // consecutive tokens: row k of group g (rows tok_goff[g] .. tok_goff[g + 1]) holds incidence
-    // k of tokens 32 g + lane at tok_sd[32 * row + lane], FA_SD_NONE past a token's count, so a
-    // warp reading one row reads 128 contiguous bytes
+    // (src << 16) | dst of every incidence, token-major: tokens in the order tok_perm (by
+    // incidence count, ties by id), interleaved by groups of 32: row k of group g (rows
+    // tok_goff[g] .. tok_goff[g + 1]) holds incidence k of token tok_perm[32 g + lane] at
+    // tok_sd[32 * row + lane], FA_SD_NONE past a token's count, so a warp reading one row
+    // reads 128 contiguous bytes
     uint32_t *tok_sd = nullptr;
     int64_t *tok_goff = nullptr;     // [ceil(V / 32) + 1]
+    int32_t *tok_perm = nullptr;     // [V]
     // cells (device), sorted by (src, dst)
     int32_t *row_cell_off = nullptr;  // [S+1]
     int32_t *cell_dst = nullptr;      // [n_cells]

@@ -100,6 +100,7 @@ struct DevFA {
     const int32_t *accept, *accept_mask, *edge_src, *edge_dst;
     const uint32_t *tok_sd;
     const int64_t *tok_goff;
+    const int32_t *tok_perm;
     const int64_t *tok_off;
     const int32_t *tok_edges;
     const int32_t *row_cell_off, *cell_dst, *cell_src;
@@ -116,6 +117,7 @@ DevFA dev_view(const fa_automaton *a) {
     d.accept = a->accept; d.accept_mask = a->accept_mask; d.edge_src = a->edge_src; d.edge_dst = a->edge_dst;
     d.tok_sd = a->tok_sd;
     d.tok_goff = a->tok_goff;
+    d.tok_perm = a->tok_perm;
     d.tok_off = a->tok_off; d.tok_edges = a->tok_edges;
     d.row_cell_off = a->row_cell_off; d.cell_dst = a->cell_dst; d.cell_src = a->cell_src;
     d.cell_off = a->cell_off; d.cell_tok = a->cell_tok;
@@ -1185,11 +1187,13 @@ __global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int 
     __syncthreads();
     const float *prow = probs + pos * (size_t)V;
     float sl = 0.0f, cl = 0.0f;  // compensated sum of p ln p
-    // warp w takes the token groups g0 + w, g0 + w + kTmWarps, ...; lane l the token 32 g + l,
-    // reading row k of the group's interleaved incidences (one 128-byte line per warp)
+    // the block's range [v0, v1) is in the tok_perm order; warp w takes the token groups
+    // g0 + w, g0 + w + kTmWarps, ...; lane l the token tok_perm[32 g + l], reading row k of
+    // the group's interleaved incidences (one 128-byte line per warp)
     for (int g = v0 / 32 + warp; g < (v1 + 31) / 32; g += kTmWarps) {
-        const int v = 32 * g + lane;
-        const float w = v < v1 ? __ldg(prow + v) : 0.0f;
+        const int i = 32 * g + lane;
+        const int v = i < v1 ? __ldg(fa.tok_perm + i) : 0;
+        const float w = i < v1 ? __ldg(prow + v) : 0.0f;
         const int64_t r0 = fa.tok_goff[g], nr = fa.tok_goff[g + 1] - r0;
         const uint32_t *col = fa.tok_sd + (size_t)r0 * 32 + lane;
         float acc = 0.0f;
@@ -1206,7 +1210,7 @@ __global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int 
                 }
             }
         }
-        if (v >= v1) continue;
+        if (i >= v1) continue;
         const float pv = w > 0.0f ? w * acc * inv : 0.0f;
         if (out) out[v] = pv;
         if (pv > 0.0f) {
