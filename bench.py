@@ -5,8 +5,10 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [-
 
 One step = one fa_constrained_step call over one batch: emission reweighting, the span
 up-sweep, root and top-down sampling with prefix/suffix messages, leaf tokens with
-constrained marginals, and the top-k commit.  The default workload is the random DFA with
-64 states, vocabulary 32000, L=128, B=1, half the positions committed (synthetic, seeded).
+constrained marginals, and the top-k commit.  The default workload is the block-wise
+decoding batch: a random DFA with 512 states (p_dead 0.9), vocabulary 151936, B=16
+sequences of L=512 positions, all masked at the first step (synthetic, seeded); its whole
+64-step block-wise remasking schedule is timed beside the step.  --workload picks another.
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier and a device
 synchronisation on both sides; each step is one CUDA-graph replay of the step, bracketed
@@ -15,7 +17,8 @@ Stage boundaries are recorded inside the graph (fa_profile_enable), which gives 
 per-stage device time used for the roofline of the dominant stage.  N > 1 runs
 independent replicas (one per GPU, weak scaling); rank 0 prints one JSON line.
 
---impl reference times the float64 CPU oracle on the host cores on the same workload.
+--impl reference times the float64 CPU oracle on the host cores on the same workload, a
+bounded sample per step (the first sequences of the batch, as many as fit about 20 s).
 """
 from __future__ import annotations
 
@@ -36,15 +39,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ms per constrained denoising step and positions/s at 1 GB300; % of roofline"
 UNIT = "positions/s"
-DEFAULT_WORKLOAD = "random_dfa_S64_L128"
+DEFAULT_WORKLOAD = "blockwise_dfa_S512_L512"
 FLUSH_BYTES = 256 << 20
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-graph", action="store_true", help="launch the step eagerly instead of a graph replay")
@@ -54,8 +57,10 @@ def parse():
     ap.add_argument("--method", default="tree", choices=["tree", "chain", "greedy"],
                     help="log-depth tree (default), the O(L) chain form of the same step, or greedy (T=0) "
                          "decoding by max-product over the tree")
-    ap.add_argument("--schedule", action="store_true",
-                    help="also time the workload's whole remasking schedule (block-wise workload)")
+    ap.add_argument("--schedule", dest="schedule", action="store_true", default=True,
+                    help="also time the workload's whole remasking schedule (workloads with one; the default)")
+    ap.add_argument("--no-schedule", dest="schedule", action="store_false",
+                    help="skip the remasking schedule")
     ap.add_argument("--confidence", default="marginal", choices=["marginal", "neg_entropy", "unconstrained"],
                     help="remasking confidence the commit ranks by")
     return ap.parse_args()
@@ -103,21 +108,27 @@ def replica_value(positions_per_rank, world, ms_max):
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks, power and throttle reasons sampled every 200 ms while running.
+
+    Start it before the warm-up (wait_first() blocks until nvidia-smi answers), bracket the
+    timed region with mark_start() / mark_end(), and summary() keeps the samples taken
+    inside that window (all samples, flagged, if the window caught none)."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 200
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []          # (monotonic time, csv line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -127,7 +138,20 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def wait_first(self, timeout: float = 10.0):
+        end = time.monotonic() + timeout
+        while self.proc is not None and not self.lines and time.monotonic() < end and self.proc.poll() is None:
+            time.sleep(0.02)
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        # one more period so the sample covering the end of the region is read
+        self.t1 = time.monotonic()
+        time.sleep(self.PERIOD_MS / 1e3 + 0.05)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -138,27 +162,57 @@ class ClockSampler:
                 self.proc.kill()
             self.t.join(timeout=2)
 
-    def summary(self):
-        if not self.lines:
+    @staticmethod
+    def _parse(ln):
+        f = [x.strip() for x in ln.split(",")]
+        if len(f) < 9:
             return None
-        sm, mx, reasons = [], [], set()
+        try:
+            sm, mx = float(f[1]), float(f[2])
+        except ValueError:
+            return None
+        try:
+            pw = float(f[3])
+        except ValueError:
+            pw = None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        reasons = [n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")]
+        return sm, mx, pw, reasons
+
+    def summary(self):
+        rows = [(t, self._parse(ln)) for t, ln in self.lines]
+        rows = [(t, r) for t, r in rows if r is not None]
+        if not rows:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        t0 = self.t0 if self.t0 is not None else -math.inf
+        t1 = (self.t1 + self.PERIOD_MS / 1e3) if self.t1 is not None else math.inf
+        inside = [r for t, r in rows if t0 <= t <= t1]
+        use = inside if inside else [r for _, r in rows]
+        sm = [r[0] for r in use]
+        pw = [r[2] for r in use if r[2] is not None]
+        reasons = sorted({n for r in use for n in r[3]})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(r[1] for r in use)), "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_median": float(np.median(pw)) if pw else None,
+                "window_s": (self.t1 - self.t0) if (self.t0 is not None and self.t1 is not None) else None}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU baseline."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 # ----------------------------------------------------------------------------- roofline model
@@ -267,12 +321,12 @@ def cpu_baseline(w, probs, seconds: float, greedy: bool = False):
             el = time.perf_counter() - t0
             if el >= seconds:
                 break
-        return {"value": reps * nb * w.L / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+        return {"value": reps * nb * w.L / el, "unit": UNIT, "cores": 1, "cpu_model": cpu_model(), "kind": "oracle",
                 "sample": "%d greedy passes over %d of the %d sequences of %s (L=%d) in %.1f s, one thread"
                           % (reps, nb, w.B, w.name, w.L, el),
                 "ms_per_step": 1e3 * el / reps * w.B / nb}
     if o.posterior(probs[0], w.committed[0])["empty"]:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+        return {"value": None, "unit": UNIT, "cores": 1, "cpu_model": cpu_model(), "kind": "oracle",
                 "sample": "none: the constrained distribution of %s at L=%d is empty" % (w.name, w.L)}
     while True:
         for b in range(nb):
@@ -283,9 +337,9 @@ def cpu_baseline(w, probs, seconds: float, greedy: bool = False):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": reps * nb * w.L / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d passes over %d of the %d sequences of %s (L=%d) in %.1f s, one thread"
-                      % (reps, nb, w.B, w.name, w.L, el),
+    return {"value": reps * nb * w.L / el, "unit": UNIT, "cores": 1, "cpu_model": cpu_model(), "kind": "oracle",
+            "sample": "%d passes over %d of the %d sequences of %s (L=%d) in %.1f s, one thread; a whole step "
+                      "of all %d sequences scales this by %d" % (reps, nb, w.B, w.name, w.L, el, w.B, w.B // nb),
             "ms_per_step": 1e3 * el / reps * w.B / nb}
 
 
@@ -327,42 +381,55 @@ def run_schedule(w, aut, stream, seed):
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the float64 oracle as it stands, single-threaded on a host core,
+    on the same workload.  One step is a bounded sample of the workload's step: the first
+    nb sequences of the batch (sample, posterior with the marginals of the sample, commit),
+    nb as large as keeps one step near 20 s (the other sequences are the same computation
+    on other rows); warm-up and timed steps are capped to a few minutes in all."""
     if rank != 0:
         return
     from constrained_decoding_diffusion_gb300 import synth
-    w = synth.workload(args.workload)
-    probs = w.probs()
     import oracle
+    w = synth.workload(args.workload)
     o = oracle.OracleFA(w.fa)
+    probs = w.probs(n_rows=1)
 
-    def one(seed):
-        for b in range(w.B):
+    def one(seed, nb):
+        for b in range(nb):
             x = o.sample(probs[b], w.committed[b], 1, seed=seed)[0]
             r = o.posterior(probs[b], w.committed[b], tokens=x)
             oracle.topk(r["marg_tokens"], w.committed[b], w.k, 0, w.window)
 
     t = time.perf_counter()
-    one(0)                       # the first warm-up step, timed to size the run
-    est = time.perf_counter() - t
+    one(0, 1)                    # the first warm-up step (one sequence), timed to size the run
+    est1 = time.perf_counter() - t
+    nb = max(1, min(w.B, int(20.0 / max(est1, 1e-6))))
+    if nb > 1:
+        probs = w.probs(n_rows=nb)
+    est = est1 * nb
     budget = 120.0
     warm = max(1, min(args.warmup, int(0.25 * budget / max(est, 1e-6))))
     for i in range(1, warm):
-        one(i)
+        one(i, nb)
     steps = max(1, min(args.steps, int(budget / max(est, 1e-6))))
     t0 = time.perf_counter()
     for i in range(steps):
-        one(i)
+        one(i, nb)
     el = time.perf_counter() - t0
     ms = 1e3 * el / steps
-    value = w.B * w.L / (el / steps)
+    value = nb * w.L / (el / steps)
+    sample = ("%d of the %d sequences of %s (L=%d) per step, %d timed steps after %d warm-up, one thread "
+              "(steps capped to a %.0f s budget; a whole step of the batch takes %d times as long)"
+              % (nb, w.B, w.name, w.L, steps, warm, budget, w.B // nb))
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": steps,
             "steps_requested": args.steps, "warmup": warm, "warmup_requested": args.warmup, "ms_per_step": ms,
+            "ms_per_batch_step": ms * w.B / nb,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "V": w.V, "k": w.k},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "%d full steps, one thread (step count capped to a %.0f s budget)"
-                                       % (steps, budget)},
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "S": w.S, "V": w.V, "k": w.k,
+                       "sequences_per_step": nb},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "cpu_model": cpu_model(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -375,6 +442,7 @@ def run_native(args, rank, world, local):
 
     torch.cuda.set_device(local)
     native.load()
+    clocks = ClockSampler(local).__enter__()   # sampling from here on; summarised over the timed steps
     w = synth.workload(args.workload)
     if args.length is not None:
         w.L = args.length
@@ -439,17 +507,19 @@ def run_native(args, rank, world, local):
 
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks.wait_first()
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    with ClockSampler(local) as clocks:
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                flush.zero_()
-                ev_s[i].record(stream)
-                run_one(i)
-                ev_e[i].record(stream)
-        torch.cuda.synchronize()
+    clocks.mark_start()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            ev_s[i].record(stream)
+            run_one(i)
+            ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
     barrier(world)
     wall = time.perf_counter() - t_wall
     step_ms = [s.elapsed_time(e) for s, e in zip(ev_s, ev_e)]
@@ -501,6 +571,8 @@ def run_native(args, rank, world, local):
     h2d = probs.numel() * 4 + committed.numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in outs)
 
+    clock_summary = clocks.summary()
+    clocks.__exit__(None, None, None)
     if rank != 0:
         return
     value = replica_value(w.B * w.L, world, ms_max)
@@ -527,7 +599,7 @@ def run_native(args, rank, world, local):
                        "method": args.method, "confidence": args.confidence,
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roof,
-            "reweight_gather": reweight_gather(w, masked, per_stage.get("reweight", 0.0), clocks.summary()),
+            "reweight_gather": reweight_gather(w, masked, per_stage.get("reweight", 0.0), clock_summary),
             "step_roofline": {"ms_at_roofline": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_max,
                               "bytes": tot_bytes, "span_flops": alg["upsweep"]["flops"]},
             "stage_ms": per_stage,
@@ -535,7 +607,7 @@ def run_native(args, rank, world, local):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
             "wall_s": wall, "row_status_ok": bool((status == 0).all()),
-            "clocks": clocks.summary()}
+            "clocks": clock_summary}
     if args.schedule and w.steps > 1:
         del graph
         line["schedule"] = run_schedule(w, aut, stream, seed)

@@ -10,14 +10,15 @@
 // (file scope, FA_NOALLOC_SCRATCH_BYTES bytes, 256-byte aligned).  Every GPU that loads the
 // library holds that array until the process exits.
 //
-// Set-up: the first call on each device, with that device current, looks up the array's
-// device address with cudaGetSymbolAddress (host code cannot use the array's name as a
-// device pointer) and keeps it; make that first call before any stream capture.  All calls
-// on a device share the one array, which keeps whatever the last call left in it: the step
+// Set-up: every call looks up the array's device address on the current device with
+// cudaGetSymbolAddress (host code cannot use the array's name as a device pointer).  The
+// first call on a device loads the library's device code there, so make it before any
+// stream capture.  Looking the address up each time (cheap once loaded) keeps it right
+// after a device reset, which reloads the module and may move the array.  All calls on a
+// device share the one array, which keeps whatever the last call left in it: the step
 // initialises every scratch word before reading it, so nothing needs clearing between
 // calls, but two calls whose work overlaps on the GPU (other streams, other host threads)
 // race on the array and must be serialised by the caller.
-#include <mutex>
 #include <string>
 
 #include "fa_internal.cuh"
@@ -26,29 +27,14 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRA
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kMaxDevices] = {nullptr};
-
 fa_status noalloc_scratch(void **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        fa_set_error("fa_constrained_step_noalloc: no usable current device");
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+        fa_set_error(std::string("fa_constrained_step_noalloc: cudaGetSymbolAddress failed: ") + cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            fa_set_error(std::string("fa_constrained_step_noalloc: cudaGetSymbolAddress failed: ") +
-                         cudaGetErrorString(e));
-            return FA_ERR_CUDA;
-        }
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    *out = p;
     return FA_OK;
 }
 
@@ -59,6 +45,12 @@ extern "C" fa_status fa_constrained_step_noalloc(const fa_automaton *aut, int32_
                                                  uint64_t philox_offset, int32_t k, int32_t commit_lo,
                                                  int32_t commit_hi, int32_t *tokens, double *logZ, float *marg,
                                                  int32_t *commit_idx, int32_t *row_status, fa_stream stream) {
+    // the step's own range checks, first, so an out-of-range B or k is reported as such and
+    // not as a scratch shortfall
+    if (B < 0 || B > 65535 || L < 0 || L > FA_MAX_LENGTH || k < 0) {
+        fa_set_error("fa_constrained_step_noalloc: B, L or k out of range");
+        return FA_ERR_INVALID_ARG;
+    }
     size_t need = 0;
     fa_status st = fa_step_workspace_bytes(aut, B, L, &need);
     if (st != FA_OK) return st;

@@ -26,8 +26,15 @@
 // from its own 32-lane quarter) and write the tile row-major with its row maxima.
 //
 // Every mbarrier wait is bounded (about a second); a wait that runs out records
-// FA_ROW_TIMEOUT in the error word, tensor memory is released and the CTA returns.
+// FA_ROW_TIMEOUT in the error word, tensor memory is released and the CTA returns.  The
+// pipeline waits also give up as soon as the other role has failed, while the waits that
+// drain work already issued (the producer's last bulk copies, the MMAs before the final
+// commit) keep the long limit: that work completes on its own, and no CTA may leave while a
+// copy can still land in its shared memory or an MMA still reads it.
 #include <stdint.h>
+
+#include <atomic>
+#include <cfloat>
 
 #include "fa_internal.cuh"
 
@@ -41,6 +48,7 @@ constexpr int NSTAGE = 4;                   // three stages in flight while one 
 constexpr uint32_t KGRP = TK * 32;          // bytes of one 8-row group (8 rows x TK x 4 B)
 constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 constexpr long long kSpinCycles = 2000000000LL;
+constexpr long long kInjectCycles = 1LL << 20;   // the injected wait of a failure test (~0.5 ms)
 constexpr int A_IMG = 2 * A_BYTES;          // hi + lo image of one 128x16 left tile
 constexpr int PREP_KT = 256 / TK;           // K steps converted per k_tc_prep block (256 columns)
 constexpr int B_IMG = 2 * B_BYTES;          // hi + lo image of one 256x16 right tile
@@ -77,11 +85,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// bounded wait (about a second of SM clock); false when the limit ran out
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// bounded wait (about a second of SM clock by default); false when the limit ran out or,
+// given abort, when another thread of the CTA has flagged a failure
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit = kSpinCycles,
+                                          const volatile int *abort = nullptr) {
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kSpinCycles) return false;
+    while (!mbar_try_wait(bar, parity)) {
+        if (abort && *abort) return false;
+        if (clock64() - t0 > limit) return false;
+    }
     return true;
 }
 
@@ -145,8 +157,10 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
 // operand (256-column tiles, transposed to K-major).
 __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                 const int32_t *__restrict__ rho_c,
-                                                const int32_t *__restrict__ rmax_c, int nc,
-                                                const int32_t *__restrict__ mu, unsigned char *img) {
+                                                const int32_t *__restrict__ rmax_c,
+                                                const int32_t *__restrict__ rminc_c, int nc,
+                                                const int32_t *__restrict__ mu, unsigned char *img,
+                                                int32_t *range_lost) {
     const int tid = threadIdx.x;
     const int tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN, nkt = (S + TK - 1) / TK;
     const int per = tiles_m + tiles_n;
@@ -166,9 +180,10 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
     if (w < tiles_m) {
         const int tm = w, row = tid >> 1, gi = tm * TM + row;
         const float *A = mant_c + lnode * SS;
-        const int32_t *rhoR = rho_c + rnode * S, *rmaxR = rmax_c + rnode * S;
+        const int32_t *rhoR = rho_c + rnode * S, *rmaxR = rmax_c + rnode * S, *rmincR = rminc_c + rnode * S;
         const int mrow = gi < S ? mu[pnode * S + gi] : FA_INT_NONE;
         unsigned char *base = img + (size_t)bn * per_prod_a + (size_t)tm * nkt * A_IMG;
+        int lost = 0;
         for (int kt = kt0; kt < kt1; ++kt) {
             unsigned char *t = base + (size_t)kt * A_IMG;
 #pragma unroll
@@ -181,8 +196,15 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
                 for (int e = 0; e < 4; ++e) {
                     const int m = m0 + e;
                     float y = 0.0f;
-                    if (x[e] > 0.0f && mrow != FA_INT_NONE && m < S && __ldg(rmaxR + m) > 0)
-                        y = fa_mul_pow2(x[e], __ldg(rhoR + m) - mrow);
+                    if (x[e] > 0.0f && mrow != FA_INT_NONE && m < S && __ldg(rmaxR + m) > 0) {
+                        const int d = __ldg(rhoR + m) - mrow;
+                        // below the normal range after the prescale, alone or times the right
+                        // row's smallest entry: mass may be lost
+                        const int rn = __ldg(rmincR + m);
+                        const int emin = rn > 0 ? min(0, fa_exponent(__int_as_float(0x7fffffff - rn))) : 0;
+                        if (fa_exponent(x[e]) + d + emin < -126) lost = 1;
+                        y = fa_mul_pow2(x[e], d);
+                    }
                     split_tf32(y, hi[e], lo[e]);
                 }
                 const uint32_t off = kmaj_off(row, kk);
@@ -190,6 +212,7 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
                 *reinterpret_cast<float4 *>(t + A_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
+        if (__any_sync(0xffffffffu, lost) && (tid & 31) == 0) atomicOr(range_lost + b, 1);
     } else {
         const int tn = w - tiles_m, n = tid, gj = tn * TN + n;
         const float *Bm = mant_c + rnode * SS;
@@ -215,11 +238,13 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
 
 __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                     const int32_t *__restrict__ rho_c,
-                                                    const int32_t *__restrict__ rmax_c, int nc,
+                                                    const int32_t *__restrict__ rmax_c,
+                                                    const int32_t *__restrict__ rminc_c, int nc,
                                                     const int32_t *__restrict__ mu, const unsigned char *__restrict__ img,
-                                                    float *mant_p, int32_t *rho_p, int32_t *rmax_p, int32_t *err) {
+                                                    float *mant_p, int32_t *rho_p, int32_t *rmax_p, int32_t *rminc_p,
+                                                    int32_t *err, int inject_timeout) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ uint64_t full[NSTAGE], empty[NSTAGE], done;
+    __shared__ uint64_t full[NSTAGE], empty[NSTAGE], done, never;
     __shared__ uint32_t tmem_base_s;
     __shared__ int fail_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -243,6 +268,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
             for (int r = i0 + tid; r < min(i0 + TM, S); r += NTHR) {
                 rho_p[pnode * S + r] = rho_c[lnode * S + r];
                 rmax_p[pnode * S + r] = rmax_c[lnode * S + r];
+                rminc_p[pnode * S + r] = rminc_c[lnode * S + r];
             }
         return;
     }
@@ -253,6 +279,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
     if (tid == 0) {
         for (int s2 = 0; s2 < NSTAGE; ++s2) { mbar_init(&full[s2], 1); mbar_init(&empty[s2], 1); }
         mbar_init(&done, 1);
+        mbar_init(&never, 1);   // nothing ever arrives here: the target of an injected wait
         fail_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -271,25 +298,28 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
         int issued = 0;
         for (int kt = 0; kt < nkt; ++kt) {
             const int st = kt % NSTAGE;
-            if (kt >= NSTAGE && !mbar_wait(&empty[st], ((kt / NSTAGE) - 1) & 1)) { atomicExch(&fail_s, 1); break; }
+            if (kt >= NSTAGE && !mbar_wait(&empty[st], ((kt / NSTAGE) - 1) & 1, kSpinCycles, &fail_s)) {
+                atomicExch(&fail_s, 1);
+                break;
+            }
             unsigned char *stage = smem + st * STAGE_BYTES;
             mbar_expect_tx(&full[st], STAGE_BYTES);
             bulk_g2s(stage, a_img + (size_t)kt * A_IMG, A_IMG, &full[st]);
             bulk_g2s(stage + A_IMG, b_img + (size_t)kt * B_IMG, B_IMG, &full[st]);
             issued = kt + 1;
         }
-        if (fail_s) {
-            // copies still in flight land in this CTA's stages: wait (bounded) for the last
-            // phase issued on each stage before the CTA may leave
-            for (int kt = max(0, issued - NSTAGE); kt < issued; ++kt) (void)mbar_wait(&full[kt % NSTAGE], (kt / NSTAGE) & 1);
-        }
+        // the last phase issued on each stage has landed before the CTA may leave (already
+        // true unless a wait failed; the copies complete on their own, so the long limit)
+        for (int kt = max(0, issued - NSTAGE); kt < issued; ++kt) (void)mbar_wait(&full[kt % NSTAGE], (kt / NSTAGE) & 1);
     } else if (tid == 32) {
         // MMA issuer
         const uint32_t idesc = umma_idesc_tf32();
+        // failure test: a short wait on a barrier nothing completes runs out
+        if (inject_timeout && !mbar_wait(&never, 0, kInjectCycles)) atomicExch(&fail_s, 1);
         int kt = 0;
-        for (; kt < nkt; ++kt) {
+        for (; kt < nkt && !fail_s; ++kt) {
             const int st = kt % NSTAGE;
-            if (!mbar_wait(&full[st], (kt / NSTAGE) & 1)) { atomicExch(&fail_s, 1); break; }
+            if (!mbar_wait(&full[st], (kt / NSTAGE) & 1, kSpinCycles, &fail_s)) { atomicExch(&fail_s, 1); break; }
             tc_fence_after();
             const uint32_t a_hi = smem_u32(smem + st * STAGE_BYTES), a_lo = a_hi + A_BYTES;
             const uint32_t b_hi = a_hi + A_IMG, b_lo = b_hi + B_BYTES;
@@ -306,14 +336,15 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
         }
         umma_commit(&done);
     }
-    // everyone: wait for the last MMAs, then read the accumulators
+    // everyone: wait for the last MMAs (issued ones complete on their own: the long limit),
+    // then read the accumulators
     if (!mbar_wait(&done, 0)) atomicExch(&fail_s, 1);
     tc_fence_after();
     __syncthreads();
     if (!fail_s) {
         const int q = warp & 3, half = warp >> 2;
         const int row = 32 * q + lane, gi = i0 + row;
-        float mx = 0.0f;
+        float mx = 0.0f, mn = FLT_MAX;
 #pragma unroll 1
         for (int cch = 0; cch < 4; ++cch) {
             const int col = 128 * half + 32 * cch;
@@ -332,15 +363,25 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4 *>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, v[e]);
+                    for (int e = 0; e < 32; ++e) {
+                        mx = fmaxf(mx, v[e]);
+                        if (v[e] > 0.0f) mn = fminf(mn, v[e]);
+                    }
                 } else {
                     for (int e = 0; e < 32; ++e)
-                        if (j0 + col + e < S) { dst[e] = v[e]; mx = fmaxf(mx, v[e]); }
+                        if (j0 + col + e < S) {
+                            dst[e] = v[e];
+                            mx = fmaxf(mx, v[e]);
+                            if (v[e] > 0.0f) mn = fminf(mn, v[e]);
+                        }
                 }
             }
         }
         if (gi < S) {
-            if (mx > 0.0f) atomicMax(&rmax_p[pnode * S + gi], __float_as_int(mx));
+            if (mx > 0.0f) {
+                atomicMax(&rmax_p[pnode * S + gi], __float_as_int(mx));
+                atomicMax(&rminc_p[pnode * S + gi], 0x7fffffff - __float_as_int(mn));
+            }
             if (tn == 0 && half == 0) {
                 const int mr = mu[pnode * S + gi];
                 rho_p[pnode * S + gi] = (mr == FA_INT_NONE) ? 0 : rho_c[lnode * S + gi] + mr;
@@ -361,6 +402,15 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
 
 size_t fa_span_tc_smem(int S) { (void)S; return (size_t)NSTAGE * STAGE_BYTES; }
 
+// Launches of k_span_tc still to take the injected wait (failure tests only).
+static std::atomic<int> g_inject_timeouts{0};
+
+extern "C" fa_status fa_debug_inject_wait_timeouts(int32_t n_launches) {
+    if (n_launches < 0) { fa_set_error("fa_debug_inject_wait_timeouts: negative count"); return FA_ERR_INVALID_ARG; }
+    g_inject_timeouts.store(n_launches);
+    return FA_OK;
+}
+
 bool fa_span_tc_supported(int S) { return S >= 128 && (S % 4) == 0; }
 
 size_t fa_span_tc_image_bytes(int S, long products) {
@@ -369,20 +419,25 @@ size_t fa_span_tc_image_bytes(int S, long products) {
 }
 
 fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant_c, const int32_t *rho_c,
-                           const int32_t *rmax_c, int nc, const int32_t *mu, float *mant_p, int32_t *rho_p,
-                           int32_t *rmax_p, int32_t *err, void *img, cudaStream_t stream) {
+                           const int32_t *rmax_c, const int32_t *rminc_c, int nc, const int32_t *mu, float *mant_p,
+                           int32_t *rho_p, int32_t *rmax_p, int32_t *rminc_p, int32_t *err, int32_t *range_lost,
+                           void *img, cudaStream_t stream) {
     const size_t smem = fa_span_tc_smem(S);
     cudaError_t e = cudaFuncSetAttribute(k_span_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     const long tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN;
     const long kch = ((S + TK - 1) / TK + PREP_KT - 1) / PREP_KT;
-    k_tc_prep<<<(unsigned)((long)B * nk * (tiles_m + tiles_n) * kch), NTHR, 0, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, nc,
-                                                                                  mu, (unsigned char *)img);
+    k_tc_prep<<<(unsigned)((long)B * nk * (tiles_m + tiles_n) * kch), NTHR, 0, stream>>>(
+        S, L, k, nk, mant_c, rho_c, rmax_c, rminc_c, nc, mu, (unsigned char *)img, range_lost);
     e = cudaGetLastError();
     if (e != cudaSuccess) { fa_set_error(std::string("operand images (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     const long grid = (long)B * nk * tiles_m * tiles_n;
-    k_span_tc<<<(unsigned)grid, NTHR, smem, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, nc, mu,
-                                                      (const unsigned char *)img, mant_p, rho_p, rmax_p, err);
+    int inject = 0;
+    for (int n = g_inject_timeouts.load(); n > 0 && !inject;)
+        if (g_inject_timeouts.compare_exchange_weak(n, n - 1)) inject = 1;
+    k_span_tc<<<(unsigned)grid, NTHR, smem, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, rminc_c, nc, mu,
+                                                      (const unsigned char *)img, mant_p, rho_p, rmax_p, rminc_p, err,
+                                                      inject);
     e = cudaGetLastError();
     if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     return FA_OK;

@@ -6,7 +6,9 @@
 //
 // Span number format.  A span matrix A[l, r) = M_{l+1} ... M_r is stored as an fp32
 // mantissa matrix Ã and one power-of-two exponent per row: A[i, j] = Ã[i, j] * 2^rho[i].
-// rmax[i] holds the bit pattern of max_j Ã[i, j] (0 for an all-zero row).  Products of
+// rmax[i] holds the bit pattern of max_j Ã[i, j] (0 for an all-zero row) and rminc[i] the
+// complement 0x7fffffff - bits of the smallest nonzero Ã[i, j] (0 for an all-zero row), so
+// both accumulate with atomicMax from zero.  Products of
 // hundreds of probabilities leave the fp32 range long before a sequence ends, and rows of one
 // span differ by far more than 2^254 once committed tokens pin the path, so a single
 // exponent per matrix would flush whole rows; per-row exponents keep every row at full
@@ -30,10 +32,10 @@ constexpr int kWarps = kThreads / 32;
 struct Plan {
     int B = 0, L = 0, S = 0, V = 0, K = 0, Lp = 1;
     int nk[18] = {0};
-    size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, mu[18] = {0};
+    size_t mant[18] = {0}, rho[18] = {0}, rmax[18] = {0}, rminc[18] = {0}, mu[18] = {0};
     size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, conf = 0, den_m = 0, den_e = 0, tm_part = 0, zsum = 0, zexp = 0;
     int tm_chunks = 1, tm_chunk = kTmChunkMax;
-    size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0, img = 0;
+    size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0, range_lost = 0, img = 0;
     size_t total = 0;
 };
 
@@ -54,18 +56,22 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
         p.rho[k] = take(nodes * S * sizeof(int32_t));
         p.mu[k] = take(k ? nodes * S * sizeof(int32_t) : 0);
     }
-    // row maxima: level 0, then levels 1..K back to back (cleared together by the reweight)
+    // row maxima and complemented row minima: level 0 (written whole by the reweight), then
+    // levels 1..K back to back with the step's counters and flags (cleared together by the
+    // reweight; the products accumulate into them with atomicMax)
     p.rmax[0] = take((size_t)B * p.nk[0] * S * sizeof(int32_t));
-    size_t hi = 0;
-    for (int k = 1; k <= p.K; ++k) hi += (size_t)B * p.nk[k] * S * sizeof(int32_t);
+    p.rminc[0] = take((size_t)B * p.nk[0] * S * sizeof(int32_t));
     p.rmax_hi = off;
-    p.rmax_hi_bytes = hi;
     {
         size_t o = p.rmax_hi;
         for (int k = 1; k <= p.K; ++k) { p.rmax[k] = o; o += (size_t)B * p.nk[k] * S * sizeof(int32_t); }
-        p.tc_err = p.rmax_hi + hi;             // timeout word of the tensor-core span products
+        for (int k = 1; k <= p.K; ++k) { p.rminc[k] = o; o += (size_t)B * p.nk[k] * S * sizeof(int32_t); }
+        p.tc_err = o;                          // timeout word of the tensor-core span products
         p.leaf_done = p.tc_err + sizeof(int32_t);  // per-sequence ticket counters of the leaf blocks
-        p.rmax_hi_bytes = hi + (1 + (size_t)B) * sizeof(int32_t);
+        // per-sequence range-loss flags: set when a span product may push nonzero mass below
+        // the fp32 normal range
+        p.range_lost = p.leaf_done + (size_t)B * sizeof(int32_t);
+        p.rmax_hi_bytes = (p.range_lost - p.rmax_hi) + (size_t)B * sizeof(int32_t);
         off = align256(p.rmax_hi + p.rmax_hi_bytes);
     }
     size_t bnd = (size_t)B * (size_t)(L + 1);
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
                                                                 const int32_t *__restrict__ committed,
                                                                 const int4 *__restrict__ rbm, int nrb, int tot_floats,
                                                                     float *mant, int32_t *rho, int32_t *rmax,
-                                                                    int32_t *zero, long n_zero) {
+                                                                    int32_t *rminc, int32_t *zero, long n_zero) {
     extern __shared__ float smem_f[];
     const int nthr = blockDim.x;
     // clear the row maxima of the higher tree levels (their products accumulate with atomicMax)
@@ -195,8 +201,9 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
     }
     const int S = fa.S, CH = fa.chunk_tokens, nch = fa.n_chunks;
     // shared memory: [0, tot_floats) holds the staged chunk ([CH] = 0) while the chunks are
-    // walked, then every unit's run totals (FA_UNIT_SLOTS per unit) followed by the row maxima;
-    // after it, one slot array per warp for the run sums of the chunk being walked
+    // walked, then every unit's run totals (FA_UNIT_SLOTS per unit) followed by the row maxima
+    // and the complemented row minima; after it, one slot array per warp for the run sums of
+    // the chunk being walked
     float *utot = smem_f;
     float *slots = smem_f + tot_floats;                    // [FA_RW_WARPS * FA_UNIT_SLOTS]
     const int t = blockIdx.x / nrb, r = blockIdx.x % nrb, b = blockIdx.y;
@@ -206,6 +213,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
     const int c = committed[pos];
     const int r0 = m0.x, r1 = m0.y, u0 = m0.z, nu = m0.w - m0.z, c0 = m1.x, c1 = m1.y;
     int *smax = (int *)(utot + nu * FA_UNIT_SLOTS);        // [rows] row maxima (bits), once the chunks are done
+    int *smin = smax + (r1 - r0);                          // [rows] complemented row minima
     float *M = mant + pos * (size_t)S * S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // a masked position writes every cell of its rows: the rest of the rows is cleared, all
@@ -316,7 +324,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
                 for (int q = 0; q < FA_RUN_SLOTS; ++q) utot[uw * FA_UNIT_SLOTS + q * 32 + lane] = tot[h][q];
             }
         }
-        for (int i = tid; i < r1 - r0; i += nthr) smax[i] = 0;
+        for (int i = tid; i < r1 - r0; i += nthr) { smax[i] = 0; smin[i] = 0; }
         __syncthreads();
         for (int cell = c0 + tid; cell < c1; cell += nthr) {
             const int s = fa.cell_src[cell];
@@ -330,10 +338,14 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
             const unsigned act = __activemask();
             const unsigned same = __match_any_sync(act, s);
             const int rowmax = (int)__reduce_max_sync(same, (unsigned)__float_as_int(v));
-            if ((threadIdx.x & 31) == __ffs(same) - 1) atomicMax(&smax[s - r0], rowmax);
+            const int rowminc = (int)__reduce_max_sync(same, v > 0.0f ? 0x7fffffffu - (unsigned)__float_as_int(v) : 0u);
+            if ((threadIdx.x & 31) == __ffs(same) - 1) {
+                atomicMax(&smax[s - r0], rowmax);
+                atomicMax(&smin[s - r0], rowminc);
+            }
         }
     } else {
-        for (int i = tid; i < r1 - r0; i += nthr) smax[i] = 0;
+        for (int i = tid; i < r1 - r0; i += nthr) { smax[i] = 0; smin[i] = 0; }
         __syncthreads();
         if (c < fa.V) {
             const int64_t a0 = fa.tok_off[c], a1 = fa.tok_off[c + 1];
@@ -349,7 +361,11 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
             for (int64_t j = a0 + tid; j < a1; j += nthr) {
                 const int e = fa.tok_edges[j];
                 const int s = fa.edge_src[e];
-                if (s >= r0 && s < r1) atomicMax(&smax[s - r0], __float_as_int(M[(size_t)s * S + fa.edge_dst[e]]));
+                if (s >= r0 && s < r1) {
+                    const int bits = __float_as_int(M[(size_t)s * S + fa.edge_dst[e]]);  // an edge count >= 1
+                    atomicMax(&smax[s - r0], bits);
+                    atomicMax(&smin[s - r0], 0x7fffffff - bits);
+                }
             }
         }
     }
@@ -357,6 +373,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
     for (int i = tid; i < r1 - r0; i += nthr) {
         rho[pos * S + r0 + i] = 0;
         if (rmax) rmax[pos * S + r0 + i] = smax[i];
+        if (rminc) rminc[pos * S + r0 + i] = smin[i];
     }
 }
 
@@ -404,13 +421,15 @@ constexpr int ST = 32;
 template <bool MAX>
 __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                        const int32_t *__restrict__ rho_c,
-                                                       const int32_t *__restrict__ rmax_c, int nc, float *mant_p,
-                                                       int32_t *rho_p, int32_t *rmax_p) {
+                                                       const int32_t *__restrict__ rmax_c,
+                                                       const int32_t *__restrict__ rminc_c, int nc, float *mant_p,
+                                                       int32_t *rho_p, int32_t *rmax_p, int32_t *rminc_p,
+                                                       int32_t *range_lost) {
     // the A tile is stored transposed (At[m][row]) and both tiles padded to 16-byte rows, so
     // the inner loop reads two float2 per step
     __shared__ __align__(16) float At[SMALL_S][ST + 4];
     __shared__ __align__(16) float Bs[SMALL_S][ST + 4];
-    __shared__ int rhoR_s[SMALL_S], rmaxR_s[SMALL_S], mu_s[ST];
+    __shared__ int rhoR_s[SMALL_S], rmaxR_s[SMALL_S], eminR_s[SMALL_S], mu_s[ST];
     const int tpd = (S + ST - 1) / ST;
     const int tile = blockIdx.x % (tpd * tpd);
     const long bn = blockIdx.x / (tpd * tpd);
@@ -431,6 +450,7 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
             for (int r = i0 + tid; r < min(i0 + ST, S); r += kThreads) {
                 rho_p[pnode * S + r] = rho_c[lnode * S + r];
                 rmax_p[pnode * S + r] = rmax_c[lnode * S + r];
+                rminc_p[pnode * S + r] = rminc_c[lnode * S + r];
             }
         return;
     }
@@ -439,7 +459,7 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
         // all loads of this thread in flight before any shared-memory store
         constexpr int U = ST * SMALL_S / kThreads;  // 8
         float va[U], vb[U];
-        int ra = 0, rr = 0;
+        int ra = 0, rr = 0, rn = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int q = tid + u * kThreads;
@@ -451,6 +471,7 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
         if (tid < SMALL_S) {
             ra = tid < S ? rho_c[rnode * S + tid] : 0;
             rr = tid < S ? rmax_c[rnode * S + tid] : 0;
+            rn = tid < S ? rminc_c[rnode * S + tid] : 0;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -458,7 +479,12 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
             At[q % SMALL_S][q / SMALL_S] = va[u];
             Bs[q / ST][q % ST] = vb[u];
         }
-        if (tid < SMALL_S) { rhoR_s[tid] = ra; rmaxR_s[tid] = rr; }
+        if (tid < SMALL_S) {
+            rhoR_s[tid] = ra;
+            rmaxR_s[tid] = rr;
+            // exponent of the right row's smallest nonzero entry, capped at 0
+            eminR_s[tid] = rn > 0 ? min(0, fa_exponent(__int_as_float(0x7fffffff - rn))) : 0;
+        }
     }
     __syncthreads();
     {
@@ -476,13 +502,18 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
         if (seg == 0) mu_s[r] = best;
     }
     __syncthreads();
+    int lost = 0;
     for (int q = tid; q < ST * SMALL_S; q += kThreads) {
         const int m = q / ST, r = q % ST;
         const float x = At[m][r];
         const int mr = mu_s[r];
-        At[m][r] = (x > 0.0f && mr != FA_INT_NONE && m < S && rmaxR_s[m] > 0) ? fa_mul_pow2(x, rhoR_s[m] - mr) : 0.0f;
+        const bool live = x > 0.0f && mr != FA_INT_NONE && m < S && rmaxR_s[m] > 0;
+        // a nonzero entry prescaled below the normal range, or whose product with the right
+        // row's smallest entry would be, may lose its mass
+        if (live && fa_exponent(x) + rhoR_s[m] - mr + eminR_s[m] < -126) lost = 1;
+        At[m][r] = live ? fa_mul_pow2(x, rhoR_s[m] - mr) : 0.0f;
     }
-    __syncthreads();
+    if (__syncthreads_or(lost) && tid == 0) atomicOr(range_lost + b, 1);
     const int tx = tid & 15, ty = tid >> 4;          // 2x2 outputs per thread
     float c00 = 0.0f, c01 = 0.0f, c10 = 0.0f, c11 = 0.0f;
     auto step = [&](int m) {
@@ -506,19 +537,26 @@ __global__ void __launch_bounds__(kThreads) k_span_small(int S, int L, int k, in
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
         const int i = i0 + 2 * ty + p;
-        float mx = 0.0f;
+        float mx = 0.0f, mn = FLT_MAX;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int j = j0 + 2 * tx + q;
             if (i < S && j < S) {
                 C[(size_t)i * S + j] = cv[p][q];
                 mx = fmaxf(mx, cv[p][q]);
+                if (cv[p][q] > 0.0f) mn = fminf(mn, cv[p][q]);
             }
         }
 #pragma unroll
-        for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int o = 8; o; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
         if (tx == 0 && i < S) {
-            if (mx > 0.0f) atomicMax(&rmax_p[pnode * S + i], __float_as_int(mx));
+            if (mx > 0.0f) {
+                atomicMax(&rmax_p[pnode * S + i], __float_as_int(mx));
+                atomicMax(&rminc_p[pnode * S + i], 0x7fffffff - __float_as_int(mn));
+            }
             if (j0 == 0) {
                 const int mr = mu_s[2 * ty + p];
                 rho_p[pnode * S + i] = (mr == FA_INT_NONE) ? 0 : rho_c[lnode * S + i] + mr;
@@ -534,9 +572,10 @@ constexpr int GBM = 64, GBN = 64, GBK = 16;
 template <bool MAX>
 __global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                       const int32_t *__restrict__ rho_c,
-                                                      const int32_t *__restrict__ rmax_c, int nc,
+                                                      const int32_t *__restrict__ rmax_c,
+                                                      const int32_t *__restrict__ rminc_c, int nc,
                                                       const int32_t *__restrict__ mu, float *mant_p, int32_t *rho_p,
-                                                      int32_t *rmax_p) {
+                                                      int32_t *rmax_p, int32_t *rminc_p, int32_t *range_lost) {
     __shared__ float As[GBK][GBM + 4];
     __shared__ float Bs[GBK][GBN + 4];
     __shared__ int mu_s[GBM];
@@ -562,16 +601,19 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int
                 if (i0 + r < S) {
                     rho_p[pnode * S + i0 + r] = rho_c[lnode * S + i0 + r];
                     rmax_p[pnode * S + i0 + r] = rmax_c[lnode * S + i0 + r];
+                    rminc_p[pnode * S + i0 + r] = rminc_c[lnode * S + i0 + r];
                 }
         return;
     }
     const float *Bm = mant_c + rnode * (size_t)S * S;
     const int32_t *rhoR = rho_c + rnode * S;
     const int32_t *rmaxR = rmax_c + rnode * S;
+    const int32_t *rmincR = rminc_c + rnode * S;
     for (int r = tid; r < GBM; r += kThreads) mu_s[r] = (i0 + r < S) ? mu[pnode * S + i0 + r] : FA_INT_NONE;
     __syncthreads();
     const int tx = tid & 15, ty = tid >> 4;
     float acc[4][4] = {};
+    int lost = 0;
     for (int k0 = 0; k0 < S; k0 += GBK) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -582,7 +624,14 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int
             if (i < S && m < S) {
                 const float x = A[(size_t)i * S + m];
                 const int mr = mu_s[r];
-                if (x > 0.0f && mr != FA_INT_NONE && rmaxR[m] > 0) v = fa_mul_pow2(x, rhoR[m] - mr);
+                if (x > 0.0f && mr != FA_INT_NONE && rmaxR[m] > 0) {
+                    // below the normal range after the prescale, alone or times the right
+                    // row's smallest entry: mass may be lost
+                    const int rn = rmincR[m];
+                    const int emin = rn > 0 ? min(0, fa_exponent(__int_as_float(0x7fffffff - rn))) : 0;
+                    if (fa_exponent(x) + rhoR[m] - mr + emin < -126) lost = 1;
+                    v = fa_mul_pow2(x, rhoR[m] - mr);
+                }
             }
             As[kk][r] = v;
         }
@@ -609,22 +658,30 @@ __global__ void __launch_bounds__(kThreads) k_gemm_simt(int S, int L, int k, int
         }
         __syncthreads();
     }
+    if (__syncthreads_or(lost) && tid == 0) atomicOr(range_lost + b, 1);
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         const int i = i0 + ty * 4 + p;
-        float mx = 0.0f;
+        float mx = 0.0f, mn = FLT_MAX;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int j = j0 + tx * 4 + q;
             if (i < S && j < S) {
                 C[(size_t)i * S + j] = acc[p][q];
                 mx = fmaxf(mx, acc[p][q]);
+                if (acc[p][q] > 0.0f) mn = fminf(mn, acc[p][q]);
             }
         }
 #pragma unroll
-        for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int o = 8; o; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
         if (tx == 0 && i < S) {
-            if (mx > 0.0f) atomicMax(&rmax_p[pnode * S + i], __float_as_int(mx));
+            if (mx > 0.0f) {
+                atomicMax(&rmax_p[pnode * S + i], __float_as_int(mx));
+                atomicMax(&rminc_p[pnode * S + i], 0x7fffffff - __float_as_int(mn));
+            }
             if (tj == 0) {
                 const int mr = mu_s[ty * 4 + p];
                 rho_p[pnode * S + i] = (mr == FA_INT_NONE) ? 0 : rho_c[lnode * S + i] + mr;
@@ -642,7 +699,8 @@ __global__ void __launch_bounds__(kThreads) k_root(DevFA fa, int L, int K, int n
                                                  const int32_t *__restrict__ rho_root, uint64_t seed, uint64_t offset,
                                                  int32_t *z, float *am, int32_t *ae, float *bm, int32_t *be,
                                                  float *zsum_ws, int32_t *zexp_ws, double *logZ, int32_t *status,
-                                                 const int32_t *__restrict__ tc_err) {
+                                                 const int32_t *__restrict__ tc_err,
+                                                 const int32_t *__restrict__ range_lost) {
     const int b = blockIdx.x, S = fa.S, s0 = fa.start;
     const float *row = mant_root + (size_t)b * nK * S * S + (size_t)s0 * S;
     const size_t bnd0 = (size_t)b * (L + 1);
@@ -663,6 +721,14 @@ __global__ void __launch_bounds__(kThreads) k_root(DevFA fa, int L, int K, int n
         if (tc_err && *tc_err) {
             status[b] = FA_ROW_TIMEOUT;
             logZ[b] = -INFINITY;
+            z[bnd0 + L] = s0;
+            zsum_ws[b] = 0.0f;
+            zexp_ws[b] = 0;
+        } else if (range_lost && range_lost[b]) {
+            // the up-sweep dropped nonzero mass below the fp32 range: Z and every draw from
+            // these spans may be wrong, so none is reported
+            status[b] = FA_ROW_UNDERFLOW;
+            logZ[b] = NAN;
             z[bnd0 + L] = s0;
             zsum_ws[b] = 0.0f;
             zexp_ws[b] = 0;
@@ -1469,7 +1535,7 @@ __device__ int warp_argmax(int n, WF w, float *best) {
 
 __global__ void __launch_bounds__(32) k_map_root(DevFA fa, int L, int nK, const float *__restrict__ mant_root,
                                                  const int32_t *__restrict__ rho_root, int32_t *z, double *score,
-                                                 int32_t *status) {
+                                                 int32_t *status, const int32_t *__restrict__ range_lost) {
     const int b = blockIdx.x, S = fa.S, s0 = fa.start;
     const float *row = mant_root + (size_t)b * nK * S * S + (size_t)s0 * S;
     float best;
@@ -1477,7 +1543,11 @@ __global__ void __launch_bounds__(32) k_map_root(DevFA fa, int L, int nK, const 
     if (threadIdx.x == 0) {
         const size_t bnd0 = (size_t)b * (L + 1);
         z[bnd0] = s0;
-        if (pick < 0) {
+        if (range_lost[b]) {            // a max-product lost a candidate below the fp32 range
+            status[b] = FA_ROW_UNDERFLOW;
+            score[b] = NAN;
+            z[bnd0 + L] = s0;
+        } else if (pick < 0) {
             status[b] = FA_ROW_EMPTY;
             score[b] = -INFINITY;
             z[bnd0 + L] = s0;
@@ -1699,22 +1769,22 @@ fa_status check_device(const fa_automaton *a, const char *fn) {
 }
 
 fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *probs, const int32_t *committed,
-                          float *mant, int32_t *rho, int32_t *rmax, cudaStream_t st, int32_t *zero = nullptr,
-                          long n_zero = 0, bool use_max = false) {
+                          float *mant, int32_t *rho, int32_t *rmax, int32_t *rminc, cudaStream_t st,
+                          int32_t *zero = nullptr, long n_zero = 0, bool use_max = false) {
     const int p = pick_partition(a, (long)B * L);
     const int nrb = a->part_count[p];
     const int4 *rbm = reinterpret_cast<const int4 *>(a->rb_meta) + 2 * a->part_first[p];
     const int max_units = a->part_max_units[p];
     const int threads = std::min(32 * FA_RW_WARPS, std::max(256, 32 * max_units));
-    // the staged chunk, whose space takes the units' run totals and the row maxima at the
-    // end, then one run-slot array per warp
+    // the staged chunk, whose space takes the units' run totals and the row maxima and minima
+    // at the end, then one run-slot array per warp
     const int tot_floats = (int)std::max((size_t)((a->chunk_tokens + 4) & ~3),
-                                         (size_t)max_units * FA_UNIT_SLOTS + (size_t)a->part_max_rows[p]);
+                                         (size_t)max_units * FA_UNIT_SLOTS + 2 * (size_t)a->part_max_rows[p]);
     const size_t smem = sizeof(float) * ((size_t)tot_floats + (size_t)(threads / 32) * FA_UNIT_SLOTS);
     // units per warp: the register totals of a third unit cost the smaller layouts ~10%
     const int upw = (max_units + FA_RW_WARPS - 1) / FA_RW_WARPS;
     using K = void (*)(DevFA, int, const float *, const int32_t *, const int4 *, int, int, float *, int32_t *, int32_t *,
-                       int32_t *, long);
+                       int32_t *, int32_t *, long);
     K kern = upw <= 1 ? (use_max ? (K)k_reweight<true, 1> : (K)k_reweight<false, 1>)
              : upw == 2 ? (use_max ? (K)k_reweight<true, 2> : (K)k_reweight<false, 2>)
                         : (use_max ? (K)k_reweight<true, 3> : (K)k_reweight<false, 3>);
@@ -1723,7 +1793,8 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
         if (e != cudaSuccess) { fa_set_error(std::string("reweight smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     }
     dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
-    kern<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, tot_floats, mant, rho, rmax, zero, n_zero);
+    kern<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, tot_floats, mant, rho, rmax, rminc,
+                                      zero, n_zero);
     return launch_check("reweight");
 }
 
@@ -1804,16 +1875,16 @@ extern "C" fa_status fa_map_step(const fa_automaton *aut, int32_t B, int32_t L, 
     auto I = [&](size_t off) { return (int32_t *)(ws + off); };
     const int S = aut->S;
     stage_mark(0, s);
-    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), s, I(p.rmax_hi),
-                         (long)(p.rmax_hi_bytes / sizeof(int32_t)), true);
+    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), I(p.rminc[0]), s,
+                         I(p.rmax_hi), (long)(p.rmax_hi_bytes / sizeof(int32_t)), true);
     if (st != FA_OK) return st;
     stage_mark(1, s);
     for (int kk = 1; kk <= p.K; ++kk) {
         if (S <= SMALL_S) {
             const long tpd = (S + ST - 1) / ST;
             k_span_small<true><<<(unsigned)((long)B * p.nk[kk] * tpd * tpd), kThreads, 0, s>>>(
-                S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), p.nk[kk - 1], F(p.mant[kk]),
-                I(p.rho[kk]), I(p.rmax[kk]));
+                S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), I(p.rminc[kk - 1]),
+                p.nk[kk - 1], F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]), I(p.rminc[kk]), I(p.range_lost));
             if ((st = launch_check("span product (small, max)")) != FA_OK) return st;
             continue;
         }
@@ -1823,12 +1894,13 @@ extern "C" fa_status fa_map_step(const fa_automaton *aut, int32_t B, int32_t L, 
         if ((st = launch_check("rowshift")) != FA_OK) return st;
         const long tiles = (S + GBN - 1) / GBN;
         k_gemm_simt<true><<<(unsigned)((long)B * p.nk[kk] * tiles * tiles), kThreads, 0, s>>>(
-            S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), p.nk[kk - 1], I(p.mu[kk]),
-            F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]));
+            S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), I(p.rminc[kk - 1]),
+            p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]), I(p.rminc[kk]), I(p.range_lost));
         if ((st = launch_check("span product (max)")) != FA_OK) return st;
     }
     stage_mark(2, s);
-    k_map_root<<<B, 32, 0, s>>>(dev_view(aut), L, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), I(p.z), score, row_status);
+    k_map_root<<<B, 32, 0, s>>>(dev_view(aut), L, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), I(p.z), score, row_status,
+                                I(p.range_lost));
     if ((st = launch_check("greedy root")) != FA_OK) return st;
     for (int kk = p.K - 1; kk >= 0; --kk) {
         const int np = p.nk[kk + 1];
@@ -1862,7 +1934,7 @@ extern "C" fa_status fa_transition_matrices(const fa_automaton *aut, int32_t B, 
     if (!probs || !committed || !mant || !row_exp) { fa_set_error("fa_transition_matrices: NULL buffer"); return FA_ERR_INVALID_ARG; }
     fa_status st = check_device(aut, "fa_transition_matrices");
     if (st != FA_OK) return st;
-    return launch_reweight(aut, B, L, probs, committed, mant, row_exp, nullptr, (cudaStream_t)stream);
+    return launch_reweight(aut, B, L, probs, committed, mant, row_exp, nullptr, nullptr, (cudaStream_t)stream);
 }
 
 extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
@@ -1941,8 +2013,8 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
 
     // 1. emission reweighting -> level-0 spans (also clears the row maxima of levels >= 1)
     stage_mark(0, s);
-    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), s, I(p.rmax_hi),
-                         (long)(p.rmax_hi_bytes / sizeof(int32_t)));
+    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), I(p.rminc[0]), s,
+                         I(p.rmax_hi), (long)(p.rmax_hi_bytes / sizeof(int32_t)));
     if (st != FA_OK) return st;
 
     if (chain) {
@@ -1970,8 +2042,8 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
         if (S <= SMALL_S) {
             const long tpd = (S + ST - 1) / ST;
             k_span_small<false><<<(unsigned)((long)B * p.nk[kk] * tpd * tpd), kThreads, 0, s>>>(
-                S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), p.nk[kk - 1], F(p.mant[kk]),
-                I(p.rho[kk]), I(p.rmax[kk]));
+                S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]), I(p.rminc[kk - 1]),
+                p.nk[kk - 1], F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]), I(p.rminc[kk]), I(p.range_lost));
             if ((st = launch_check("span product (small)")) != FA_OK) return st;
             continue;
         }
@@ -1982,15 +2054,16 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
         if (fa_span_tc_supported(S)) {
             g_launches.fetch_add(2, std::memory_order_relaxed);
             st = fa_span_tc_level(S, B, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
-                                  p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]), I(p.tc_err),
-                                  ws + p.img, s);
+                                  I(p.rminc[kk - 1]), p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]),
+                                  I(p.rmax[kk]), I(p.rminc[kk]), I(p.tc_err), I(p.range_lost), ws + p.img, s);
             if (st != FA_OK) return st;
             continue;
         }
         const long tiles = (S + GBN - 1) / GBN;
         const long g2 = (long)B * p.nk[kk] * tiles * tiles;
         k_gemm_simt<false><<<(unsigned)g2, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
-                                            p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]), I(p.rmax[kk]));
+                                            I(p.rminc[kk - 1]), p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]),
+                                            I(p.rmax[kk]), I(p.rminc[kk]), I(p.range_lost));
         if ((st = launch_check("span product")) != FA_OK) return st;
     }
 
@@ -1998,7 +2071,7 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
     if (!chain) stage_mark(2, s);
     if (!chain) k_root<<<B, kThreads, 0, s>>>(dev_view(aut), L, p.K, p.nk[p.K], F(p.mant[p.K]), I(p.rho[p.K]), philox_seed,
                                   philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be), F(p.zsum), I(p.zexp),
-                                  logZ, row_status, I(p.tc_err));
+                                  logZ, row_status, I(p.tc_err), I(p.range_lost));
     if (!chain && (st = launch_check("root")) != FA_OK) return st;
 
     // 4. top-down: midpoints and prefix/suffix messages, level K-1 .. 0

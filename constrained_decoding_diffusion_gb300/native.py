@@ -31,7 +31,7 @@ CONFIDENCE = {"marginal": FA_CONF_MARGINAL, "neg_entropy": FA_CONF_NEG_ENTROPY,
 EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_workspace_bytes",
            "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_ex", "fa_constrained_step_chain",
            "fa_token_marginals", "fa_map_step",
-           "fa_apply_commits", "fa_constrained_step_noalloc",
+           "fa_apply_commits", "fa_constrained_step_noalloc", "fa_debug_inject_wait_timeouts",
            "fa_profile_enable", "fa_profile_read",
            "fa_launch_count", "fa_last_error")
 N_STAGES = 4
@@ -83,6 +83,8 @@ def load(path: str = LIB_PATH):
     lib.fa_apply_commits.restype = st
     lib.fa_constrained_step_noalloc.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, P, P, P, P, P]
     lib.fa_constrained_step_noalloc.restype = st
+    lib.fa_debug_inject_wait_timeouts.argtypes = [i32]
+    lib.fa_debug_inject_wait_timeouts.restype = st
     lib.fa_profile_enable.argtypes = [i32]
     lib.fa_profile_enable.restype = st
     lib.fa_profile_read.argtypes = [P]
@@ -339,6 +341,13 @@ def fa_profile_read() -> dict:
     ms = np.zeros(N_STAGES, np.float32)
     _check(_lib.fa_profile_read(_np_ptr(ms)))
     return dict(zip(STAGES, (float(x) for x in ms)))
+
+
+def fa_debug_inject_wait_timeouts(n_launches: int):
+    """Failure tests: the next n_launches tensor-core span launches let a bounded wait run
+    out (the step reports FA_ROW_TIMEOUT); 0 disarms."""
+    load()
+    _check(_lib.fa_debug_inject_wait_timeouts(int(n_launches)))
 
 
 def fa_launch_count() -> int:

@@ -315,9 +315,12 @@ class Workload:
     def S(self) -> int:
         return self.fa.n_states
 
-    def probs(self, step: int = 0) -> np.ndarray:
+    def probs(self, step: int = 0, n_rows: Optional[int] = None) -> np.ndarray:
+        """The workload's probabilities at one remasking step; n_rows keeps only the first
+        sequences (the same values as the first rows of the whole batch)."""
         rng = np.random.default_rng([self.seed, 1000 + step])
-        return gaussian_probs(rng, self.B, self.L, self.V, self.sigma)
+        nb = self.B if n_rows is None else min(self.B, n_rows)
+        return gaussian_probs(rng, nb, self.L, self.V, self.sigma)
 
 
 WORKLOADS = ("real_number_L6", "random_dfa_S64_L128", "layered_chain_S256_L256",

@@ -56,8 +56,9 @@ typedef enum {
 enum {
     FA_ROW_OK = 0,
     FA_ROW_EMPTY = 1,     /* Z == 0: no accepted string has positive weight */
-    FA_ROW_UNDERFLOW = 2, /* a categorical the sampler needed summed to 0 in fp32 range */
-    FA_ROW_TIMEOUT = 3    /* reserved for bounded inter-block waits */
+    FA_ROW_UNDERFLOW = 2, /* range loss: a span product pushed nonzero mass below the fp32
+                             range, or a categorical the sampler needed summed to 0 */
+    FA_ROW_TIMEOUT = 3    /* a bounded wait inside a kernel ran out (work abandoned) */
 };
 
 /* Library limits. */
@@ -173,12 +174,19 @@ fa_status fa_transition_matrices(const fa_automaton *aut, int32_t B, int32_t L, 
  *                   bytes, 256-byte aligned, caller-owned; contents are
  *                   overwritten; concurrent steps need separate workspaces
  *   tokens          [B, L] int32 out: sampled x^ (committed positions echoed)
- *   logZ            [B] double out: ln Z (-inf when FA_ROW_EMPTY)
+ *   logZ            [B] double out: ln Z (-inf when FA_ROW_EMPTY or FA_ROW_TIMEOUT,
+ *                   NaN when the up-sweep lost range: FA_ROW_UNDERFLOW)
  *   marg            [B, L] fp32 out: constrained marginal of x^_t (1 for committed)
  *   commit_idx      [B, k] int32 out
  *   row_status      [B] int32 out: FA_ROW_*
  * When row_status[b] != FA_ROW_OK, tokens[b] echo committed (-1 where masked),
  * marg[b] is 0 where masked and commit_idx[b] is all -1.
+ *
+ * Range.  Span matrices keep an fp32 mantissa and a power-of-two exponent per row, so an
+ * entry more than about 2^126 below the largest entry of its row cannot be represented.
+ * Every span product checks its prescaled left operand: when a nonzero entry would leave
+ * the fp32 normal range, the sequence is reported as FA_ROW_UNDERFLOW (logZ NaN, no
+ * tokens, no commits) instead of being sampled from spans that lost mass.
  * Errors: FA_ERR_INVALID_ARG, FA_ERR_WORKSPACE_TOO_SMALL, FA_ERR_CUDA (launch).
  */
 fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
@@ -300,13 +308,15 @@ fa_status fa_apply_commits(int32_t B, int32_t L, int32_t k, const int32_t *commi
  * library, which every GPU that loads the library holds until the process exits.  The call
  * itself allocates nothing.
  *
- * The first call on a device (with that device current) looks up the array's device
- * address; make it before any stream capture.  All calls on a device share the array and
- * it keeps the last call's contents (the step initialises what it reads, so no clearing is
- * needed); calls whose GPU work overlaps race on it and must be serialised by the caller.
- * Errors: as fa_constrained_step, plus FA_ERR_WORKSPACE_TOO_SMALL when
- * fa_step_workspace_bytes(B, L) exceeds FA_NOALLOC_SCRATCH_BYTES, FA_ERR_CUDA if the
- * array's address cannot be obtained.
+ * Every call looks up the array's device address on the current device (so the address
+ * stays right after a device reset); the first call on a device also loads the library's
+ * device code there, so make it before any stream capture.  All calls on a device share
+ * the array and it keeps the last call's contents (the step initialises what it reads, so
+ * no clearing is needed); calls whose GPU work overlaps race on it and must be serialised
+ * by the caller.
+ * Errors: as fa_constrained_step (B, L and k are range-checked first), plus
+ * FA_ERR_WORKSPACE_TOO_SMALL when fa_step_workspace_bytes(B, L) exceeds
+ * FA_NOALLOC_SCRATCH_BYTES, FA_ERR_CUDA if the array's address cannot be obtained.
  */
 #define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
 fa_status fa_constrained_step_noalloc(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
@@ -314,6 +324,17 @@ fa_status fa_constrained_step_noalloc(const fa_automaton *aut, int32_t B, int32_
                                       int32_t k, int32_t commit_lo, int32_t commit_hi, int32_t *tokens,
                                       double *logZ, float *marg, int32_t *commit_idx, int32_t *row_status,
                                       fa_stream stream);
+
+/*
+ * fa_debug_inject_wait_timeouts -- failure-injection hook for tests (no counterpart on the
+ * pages).  The next n_launches launches of the tensor-core span product (|S| >= 128) make
+ * their MMA-issuing thread wait, with a short limit (about half a millisecond), on a
+ * barrier that nothing completes.  The wait runs out, every CTA of the launch abandons its
+ * tile after the copies and products it already issued have completed, and the step reports
+ * FA_ROW_TIMEOUT for every sequence; the next step is unaffected.  n_launches = 0 disarms.
+ * Process-wide.  Errors: FA_ERR_INVALID_ARG (n_launches < 0).
+ */
+fa_status fa_debug_inject_wait_timeouts(int32_t n_launches);
 
 /*
  * Stage timing and launch accounting (measurement support; no counterpart on the pages).

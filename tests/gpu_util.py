@@ -60,3 +60,53 @@ def check_against_oracle(fa, o: "oracle.OracleFA", probs, committed, res, k, lo=
         np.testing.assert_allclose(res["marg"][b], ref["marg_tokens"], rtol=0, atol=MARG_ATOL)
         if k > 0:
             check_commit(res["commit"][b], ref["marg_tokens"], com, k, lo, hi)
+
+
+# --------------------------------------------------------------------------- parallel oracle
+
+_WORKER_ORACLE = None
+
+
+def _worker_init(fa):
+    global _WORKER_ORACLE
+    _WORKER_ORACLE = oracle.OracleFA(fa)
+
+
+def _worker_posterior(args):
+    probs, committed, tokens = args
+    ref = _WORKER_ORACLE.posterior(probs, committed, tokens=np.where(tokens >= 0, tokens, 0))
+    return dict(logZ=ref["logZ"], empty=ref["empty"], marg_tokens=ref["marg_tokens"],
+                accepts=bool(_WORKER_ORACLE.accepts(tokens)) if (tokens >= 0).all() else False)
+
+
+def oracle_rows_parallel(fa, probs_rows, committed_rows, token_rows, workers: int = 8):
+    """The oracle's posterior (logZ, marginals of the given tokens) and acceptance of each row,
+    in a pool of spawned worker processes (spawn: the parent already holds a CUDA context)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    n = len(probs_rows)
+    with ctx.Pool(processes=max(1, min(workers, n, mp.cpu_count())), initializer=_worker_init,
+                  initargs=(fa,)) as pool:
+        return pool.map(_worker_posterior, [(np.ascontiguousarray(probs_rows[i], np.float32),
+                                             np.ascontiguousarray(committed_rows[i], np.int32),
+                                             np.ascontiguousarray(token_rows[i], np.int32)) for i in range(n)],
+                        chunksize=1)
+
+
+def check_rows_against_refs(refs, res, committed, k, lo, hi):
+    """check_against_oracle with the oracle's results computed beforehand (one per row)."""
+    for b, ref in enumerate(refs):
+        if ref["empty"]:
+            assert res["status"][b] == 1 and res["logZ"][b] == -np.inf
+            assert (res["commit"][b] == -1).all()
+            continue
+        assert res["status"][b] == 0, (b, res["status"][b])
+        lz, lz_ref = res["logZ"][b], ref["logZ"]
+        assert abs(lz - lz_ref) <= LOGZ_RTOL * max(1.0, abs(lz_ref)), (b, lz, lz_ref)
+        tok = res["tokens"][b]
+        com = committed[b]
+        assert np.array_equal(tok[com >= 0], com[com >= 0])
+        assert ref["accepts"], "sampled string rejected (row %d)" % b
+        np.testing.assert_allclose(res["marg"][b], ref["marg_tokens"], rtol=0, atol=MARG_ATOL)
+        if k > 0:
+            check_commit(res["commit"][b], ref["marg_tokens"], com, k, lo, hi)

@@ -374,9 +374,8 @@ def test_step_long_sequence_global_topk(native):
 
 @pytest.mark.parametrize("S", [128, 200, 300, 400, 512])
 def test_step_tensor_core_span_products(native, S):
-    """|S| >= 128 takes the tcgen05 3xTF32 span products; 200, 300 and 400 leave ragged
-    128x256 tiles.  Row tiles in clusters sharing the right operand: 1 CTA (128, 300),
-    2 CTAs (200) and 4 CTAs (400, 512)."""
+    """|S| >= 128 takes the tcgen05 3xTF32 span products, one CTA per 128x256 output tile;
+    200, 300 and 400 leave ragged tiles in both directions."""
     rng = np.random.default_rng(S)
     fa = synth.random_dfa(S, 3000, 0.8, 12, seed=S)
     o = oracle.OracleFA(fa)

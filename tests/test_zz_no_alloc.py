@@ -36,11 +36,16 @@ def _same(a, b):
 
 
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
+    """Three calls in a row on the shared scratch: the larger random-DFA layout, then the
+    small real-number one over its leftovers, then the random DFA again over the real-number
+    call's leftovers.  Each matches the workspace entry point: bit for bit on tokens, commit
+    set and status, within the oracle tolerances on logZ and the marginals."""
     import torch
     from constrained_decoding_diffusion_gb300 import native
     assert torch.cuda.is_available()
     native.load()
-    cases = [synth.workload("random_dfa_S64_L128"), synth.workload("real_number_L6", B=3)]
+    first = synth.workload("random_dfa_S64_L128")
+    cases = [first, synth.workload("real_number_L6", B=3), first]
     for call, w in enumerate(cases):
         aut = native.fa_compile(w.fa)
         probs = torch.from_numpy(w.probs(step=call)).cuda()
@@ -73,3 +78,19 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
                                            out["marg"], out["commit_idx"], out["row_status"])
     assert ei.value.code == native.FA_ERR_WORKSPACE_TOO_SMALL
     assert "scratch" in str(ei.value)
+
+
+def test_noalloc_rejects_out_of_range_batch_as_invalid():
+    import torch
+    from constrained_decoding_diffusion_gb300 import native
+    native.load()
+    w = synth.workload("real_number_L6")
+    aut = native.fa_compile(w.fa)
+    lib = native._lib
+    rc = lib.fa_constrained_step_noalloc(aut.handle, 70000, w.L, None, None, 1, 0, w.k, 0, w.L, None, None, None,
+                                         None, None, None)
+    assert rc == native.FA_ERR_INVALID_ARG
+    assert "out of range" in lib.fa_last_error().decode()
+    rc = lib.fa_constrained_step_noalloc(aut.handle, 1, w.L, None, None, 1, 0, -1, 0, w.L, None, None, None,
+                                         None, None, None)
+    assert rc == native.FA_ERR_INVALID_ARG
