@@ -49,6 +49,140 @@ struct RunLayout {
     std::vector<uint16_t> crun_slot, ru_tok;
 };
 
+// Entry order of one warp unit for one vocabulary chunk.  lr[l] holds lane l's runs (in slot
+// order), each as its in-chunk token indices.  A run takes whole groups of FA_GROUP_ENTRIES
+// entries (at least one), its last entry flagged with FA_RUN_END; every lane's stream is as
+// long as the longest one.  A pad reads one of the FA_PAD_SLOTS zero slots that follow the
+// chunk (index chunk + j, one per shared-memory bank), and the entries of one step (lane l's
+// k-th entry for l = 0..31) are chosen so that the lanes' real entries fall into distinct
+// banks: a run's sum is order-free, so at each step every lane picks any remaining token of
+// its current run, by a maximum bipartite matching of lanes to banks; a lane left without a
+// bank takes a pad if it has room (the rounding of its run to whole groups, or a spare group
+// of the lanes shorter than the longest), and only a lane with no room reads a conflicting
+// bank.  All the step's pads share one zero slot in a bank no real entry uses.  The result
+// is one shared-memory wavefront per warp gather in almost every step.
+// out[l] receives lane l's entries; returns the number of groups per lane.
+size_t schedule_unit_chunk(int CH, const std::vector<std::vector<std::vector<uint16_t>>> &lr,
+                           std::vector<std::vector<uint16_t>> &out) {
+    const int G = FA_GROUP_ENTRIES;
+    int64_t gmax = 0;
+    int64_t glane[32];
+    for (int l = 0; l < 32; ++l) {
+        glane[l] = 0;
+        for (const auto &r : lr[l]) glane[l] += std::max<int64_t>(1, ((int64_t)r.size() + G - 1) / G);
+        gmax = std::max(gmax, glane[l]);
+    }
+    struct Lane {
+        size_t q = 0;          // current run
+        int64_t u = 0, cap = 0, spare = 0;  // entries placed in the run, its room, spare entries
+        std::vector<uint16_t> bank[32];
+        int cnt[32] = {0}, left = 0;
+        uint32_t mask = 0;
+    };
+    std::vector<Lane> st(32);
+    auto open_run = [&](int l) {
+        Lane &s = st[l];
+        s.u = 0;
+        for (int b = 0; b < 32; ++b) { s.bank[b].clear(); s.cnt[b] = 0; }
+        s.mask = 0;
+        s.left = 0;
+        if (s.q >= lr[l].size()) { s.cap = 0; return; }
+        const auto &r = lr[l][s.q];
+        s.cap = G * std::max<int64_t>(1, ((int64_t)r.size() + G - 1) / G);
+        for (uint16_t t : r) { s.bank[t & 31].push_back(t); s.cnt[t & 31]++; s.mask |= 1u << (t & 31); }
+        s.left = (int)r.size();
+    };
+    for (int l = 0; l < 32; ++l) {
+        out[l].clear();
+        out[l].reserve((size_t)(gmax * G));
+        st[l].spare = G * (gmax - glane[l]);
+        open_run(l);
+    }
+    const int64_t steps = gmax * G;
+    int match[32];                 // bank -> lane
+    int order[32];
+    for (int64_t step = 0; step < steps; ++step) {
+        for (int b = 0; b < 32; ++b) match[b] = -1;
+        // lanes with real entries left, those without room for a pad first, then by room
+        int n = 0;
+        for (int l = 0; l < 32; ++l)
+            if (st[l].q < lr[l].size() && st[l].left > 0) order[n++] = l;
+        auto room = [&](int l) { return (st[l].cap - st[l].u - st[l].left) + st[l].spare; };
+        std::sort(order, order + n, [&](int x, int y) {
+            const int64_t rx = room(x), ry = room(y);
+            return rx != ry ? rx < ry : st[x].left > st[y].left;
+        });
+        uint32_t seen = 0;
+        // a lane tries its banks with the most tokens first (fewer forced choices later)
+        int bank_order[32][32], n_banks[32];
+        for (int i = 0; i < n; ++i) {
+            const int l = order[i];
+            int c = 0;
+            for (uint32_t m = st[l].mask; m; m &= m - 1) bank_order[l][c++] = __builtin_ctz(m);
+            std::sort(bank_order[l], bank_order[l] + c, [&](int x, int y) { return st[l].cnt[x] > st[l].cnt[y]; });
+            n_banks[l] = c;
+        }
+        std::function<bool(int)> augment = [&](int l) -> bool {
+            for (int j = 0; j < n_banks[l]; ++j) {
+                const int b = bank_order[l][j];
+                if (seen & (1u << b)) continue;
+                seen |= 1u << b;
+                if (match[b] < 0 || augment(match[b])) { match[b] = l; return true; }
+            }
+            return false;
+        };
+        int lane_bank[32];
+        for (int l = 0; l < 32; ++l) lane_bank[l] = -1;
+        for (int i = 0; i < n; ++i) { seen = 0; augment(order[i]); }
+        for (int b = 0; b < 32; ++b)
+            if (match[b] >= 0) lane_bank[match[b]] = b;
+        // banks used by real entries this step (addresses per bank for the forced conflicts)
+        int used[32] = {0};
+        for (int b = 0; b < 32; ++b) used[b] = match[b] >= 0;
+        uint16_t pick[32];
+        bool is_pad[32];
+        for (int l = 0; l < 32; ++l) {
+            Lane &s = st[l];
+            is_pad[l] = false;
+            if (s.q >= lr[l].size() || s.left == 0) { is_pad[l] = true; continue; }
+            int b = lane_bank[l];
+            if (b < 0) {
+                if (s.cap - s.u > s.left) { is_pad[l] = true; continue; }          // rounding room
+                if (s.spare >= G) { s.cap += G; s.spare -= G; is_pad[l] = true; continue; }  // a spare group
+                // no room: the least used of its banks (a conflict)
+                int best = -1;
+                for (uint32_t m = s.mask; m; m &= m - 1) {
+                    const int c = __builtin_ctz(m);
+                    if (best < 0 || used[c] < used[best]) best = c;
+                }
+                b = best;
+                used[b]++;
+            }
+            pick[l] = s.bank[b].back();
+            s.bank[b].pop_back();
+            if (--s.cnt[b] == 0) s.mask &= ~(1u << b);
+            s.left--;
+        }
+        int pad_bank = 0;
+        for (int b = 1; b < 32; ++b)
+            if (used[(CH + b) & 31] < used[(CH + pad_bank) & 31]) pad_bank = b;
+        for (int l = 0; l < 32; ++l) {
+            Lane &s = st[l];
+            uint16_t e = is_pad[l] ? (uint16_t)(CH + pad_bank) : pick[l];
+            if (s.q < lr[l].size()) {
+                s.u++;
+                if (s.u == s.cap) {          // the run's last entry
+                    e = (uint16_t)(e | FA_RUN_END);
+                    s.q++;
+                    open_run(l);
+                }
+            }
+            out[l].push_back(e);
+        }
+    }
+    return (size_t)gmax;
+}
+
 std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_t> &row_cell_off,
                              const std::vector<int64_t> &cell_off, const std::vector<int32_t> &cell_tok,
                              RunLayout &out) {
@@ -168,7 +302,7 @@ std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_
         for (int w = 0; w < g.nu; ++w) {
             for (int ch = 0; ch < nch; ++ch) {
                 const int32_t lo = ch * CH, hi = (int32_t)std::min<int64_t>((int64_t)(ch + 1) * CH, V);
-                // every lane's runs as lists of in-chunk indices, padded to whole groups
+                // every lane's runs as lists of in-chunk indices
                 std::vector<std::vector<std::vector<uint16_t>>> lr(32);
                 for (int l = 0; l < 32; ++l) {
                     for (int32_t ri : lane_runs[w * 32 + l]) {
@@ -176,116 +310,12 @@ std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_
                         std::vector<uint16_t> e;
                         for (int64_t x = cell_off[rn.cell] + rn.q; x < cell_off[rn.cell + 1]; x += rn.nr)
                             if (cell_tok[x] >= lo && cell_tok[x] < hi) e.push_back((uint16_t)(cell_tok[x] - lo));
-                        do e.push_back((uint16_t)CH);
-                        while (e.size() % FA_GROUP_ENTRIES);
                         lr[l].push_back(std::move(e));
                     }
                 }
-                // entry order: position by position, the 32 lanes' entries are chosen from their
-                // current runs (a run's sum is order-free; its last entry carries the end flag)
-                // so that they fall into distinct shared-memory banks or share an address:
-                // lanes with the fewest choices first, then augmenting paths for the rest
                 std::vector<std::vector<uint16_t>> out(32);
-                std::vector<size_t> cur(32, 0);
-                const int kWin = 48;
-                for (;;) {
-                    int lanes_left[32], nl = 0;
-                    for (int l = 0; l < 32; ++l)
-                        if (cur[l] < lr[l].size()) lanes_left[nl++] = l;
-                    if (!nl) break;
-                    int bank_addr[32], bank_lane[32];  // address held by a bank (-1 free), its first lane
-                    for (int q = 0; q < 32; ++q) { bank_addr[q] = -1; bank_lane[q] = -1; }
-                    int pick[32];
-                    for (int l = 0; l < 32; ++l) pick[l] = -1;
-                    std::sort(lanes_left, lanes_left + nl, [&](int x, int y) {
-                        return std::min<size_t>(lr[x][cur[x]].size(), kWin) < std::min<size_t>(lr[y][cur[y]].size(), kWin);
-                    });
-                    auto fits = [&](uint16_t tk) {
-                        return tk == (uint16_t)CH || bank_addr[tk & 31] == -1 || bank_addr[tk & 31] == tk;
-                    };
-                    std::vector<int> pending;
-                    for (int qi = 0; qi < nl; ++qi) {
-                        const int l = lanes_left[qi];
-                        const auto &rem = lr[l][cur[l]];
-                        const int nscan = (int)std::min<size_t>(rem.size(), kWin);
-                        int got = -1;
-                        for (int x = 0; x < nscan && got < 0; ++x)
-                            if (fits(rem[x])) got = x;
-                        if (got < 0) { pending.push_back(l); continue; }
-                        pick[l] = got;
-                        const uint16_t tk = rem[got];
-                        if (tk != (uint16_t)CH && bank_addr[tk & 31] == -1) { bank_addr[tk & 31] = tk; bank_lane[tk & 31] = l; }
-                    }
-                    // augmenting paths: lane l takes bank b from its sole holder m, which moves to
-                    // another free bank among its own candidates (depth-limited search)
-                    std::function<bool(int, int, std::vector<char> &)> augment = [&](int l, int depth,
-                                                                                      std::vector<char> &seen) {
-                        const auto &rem = lr[l][cur[l]];
-                        const int nscan = (int)std::min<size_t>(rem.size(), kWin);
-                        for (int x = 0; x < nscan; ++x) {
-                            const uint16_t tk = rem[x];
-                            if (fits(tk)) {
-                                pick[l] = x;
-                                if (tk != (uint16_t)CH && bank_addr[tk & 31] == -1) { bank_addr[tk & 31] = tk; bank_lane[tk & 31] = l; }
-                                return true;
-                            }
-                        }
-                        if (depth == 0) return false;
-                        for (int x = 0; x < nscan; ++x) {
-                            const int b = rem[x] & 31;
-                            if (seen[b]) continue;
-                            seen[b] = 1;
-                            const int m = bank_lane[b];
-                            if (m < 0) continue;
-                            // m must be the only lane on bank b (no other lane shares its address)
-                            bool sole = true;
-                            for (int o = 0; o < 32 && sole; ++o)
-                                if (o != m && pick[o] >= 0 && lr[o][cur[o]][pick[o]] == (uint16_t)bank_addr[b]) sole = false;
-                            if (!sole) continue;
-                            const int keep_pick = pick[m];
-                            const int keep_addr = bank_addr[b];
-                            pick[m] = -1;
-                            bank_addr[b] = -2;  // reserved for l: m may not return to it
-                            bank_lane[b] = -1;
-                            if (augment(m, depth - 1, seen)) {
-                                bank_addr[b] = rem[x];
-                                bank_lane[b] = l;
-                                pick[l] = x;
-                                return true;
-                            }
-                            bank_addr[b] = keep_addr;
-                            bank_lane[b] = m;
-                            pick[m] = keep_pick;
-                        }
-                        return false;
-                    };
-                    int used[32] = {0};
-                    for (int l : pending) {
-                        std::vector<char> seen(32, 0);
-                        if (augment(l, 3, seen)) continue;
-                        // no free bank: the least-used bank among the candidates
-                        const auto &rem = lr[l][cur[l]];
-                        const int nscan = (int)std::min<size_t>(rem.size(), kWin);
-                        int best = 0, bc = 1 << 30;
-                        for (int x = 0; x < nscan; ++x)
-                            if (used[rem[x] & 31] < bc) { bc = used[rem[x] & 31]; best = x; }
-                        pick[l] = best;
-                        used[rem[best] & 31]++;
-                    }
-                    for (int qi = 0; qi < nl; ++qi) {
-                        const int l = lanes_left[qi];
-                        auto &rem = lr[l][cur[l]];
-                        uint16_t tk = rem[pick[l]];
-                        rem[pick[l]] = rem.back();
-                        rem.pop_back();
-                        if (rem.empty()) { tk = (uint16_t)(tk | FA_RUN_END); cur[l]++; }
-                        out[l].push_back(tk);
-                    }
-                }
                 const int G = FA_GROUP_ENTRIES;
-                size_t len = 0;
-                for (int l = 0; l < 32; ++l) len = std::max(len, out[l].size());
-                len = (len + G - 1) / G;
+                const size_t len = schedule_unit_chunk(CH, lr, out);
                 const size_t g0 = ru_tok.size() / G;
                 ru_goff.push_back((int32_t)g0);
                 ru_tok.resize(ru_tok.size() + len * 32 * G, (uint16_t)CH);

@@ -49,8 +49,9 @@ struct fa_automaton {
     // into runs (run q of nr takes tokens q, q + nr, ...); a run belongs to one lane of one
     // warp unit and owns one accumulator slot.  Unit u's entries for chunk c are 8-byte
     // groups of FA_GROUP_ENTRIES uint16 entries at ru_goff[u*n_chunks+c] + 32 k + lane
-    // (k = 0, 1, ...): bits 0-14 give the in-chunk token index (chunk_tokens = a zero pad
-    // slot); a run's entries fill whole groups, and bit 15 of a group's last entry ends the
+    // (k = 0, 1, ...): bits 0-14 give the in-chunk token index (chunk_tokens + j for j <
+    // FA_PAD_SLOTS = a zero pad slot, one per shared-memory bank, so the lanes of one step
+    // read distinct banks or one shared pad address); a run's entries fill whole groups, and bit 15 of a group's last entry ends the
     // lane's current run (every run ends exactly once per chunk, so slot j of a lane is its
     // j-th run).  A lane's slot j is at FA_UNIT_SLOTS * (unit - row_unit0[row]) + 32 j + lane
     // relative to the first unit of the row's group; cell x adds the slots
@@ -81,6 +82,7 @@ void fa_set_error(const std::string &msg);
 #define FA_SD_NONE 0xFFFFFFFFu       // tok_sd padding
 #define FA_RUN_END 0x8000u           // entry flag: last entry of the lane's current run
 #define FA_GROUP_ENTRIES 4           // entries per 8-byte group; runs end only at group ends
+#define FA_PAD_SLOTS 32              // zero slots after a staged chunk, one per shared-memory bank
 #ifndef FA_RUN_SLOTS
 #define FA_RUN_SLOTS 8               // runs (accumulator slots) per lane
 #endif

@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
         for (long i = bid * nthr + threadIdx.x; i < n_zero; i += nb * nthr) zero[i] = 0;
     }
     const int S = fa.S, CH = fa.chunk_tokens, nch = fa.n_chunks;
-    // shared memory: [0, tot_floats) holds the staged chunk ([CH] = 0) while the chunks are
-    // walked, then every unit's run totals (FA_UNIT_SLOTS per unit) followed by the row maxima
+    // shared memory: [0, tot_floats) holds the staged chunk, followed by the pad entries'
+    // zero slots [CH, CH + FA_PAD_SLOTS), while the chunks are walked, then every unit's run totals (FA_UNIT_SLOTS per unit) followed by the row maxima
     // and the complemented row minima; after it, one slot array per warp for the run sums of
     // the chunk being walked
     float *utot = smem_f;
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
             } else {
                 for (int i = tid; i < n; i += nthr) smem_f[i] = __ldg(prow + base + i);
             }
-            if (tid == 0) smem_f[CH] = 0.0f;
+            if (tid < FA_PAD_SLOTS) smem_f[CH + tid] = 0.0f;  // the pad entries' zero slots
             asm volatile("cp.async.wait_all;\n" ::: "memory");
             __syncthreads();
             const int boff = 0;
@@ -1778,7 +1778,7 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     const int threads = std::min(32 * FA_RW_WARPS, std::max(256, 32 * max_units));
     // the staged chunk, whose space takes the units' run totals and the row maxima and minima
     // at the end, then one run-slot array per warp
-    const int tot_floats = (int)std::max((size_t)((a->chunk_tokens + 4) & ~3),
+    const int tot_floats = (int)std::max((size_t)((a->chunk_tokens + FA_PAD_SLOTS + 3) & ~3),
                                          (size_t)max_units * FA_UNIT_SLOTS + 2 * (size_t)a->part_max_rows[p]);
     const size_t smem = sizeof(float) * ((size_t)tot_floats + (size_t)(threads / 32) * FA_UNIT_SLOTS);
     // units per warp: the register totals of a third unit cost the smaller layouts ~10%

@@ -74,7 +74,7 @@ int main(int argc, char **argv) {
             std::vector<float> tot((size_t)nu * FA_UNIT_SLOTS, 0.0f);
             for (int ch = 0; ch < nch; ++ch) {
                 const int base = ch * CH, n = std::min(CH, V - base);
-                std::vector<float> sp(CH + 1, 0.0f);
+                std::vector<float> sp(CH + FA_PAD_SLOTS, 0.0f);
                 for (int q = 0; q < n; ++q) sp[q] = probs[base + q];
                 for (int w = 0; w < nu; ++w) {
                     const size_t ui = (size_t)(u0 + w) * nch + ch;
@@ -89,7 +89,7 @@ int main(int argc, char **argv) {
                             for (int h = 0; h < G; ++h) {
                                 const uint32_t e = rl.ru_tok[((size_t)gb + (size_t)k * 32 + l) * G + h];
                                 const int idx = e & 0x7fff;
-                                if (idx > CH || (idx != CH && idx >= n)) { ++bad; continue; }
+                                if (idx >= CH + FA_PAD_SLOTS || (idx < CH && idx >= n)) { ++bad; continue; }
                                 acc += sp[idx];
                                 ++entries;
                                 if (e & FA_RUN_END) {
