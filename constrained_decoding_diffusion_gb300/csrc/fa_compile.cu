@@ -46,12 +46,14 @@ fa_status cuda_fail(const char *what, cudaError_t e) {
 struct RunLayout {
     int32_t chunk_tokens = 0, n_chunks = 1, n_units = 0;
     std::vector<int32_t> row_unit0, crun_off, ru_goff, rbm, part_first, part_count, part_max_units, part_max_rows;
+    std::vector<int64_t> part_tile_floats;
     std::vector<uint16_t> crun_slot, ru_tok;
 };
 
 // Entry order of one warp unit for one vocabulary chunk.  lr[l] holds lane l's runs (in slot
 // order), each as its in-chunk token indices.  A run takes whole groups of FA_GROUP_ENTRIES
-// entries (at least one), its last entry flagged with FA_RUN_END; every lane's stream is as
+// entries (at least one), the first entry of its last group flagged with FA_RUN_END (the
+// reweight reads a group's flag before summing it); every lane's stream is as
 // long as the longest one.  A pad reads one of the FA_PAD_SLOTS zero slots that follow the
 // chunk (index chunk + j, one per shared-memory bank), and the entries of one step (lane l's
 // k-th entry for l = 0..31) are chosen so that the lanes' real entries fall into distinct
@@ -200,7 +202,7 @@ std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_
     out.chunk_tokens = CH;
     out.n_chunks = nch;
     const int64_t kUnitTokens = 8192;        // tokens per warp unit (over all chunks)
-    const int kSmallCells = 128, kUnitCells = 192;  // at most 6 runs per lane on average
+    const int kSmallCells = 128, kUnitCells = 256;  // at most 8 runs per lane on average
     struct Group { int32_t r0, r1, u0, nu, c0, c1; };
     std::vector<Group> groups;
     std::vector<int32_t> &row_unit0 = out.row_unit0;
@@ -319,8 +321,18 @@ std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_
                 const size_t g0 = ru_tok.size() / G;
                 ru_goff.push_back((int32_t)g0);
                 ru_tok.resize(ru_tok.size() + len * 32 * G, (uint16_t)CH);
+                // the scheduler flags a run's last entry; the stored group carries the flag on
+                // its first entry instead (no other entry has bit 15 set)
                 for (int l = 0; l < 32; ++l)
-                    for (size_t k = 0; k < out[l].size(); ++k) ru_tok[(g0 + (k / G) * 32 + l) * G + (k % G)] = out[l][k];
+                    for (size_t k = 0; k < out[l].size(); k += G) {
+                        const uint16_t end = out[l][k + G - 1] & FA_RUN_END;
+                        for (int h = 0; h < G; ++h) {
+                            uint16_t e = (uint16_t)(out[l][k + h] & ~FA_RUN_END);
+                            if (e >= CH + FA_PAD_SLOTS) return "reweight layout: entry out of range";
+                            if (h == 0) e = (uint16_t)(e | end);
+                            ru_tok[(g0 + (k / G) * 32 + l) * G + h] = e;
+                        }
+                    }
                 if (ru_tok.size() / G > (size_t)INT32_MAX / 2) return "automaton too large";
             }
         }
@@ -343,6 +355,7 @@ std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_
         const int cap = caps[p];
         out.part_first.push_back((int32_t)(rbm.size() / 8));
         int count = 0, maxu = 1, maxr = 1;
+        int64_t maxt = 0;
         for (size_t gi = 0; gi < groups.size();) {
             size_t gj = gi;
             int nu = 0;
@@ -351,12 +364,14 @@ std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_
             rbm.insert(rbm.end(), {A.r0, Z.r1, A.u0, Z.u0 + Z.nu, A.c0, Z.c1, 0, 0});
             maxu = std::max(maxu, nu);
             maxr = std::max(maxr, Z.r1 - A.r0);
+            maxt = std::max<int64_t>(maxt, (int64_t)nu * FA_UNIT_SLOTS + (int64_t)(Z.r1 - A.r0) * S);
             ++count;
             gi = gj;
         }
         out.part_count.push_back(count);
         out.part_max_units.push_back(maxu);
         out.part_max_rows.push_back(maxr);
+        out.part_tile_floats.push_back(maxt);
         if (p + 1 == (int)caps.size() || count == (int)groups.size()) break;
     }
     return std::string();
@@ -492,6 +507,16 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     a->part_count = rl.part_count;
     a->part_max_units = rl.part_max_units;
     a->part_max_rows = rl.part_max_rows;
+    a->part_tile_floats = rl.part_tile_floats;
+
+    std::vector<int2> cell_rec(a->n_cells);
+    for (int c = 0; c < a->n_cells; ++c) {
+        const int s = cell_src[c];
+        cell_rec[c].x = s * S + cell_dst[c];
+        cell_rec[c].y = rl.crun_off[c + 1] - rl.crun_off[c] == 1
+                            ? rl.row_unit0[s] * FA_UNIT_SLOTS + (int32_t)rl.crun_slot[rl.crun_off[c]]
+                            : -1;
+    }
 
     std::vector<int32_t> esrc(edge_src, edge_src + E), edst(edge_dst, edge_dst + E);
     // the (src, dst) pair of every token-edge incidence (|S| <= 4096 fits 16 bits), the tokens
@@ -547,6 +572,7 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     bb.add(&a->row_unit0, rl.row_unit0);
     bb.add(&a->crun_off, rl.crun_off);
     bb.add(&a->crun_slot, rl.crun_slot);
+    bb.add(&a->cell_rec, cell_rec);
 
     cudaError_t err = cudaMalloc(&a->blob, bb.total);
     if (err != cudaSuccess) { delete a; return cuda_fail("fa_compile: cudaMalloc", err); }

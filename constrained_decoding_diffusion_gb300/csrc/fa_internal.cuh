@@ -51,15 +51,18 @@ struct fa_automaton {
     // groups of FA_GROUP_ENTRIES uint16 entries at ru_goff[u*n_chunks+c] + 32 k + lane
     // (k = 0, 1, ...): bits 0-14 give the in-chunk token index (chunk_tokens + j for j <
     // FA_PAD_SLOTS = a zero pad slot, one per shared-memory bank, so the lanes of one step
-    // read distinct banks or one shared pad address); a run's entries fill whole groups, and bit 15 of a group's last entry ends the
-    // lane's current run (every run ends exactly once per chunk, so slot j of a lane is its
-    // j-th run).  A lane's slot j is at FA_UNIT_SLOTS * (unit - row_unit0[row]) + 32 j + lane
+    // read distinct banks or one shared pad address); a run's entries fill whole groups, and
+    // bit 15 of a group's first entry says that the group ends the lane's current run (every
+    // run ends exactly once per chunk, so slot j of a lane is its j-th run).  A lane's slot j is at FA_UNIT_SLOTS * (unit - row_unit0[row]) + 32 j + lane
     // relative to the first unit of the row's group; cell x adds the slots
     // crun_slot[crun_off[x] .. crun_off[x+1]] in order.
     int32_t chunk_tokens = 0, n_chunks = 1, n_units = 0;
     uint16_t *ru_tok = nullptr;
     int32_t *ru_goff = nullptr, *row_unit0 = nullptr, *crun_off = nullptr;
     uint16_t *crun_slot = nullptr;
+    // per cell {s * |S| + dst, its slot relative to the unit array (FA_UNIT_SLOTS * row_unit0[s]
+    // + crun_slot) when the cell is one run, else -1}: one coalesced load per cell
+    int2 *cell_rec = nullptr;
     // row blocks for the reweight grid: partition p holds part_count[p] blocks of whole rows
     // (at most FA_RW_MAX_UNITS, 32, 16, ..., 1 units each for p = 0, 1, 2, ..., unless one row
     // group needs more); block i of partition p is rb_meta[8 * (part_first[p] + i) ..] =
@@ -67,6 +70,8 @@ struct fa_automaton {
     // 32 part_max_units[p])) threads, a warp walking up to three units.
     int32_t *rb_meta = nullptr;
     std::vector<int32_t> part_first, part_count, part_max_units, part_max_rows;
+    // per partition, the largest block's unit totals plus its rows of M_t, in floats
+    std::vector<int64_t> part_tile_floats;
     void *blob = nullptr;  // one device allocation holding every array above
     size_t blob_bytes = 0;
 };
@@ -80,7 +85,7 @@ void fa_set_error(const std::string &msg);
 #define FA_REWEIGHT_MAX_CHUNK 24576  // tokens per staged vocabulary chunk
 #endif
 #define FA_SD_NONE 0xFFFFFFFFu       // tok_sd padding
-#define FA_RUN_END 0x8000u           // entry flag: last entry of the lane's current run
+#define FA_RUN_END 0x8000u           // flag on a group's first entry: the group ends the lane's run
 #define FA_GROUP_ENTRIES 4           // entries per 8-byte group; runs end only at group ends
 #define FA_PAD_SLOTS 32              // zero slots after a staged chunk, one per shared-memory bank
 #ifndef FA_RUN_SLOTS

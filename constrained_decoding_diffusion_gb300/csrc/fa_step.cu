@@ -113,6 +113,7 @@ struct DevFA {
     const int64_t *cell_off;
     const int32_t *cell_tok;
     const uint16_t *ru_tok, *crun_slot;
+    const int2 *cell_rec;
     const int32_t *ru_goff, *row_unit0, *crun_off;
     int chunk_tokens, n_chunks, n_cells;
 };
@@ -129,6 +130,7 @@ DevFA dev_view(const fa_automaton *a) {
     d.cell_off = a->cell_off; d.cell_tok = a->cell_tok;
     d.ru_tok = a->ru_tok; d.crun_slot = a->crun_slot; d.ru_goff = a->ru_goff;
     d.row_unit0 = a->row_unit0; d.crun_off = a->crun_off;
+    d.cell_rec = a->cell_rec;
     d.chunk_tokens = a->chunk_tokens; d.n_chunks = a->n_chunks; d.n_cells = a->n_cells;
     return d;
 }
@@ -171,6 +173,44 @@ __device__ int warp_categorical(int n, float u, WF w) {
 
 // ----------------------------------------------------------------------------- 1. reweight
 
+// The reweight's entry groups.  A group is four 16-bit entries (x: entries 0 and 1, y: 2 and
+// 3); bits 0-14 of each index the staged chunk, whose shared address is base, and bit 15 of
+// entry 0 says that the group ends the lane's current run (no other entry has bit 15 set).
+// Written as PTX so that a group costs four shared loads and a handful of integer and float
+// instructions, with no branch.
+#define FA_RW_GATHER_PTX(OP)                                                                  \
+    "{\n\t.reg .u32 a0, a1, a2, a3;\n\t.reg .f32 f0, f1, f2, f3;\n\t"                         \
+    "and.b32 a0, %1, 32767;\n\tshr.u32 a1, %1, 16;\n\tand.b32 a2, %2, 65535;\n\tshr.u32 a3, %2, 16;\n\t" \
+    "mad.lo.u32 a0, a0, 4, %3;\n\tmad.lo.u32 a1, a1, 4, %3;\n\t"                               \
+    "mad.lo.u32 a2, a2, 4, %3;\n\tmad.lo.u32 a3, a3, 4, %3;\n\t"                               \
+    "ld.shared.f32 f0, [a0];\n\tld.shared.f32 f1, [a1];\n\t"                                   \
+    "ld.shared.f32 f2, [a2];\n\tld.shared.f32 f3, [a3];\n\t"                                   \
+    OP ".f32 f0, f0, f1;\n\t" OP ".f32 f2, f2, f3;\n\t" OP ".f32 %0, f0, f2;\n\t}"
+
+// Sum (MAX: maximum) of the four staged probabilities a group names.
+template <bool MAX>
+__device__ __forceinline__ float rw_gather(const uint2 v, uint32_t base) {
+    float s;
+    if constexpr (MAX) asm volatile(FA_RW_GATHER_PTX("max") : "=f"(s) : "r"(v.x), "r"(v.y), "r"(base));
+    else asm volatile(FA_RW_GATHER_PTX("add") : "=f"(s) : "r"(v.x), "r"(v.y), "r"(base));
+    return s;
+}
+
+#define FA_RW_END_PTX(OP)                                                                     \
+    "{\n\t.reg .u32 t, ad;\n\t.reg .pred p;\n\t" OP ".f32 %0, %0, %2;\n\t"                    \
+    "and.b32 t, %3, 32768;\n\tsetp.ne.u32 p, t, 0;\n\tselp.b32 ad, %1, %4, p;\n\t"             \
+    "st.shared.f32 [ad], %0;\n\tselp.f32 %0, 0f00000000, %0, p;\n\t"                           \
+    "shr.u32 t, t, 8;\n\tadd.u32 %1, %1, t;\n\t}"
+
+// Adds a group's sum s to the lane's running run sum acc; if the group ends the run (x = the
+// group's first two entries), stores acc at the run's slot, clears it and steps slot to the
+// next one (128 bytes on); otherwise the store goes to the lane's dummy slot.
+template <bool MAX>
+__device__ __forceinline__ void rw_group_end(float s, uint32_t x, uint32_t dummy, float &acc, uint32_t &slot) {
+    if constexpr (MAX) asm volatile(FA_RW_END_PTX("max") : "+f"(acc), "+r"(slot) : "f"(s), "r"(x), "r"(dummy));
+    else asm volatile(FA_RW_END_PTX("add") : "+f"(acc), "+r"(slot) : "f"(s), "r"(x), "r"(dummy));
+}
+
 // One block per (position, row block): M_t(s, s') for rows s in [r0, r1), row exponent 0.  A
 // masked position sums its probabilities over each cell's tokens (papernotes.org key design
 // 1: g(x=v | z=e) = 1[v in label(e)] p_t(v), aggregated over the edges s -> s'); a committed
@@ -190,7 +230,8 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
                                                                 const int32_t *__restrict__ committed,
                                                                 const int4 *__restrict__ rbm, int nrb, int tot_floats,
                                                                     float *mant, int32_t *rho, int32_t *rmax,
-                                                                    int32_t *rminc, int32_t *zero, long n_zero) {
+                                                                    int32_t *rminc, int32_t *zero, long n_zero,
+                                                                    int tile) {
     extern __shared__ float smem_f[];
     const int nthr = blockDim.x;
     // clear the row maxima of the higher tree levels (their products accumulate with atomicMax)
@@ -201,9 +242,10 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
     }
     const int S = fa.S, CH = fa.chunk_tokens, nch = fa.n_chunks;
     // shared memory: [0, tot_floats) holds the staged chunk, followed by the pad entries'
-    // zero slots [CH, CH + FA_PAD_SLOTS), while the chunks are walked, then every unit's run totals (FA_UNIT_SLOTS per unit) followed by the row maxima
-    // and the complemented row minima; after it, one slot array per warp for the run sums of
-    // the chunk being walked
+    // zero slots [CH, CH + FA_PAD_SLOTS), while the chunks are walked, then every unit's run
+    // totals (FA_UNIT_SLOTS per unit) followed by the row maxima and the complemented row
+    // minima; after it, one slot array per warp for the run sums of the chunk being walked,
+    // then one dummy slot per lane that takes the stores of groups ending no run
     float *utot = smem_f;
     float *slots = smem_f + tot_floats;                    // [FA_RW_WARPS * FA_UNIT_SLOTS]
     const int t = blockIdx.x / nrb, r = blockIdx.x % nrb, b = blockIdx.y;
@@ -216,9 +258,10 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
     int *smin = smax + (r1 - r0);                          // [rows] complemented row minima
     float *M = mant + pos * (size_t)S * S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // a masked position writes every cell of its rows: the rest of the rows is cleared, all
-    // of it unless the cells cover every (s, s') pair of the rows
-    if (c >= 0 || c1 - c0 < (r1 - r0) * S)
+    // a masked position writes every cell of its rows (whole rows when they are assembled in
+    // shared memory): the rest of the rows is cleared, all of it unless the cells cover every
+    // (s, s') pair of the rows
+    if (c >= 0 || (!tile && c1 - c0 < (r1 - r0) * S))
         for (size_t i = (size_t)r0 * S + tid; i < (size_t)r1 * S; i += nthr) M[i] = 0.0f;
     if (c < 0) {
         const float *prow = probs + pos * (size_t)fa.V;
@@ -229,6 +272,9 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
         // order.  Warp w walks units w, w + FA_RW_WARPS, ... of the block (UPW at most).
         float *my = slots + warp * FA_UNIT_SLOTS + lane;
         const uint32_t my_addr = (uint32_t)__cvta_generic_to_shared(my);
+        // one dummy slot per lane after the warps' slot arrays (shared by the warps; never read)
+        const uint32_t dummy_addr =
+            (uint32_t)__cvta_generic_to_shared(slots + (blockDim.x >> 5) * FA_UNIT_SLOTS + lane);
         float tot[UPW][FA_RUN_SLOTS];
 #pragma unroll
         for (int h = 0; h < UPW; ++h)
@@ -252,67 +298,50 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
             if (tid < FA_PAD_SLOTS) smem_f[CH + tid] = 0.0f;  // the pad entries' zero slots
             asm volatile("cp.async.wait_all;\n" ::: "memory");
             __syncthreads();
-            const int boff = 0;
 #pragma unroll
             for (int h = 0; h < UPW; ++h) {
                 const int uw = warp + FA_RW_WARPS * h;
                 if (uw >= nu) break;
                 const size_t ui = (size_t)(u0 + uw) * nch + ch;
-                const int gb = fa.ru_goff[ui];
-                const int ng = (fa.ru_goff[ui + 1] - gb) >> 5;
+                const int gb = __ldg(fa.ru_goff + ui);
+                const int ng = (__ldg(fa.ru_goff + ui + 1) - gb) >> 5;
                 const uint2 *gp = g4 + gb + lane;
                 float acc = 0.0f;
                 uint32_t slot_addr = my_addr;  // shared address of the current run's slot
-                // one group of four entries: add their staged probabilities; at a run end
-                // (bit 15 of the last entry) store the sum into the run's slot, clear it and
-                // step to the next slot, all predicated (no branch)
-#define FA_RW_GROUP(V)                                                                                 \
-    {                                                                                                  \
-        const uint32_t x_ = (V).x, y_ = (V).y;                                                         \
-        const float q0_ = smem_f[boff + (int)(x_ & 0x7fffu)], q1_ = smem_f[boff + (int)((x_ >> 16) & 0x7fffu)]; \
-        const float q2_ = smem_f[boff + (int)(y_ & 0x7fffu)], q3_ = smem_f[boff + (int)((y_ >> 16) & 0x7fffu)]; \
-        const float p0_ = MAX ? fmaxf(q0_, q1_) : q0_ + q1_;                                           \
-        const float p1_ = MAX ? fmaxf(q2_, q3_) : q2_ + q3_;                                           \
-        if constexpr (MAX) acc = fmaxf(acc, fmaxf(p0_, p1_)); else acc += p0_ + p1_;                   \
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.shared.f32 [%1], %0;\n\t"  \
-                     "@p mov.f32 %0, 0f00000000;\n\t@p add.u32 %1, %1, 128;\n\t}"                   \
-                     : "+f"(acc), "+r"(slot_addr)                                                      \
-                     : "r"(y_ & 0x80000000u)                                                           \
-                     : "memory");                                                                      \
-    }
-                // whole steps of four groups, the next four loaded (unconditionally: the
-                // stream array is padded past its end) while these are summed; then the tail
-                uint2 cv[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) cv[q] = __ldg(gp + (size_t)q * 32);
+                const uint32_t cbase = (uint32_t)__cvta_generic_to_shared(smem_f);
+                // whole steps of four groups (their sixteen gathers first, then the run-end
+                // stores), the next four loaded (unconditionally: the stream array is padded
+                // past its end) while these are summed; then the tail
+                uint2 c0v = __ldg(gp), c1v = __ldg(gp + 32), c2v = __ldg(gp + 64), c3v = __ldg(gp + 96);
                 int k = 0;
                 for (; k + 4 <= ng; k += 4) {
-                    uint2 nv[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) nv[q] = __ldg(gp + (size_t)(k + 4 + q) * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) FA_RW_GROUP(cv[q]);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) cv[q] = nv[q];
+                    gp += 128;
+                    const uint2 n0 = __ldg(gp), n1 = __ldg(gp + 32), n2 = __ldg(gp + 64), n3 = __ldg(gp + 96);
+                    const float s0 = rw_gather<MAX>(c0v, cbase), s1 = rw_gather<MAX>(c1v, cbase);
+                    const float s2 = rw_gather<MAX>(c2v, cbase), s3 = rw_gather<MAX>(c3v, cbase);
+                    rw_group_end<MAX>(s0, c0v.x, dummy_addr, acc, slot_addr);
+                    rw_group_end<MAX>(s1, c1v.x, dummy_addr, acc, slot_addr);
+                    rw_group_end<MAX>(s2, c2v.x, dummy_addr, acc, slot_addr);
+                    rw_group_end<MAX>(s3, c3v.x, dummy_addr, acc, slot_addr);
+                    c0v = n0; c1v = n1; c2v = n2; c3v = n3;
                 }
-                for (int q = 0; k < ng; ++k, ++q) {
-                    const uint2 v = q == 0 ? cv[0] : q == 1 ? cv[1] : cv[2];
-                    FA_RW_GROUP(v);
-                }
-#undef FA_RW_GROUP
+                if (k < ng) rw_group_end<MAX>(rw_gather<MAX>(c0v, cbase), c0v.x, dummy_addr, acc, slot_addr);
+                if (k + 1 < ng) rw_group_end<MAX>(rw_gather<MAX>(c1v, cbase), c1v.x, dummy_addr, acc, slot_addr);
+                if (k + 2 < ng) rw_group_end<MAX>(rw_gather<MAX>(c2v, cbase), c2v.x, dummy_addr, acc, slot_addr);
+                // the slot stores above are ordered before the reads below
+                asm volatile("" ::: "memory");
                 // runs of this lane = run ends seen in the walk; fold the slots it wrote (the
-                // others may hold the sums of the warp's other unit)
+                // others may hold the sums of the warp's other unit); every lane reads only its
+                // own slots
                 const int mine = (int)((slot_addr - my_addr) >> 7);
                 const int nrun = __reduce_max_sync(0xffffffffu, mine);
-                __syncwarp();
 #pragma unroll
                 for (int q = 0; q < FA_RUN_SLOTS; ++q) {
                     if (q >= nrun) break;
-                    if (q < mine) {
-                        if constexpr (MAX) tot[h][q] = fmaxf(tot[h][q], my[q * 32]); else tot[h][q] += my[q * 32];
-                    }
+                    const float sv = q < mine ? my[q * 32] : 0.0f;
+                    if constexpr (MAX) tot[h][q] = fmaxf(tot[h][q], sv); else tot[h][q] += sv;
                 }
-                __syncwarp();  // the next walk reuses the slots
+                asm volatile("" ::: "memory");
             }
         }
         __syncthreads();  // the chunk buffer is free now: it takes the units' totals
@@ -324,16 +353,35 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
                 for (int q = 0; q < FA_RUN_SLOTS; ++q) utot[uw * FA_UNIT_SLOTS + q * 32 + lane] = tot[h][q];
             }
         }
-        for (int i = tid; i < r1 - r0; i += nthr) { smax[i] = 0; smin[i] = 0; }
+        // tile != 0: the block's rows of M_t are assembled in shared memory after the totals
+        // (dense, zero where no cell lies) and written out row by row, coalesced, with each
+        // row's maximum and smallest nonzero entry; else cells store straight to M_t
+        float *mt = utot + nu * FA_UNIT_SLOTS;
+        const int nrow = r1 - r0;
+        if (tile) {
+            for (int i = tid; i < nrow * S; i += nthr) mt[i] = 0.0f;
+        } else {
+            for (int i = tid; i < nrow; i += nthr) { smax[i] = 0; smin[i] = 0; }
+        }
         __syncthreads();
+#pragma unroll 4
         for (int cell = c0 + tid; cell < c1; cell += nthr) {
-            const int s = fa.cell_src[cell];
-            const float *sb = utot + (size_t)(fa.row_unit0[s] - u0) * FA_UNIT_SLOTS;
+            const int2 rec = __ldg(fa.cell_rec + cell);
             float v = 0.0f;
-            for (int q = fa.crun_off[cell]; q < fa.crun_off[cell + 1]; ++q) {
-                if constexpr (MAX) v = fmaxf(v, sb[fa.crun_slot[q]]); else v += sb[fa.crun_slot[q]];
+            if (rec.y >= 0) {
+                v = utot[rec.y - u0 * FA_UNIT_SLOTS];   // a cell of one run
+            } else {
+                const float *sb = utot + (size_t)(fa.row_unit0[rec.x / S] - u0) * FA_UNIT_SLOTS;
+                for (int q = fa.crun_off[cell]; q < fa.crun_off[cell + 1]; ++q) {
+                    if constexpr (MAX) v = fmaxf(v, sb[fa.crun_slot[q]]); else v += sb[fa.crun_slot[q]];
+                }
             }
-            M[(size_t)s * S + fa.cell_dst[cell]] = v;
+            if (tile) {
+                mt[rec.x - r0 * S] = v;
+                continue;
+            }
+            const int s = rec.x / S;
+            M[rec.x] = v;
             // consecutive cells mostly share a row: one atomic per row and warp
             const unsigned act = __activemask();
             const unsigned same = __match_any_sync(act, s);
@@ -343,6 +391,41 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
                 atomicMax(&smax[s - r0], rowmax);
                 atomicMax(&smin[s - r0], rowminc);
             }
+        }
+        if (tile) {
+            __syncthreads();
+            // one warp per row (entries are >= 0, so their bit patterns order like the values)
+            for (int r = warp; r < nrow; r += nthr >> 5) {
+                const float *src = mt + r * S;
+                float *dst = M + (size_t)(r0 + r) * S;
+                unsigned mx = 0u, mnc = 0u;
+                auto see = [&](float v) {
+                    const unsigned b = (unsigned)__float_as_int(v);
+                    mx = max(mx, b);
+                    if (v > 0.0f) mnc = max(mnc, 0x7fffffffu - b);
+                };
+                if (tile == 2) {  // S % 4 == 0 and M_t 16-byte aligned: float4 rows
+                    for (int j = 4 * lane; j < S; j += 128) {
+                        const float4 v = *reinterpret_cast<const float4 *>(src + j);
+                        *reinterpret_cast<float4 *>(dst + j) = v;
+                        see(v.x); see(v.y); see(v.z); see(v.w);
+                    }
+                } else {
+                    for (int j = lane; j < S; j += 32) {
+                        const float v = src[j];
+                        dst[j] = v;
+                        see(v);
+                    }
+                }
+                mx = __reduce_max_sync(0xffffffffu, mx);
+                mnc = __reduce_max_sync(0xffffffffu, mnc);
+                if (lane == 0) {
+                    rho[pos * S + r0 + r] = 0;
+                    if (rmax) rmax[pos * S + r0 + r] = (int)mx;
+                    if (rminc) rminc[pos * S + r0 + r] = (int)mnc;
+                }
+            }
+            return;
         }
     } else {
         for (int i = tid; i < r1 - r0; i += nthr) { smax[i] = 0; smin[i] = 0; }
@@ -1778,13 +1861,22 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     const int threads = std::min(32 * FA_RW_WARPS, std::max(256, 32 * max_units));
     // the staged chunk, whose space takes the units' run totals and the row maxima and minima
     // at the end, then one run-slot array per warp
-    const int tot_floats = (int)std::max((size_t)((a->chunk_tokens + FA_PAD_SLOTS + 3) & ~3),
-                                         (size_t)max_units * FA_UNIT_SLOTS + 2 * (size_t)a->part_max_rows[p]);
-    const size_t smem = sizeof(float) * ((size_t)tot_floats + (size_t)(threads / 32) * FA_UNIT_SLOTS);
+    int tot_floats = (int)std::max((size_t)((a->chunk_tokens + FA_PAD_SLOTS + 3) & ~3),
+                                   (size_t)max_units * FA_UNIT_SLOTS + 2 * (size_t)a->part_max_rows[p]);
+    // the rows of M_t are assembled in shared memory when the largest block's totals and rows
+    // fit beside the chunk without costing the second block per SM (227 KB per block, 228 KB
+    // per SM with 1 KB reserved per block)
+    const long per_block_floats = (233472L / 2 - 1024) / 4 - (long)(threads / 32) * FA_UNIT_SLOTS - 32;
+    int tile = 0;
+    if ((long)a->part_tile_floats[p] <= std::max<long>(tot_floats, per_block_floats)) {
+        tot_floats = std::max(tot_floats, (int)((a->part_tile_floats[p] + 3) & ~3L));
+        tile = ((a->S & 3) == 0 && (reinterpret_cast<uintptr_t>(mant) & 15) == 0) ? 2 : 1;
+    }
+    const size_t smem = sizeof(float) * ((size_t)tot_floats + (size_t)(threads / 32) * FA_UNIT_SLOTS + 32);
     // units per warp: the register totals of a third unit cost the smaller layouts ~10%
     const int upw = (max_units + FA_RW_WARPS - 1) / FA_RW_WARPS;
     using K = void (*)(DevFA, int, const float *, const int32_t *, const int4 *, int, int, float *, int32_t *, int32_t *,
-                       int32_t *, int32_t *, long);
+                       int32_t *, int32_t *, long, int);
     K kern = upw <= 1 ? (use_max ? (K)k_reweight<true, 1> : (K)k_reweight<false, 1>)
              : upw == 2 ? (use_max ? (K)k_reweight<true, 2> : (K)k_reweight<false, 2>)
                         : (use_max ? (K)k_reweight<true, 3> : (K)k_reweight<false, 3>);
@@ -1794,7 +1886,7 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     }
     dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
     kern<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, tot_floats, mant, rho, rmax, rminc,
-                                      zero, n_zero);
+                                      zero, n_zero, tile);
     return launch_check("reweight");
 }
 

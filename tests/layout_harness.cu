@@ -3,8 +3,8 @@
 // over the entry streams on the CPU (run sums per chunk, run ends, slot folding, per-cell
 // combination) for random probabilities, and compares every cell with a float64 sum of
 // its tokens.  It also checks the layout's invariants: every row and cell covered once per
-// partition, run ends only at group ends, no lane above FA_RUN_SLOTS runs, indices inside
-// their chunk.  Prints one line "bad=N ..." and exits non-zero when N > 0.
+// partition, run-end flags only on a group's first entry, no lane above FA_RUN_SLOTS runs,
+// indices inside their chunk or its zero pad slots.  Prints one line "bad=N ..." and exits non-zero when N > 0.
 #include "../constrained_decoding_diffusion_gb300/csrc/fa_compile.cu"
 
 #include <cmath>
@@ -85,21 +85,26 @@ int main(int argc, char **argv) {
                     for (int l = 0; l < 32; ++l) {
                         float acc = 0.0f;
                         int j = 0;
-                        for (int k = 0; k < ng; ++k)
+                        for (int k = 0; k < ng; ++k) {
+                            bool end = false;
                             for (int h = 0; h < G; ++h) {
                                 const uint32_t e = rl.ru_tok[((size_t)gb + (size_t)k * 32 + l) * G + h];
+                                if (e & FA_RUN_END) {
+                                    if (h != 0) ++bad;                // the flag sits on a group's first entry
+                                    end = true;
+                                }
                                 const int idx = e & 0x7fff;
                                 if (idx >= CH + FA_PAD_SLOTS || (idx < CH && idx >= n)) { ++bad; continue; }
                                 acc += sp[idx];
                                 ++entries;
-                                if (e & FA_RUN_END) {
-                                    if (h != G - 1) ++bad;            // run ends only at group ends
-                                    if (j >= FA_RUN_SLOTS) { ++bad; continue; }
-                                    slot[(size_t)j * 32 + l] = acc;   // the chunk's run sum
-                                    acc = 0.0f;
-                                    ++j;
-                                }
                             }
+                            if (end) {                                // the group ends the lane's run
+                                if (j >= FA_RUN_SLOTS) { ++bad; continue; }
+                                slot[(size_t)j * 32 + l] = acc;       // the chunk's run sum
+                                acc = 0.0f;
+                                ++j;
+                            }
+                        }
                     }
                     for (size_t q = 0; q < slot.size(); ++q) tot[(size_t)w * FA_UNIT_SLOTS + q] += slot[q];
                 }
