@@ -282,6 +282,22 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
             for (int q = 0; q < FA_RUN_SLOTS; ++q) tot[h][q] = 0.0f;
         for (int ch = 0; ch < nch; ++ch) {
             const int base = ch * CH, n = min(CH, fa.V - base);
+            // the warp's units' stream bounds for this chunk and the first unit's first four
+            // groups, loaded before the staging so that their latency overlaps it
+            int gbv[UPW], ngv[UPW];
+#pragma unroll
+            for (int h = 0; h < UPW; ++h) {
+                const int uw = warp + FA_RW_WARPS * h;
+                ngv[h] = -1;
+                gbv[h] = 0;
+                if (uw < nu) {
+                    const size_t ui = (size_t)(u0 + uw) * nch + ch;
+                    gbv[h] = __ldg(fa.ru_goff + ui);
+                    ngv[h] = (__ldg(fa.ru_goff + ui + 1) - gbv[h]) >> 5;
+                }
+            }
+            uint2 f0v = __ldg(g4 + gbv[0] + lane), f1v = __ldg(g4 + gbv[0] + lane + 32);
+            uint2 f2v = __ldg(g4 + gbv[0] + lane + 64), f3v = __ldg(g4 + gbv[0] + lane + 96);
             __syncthreads();  // every warp is done with the previous chunk
             if (aligned) {
                 // asynchronous 16-byte global->shared copies, all in flight before one wait
@@ -300,19 +316,21 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
             __syncthreads();
 #pragma unroll
             for (int h = 0; h < UPW; ++h) {
-                const int uw = warp + FA_RW_WARPS * h;
-                if (uw >= nu) break;
-                const size_t ui = (size_t)(u0 + uw) * nch + ch;
-                const int gb = __ldg(fa.ru_goff + ui);
-                const int ng = (__ldg(fa.ru_goff + ui + 1) - gb) >> 5;
-                const uint2 *gp = g4 + gb + lane;
+                const int ng = ngv[h];
+                if (ng < 0) break;
+                const uint2 *gp = g4 + gbv[h] + lane;
                 float acc = 0.0f;
                 uint32_t slot_addr = my_addr;  // shared address of the current run's slot
                 const uint32_t cbase = (uint32_t)__cvta_generic_to_shared(smem_f);
                 // whole steps of four groups (their sixteen gathers first, then the run-end
                 // stores), the next four loaded (unconditionally: the stream array is padded
                 // past its end) while these are summed; then the tail
-                uint2 c0v = __ldg(gp), c1v = __ldg(gp + 32), c2v = __ldg(gp + 64), c3v = __ldg(gp + 96);
+                uint2 c0v, c1v, c2v, c3v;
+                if (h == 0) {
+                    c0v = f0v; c1v = f1v; c2v = f2v; c3v = f3v;
+                } else {
+                    c0v = __ldg(gp); c1v = __ldg(gp + 32); c2v = __ldg(gp + 64); c3v = __ldg(gp + 96);
+                }
                 int k = 0;
                 for (; k + 4 <= ng; k += 4) {
                     gp += 128;
@@ -334,10 +352,8 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
                 // others may hold the sums of the warp's other unit); every lane reads only its
                 // own slots
                 const int mine = (int)((slot_addr - my_addr) >> 7);
-                const int nrun = __reduce_max_sync(0xffffffffu, mine);
 #pragma unroll
                 for (int q = 0; q < FA_RUN_SLOTS; ++q) {
-                    if (q >= nrun) break;
                     const float sv = q < mine ? my[q * 32] : 0.0f;
                     if constexpr (MAX) tot[h][q] = fmaxf(tot[h][q], sv); else tot[h][q] += sv;
                 }
