@@ -864,7 +864,7 @@ struct TopdownArgs {
     int nA, nB;           // number of alpha and beta blocks
     int CB, QS;           // alpha: columns per block, row splits
     const float *mant;    // level-k spans
-    const int32_t *rho;
+    const int32_t *rho, *rmax;
     uint64_t seed, offset;
     int32_t *z, *status;
     float *am, *bm;
@@ -912,6 +912,28 @@ __device__ void topdown_midpoint(const TopdownArgs &a, int blk) {
     }
 }
 
+// Messages: one scaled pass, the exact two-pass form where it is needed.  Every term of a
+// message entry is alpha_l(q) A(q, col) (beta: A(row, q) beta_r(q)), each with its own
+// exponent.  The fast pass scales all terms by one power of two, chosen so that the largest
+// term any row can give is at most about 4, and keeps the plain fp32 sum when that sum is
+// at least 2^-60: the terms that lose precision below the fp32 normal range then add at
+// most |S| 2^-126, under 2^-57 of the sum.  A second sum with every scale set to 1 tells an
+// exactly zero entry apart (the terms are non-negative, so a positive one never cancels).
+// Any other entry -- a state whose weight is far below the largest, such as one a committed
+// token reaches only through rare tokens -- takes the exact form: the largest term's
+// exponent first, then the sum scaled by it, so no state is lost to range.
+constexpr float kMsgFastMin = 8.6736174e-19f;  // 2^-60
+
+__device__ __forceinline__ int fa_block_max_int(int v, int *red) {
+    v = fa_warp_max_int(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int r = red[0];
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = max(r, red[i]);
+    __syncthreads();
+    return r;
+}
+
 __device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
     const int S = a.S, L = a.L, k = a.k, CB = a.CB, QS = a.QS;
     const int ncb = (S + CB - 1) / CB;
@@ -922,17 +944,75 @@ __device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
     if (m >= L) return;
     float *sa = sm;                          // [S] mantissas of alpha_l
     int *sc = (int *)(sa + S);               // [S] alpha exponent + row exponent of A[l, m)
-    int *pe = sc + S;                        // [QS * CB] partial max exponents
+    float *sf = (float *)(sc + S);           // [S] fast-pass row factors alpha_l(q) 2^(rho(q) - R)
+    float *sz = sf + S;                      // [S] 1 where alpha_l(q) > 0
+    int *pe = (int *)(sz + S);               // [QS * CB] partial max exponents
     float *ps = (float *)(pe + QS * CB);     // [QS * CB] partial sums
+    __shared__ int red[kWarps];
+    __shared__ int need_exact;
     const size_t lnode = (size_t)b * a.nc + 2 * j;
     const size_t bl = ((size_t)b * (L + 1) + l) * S, bmid = ((size_t)b * (L + 1) + m) * S;
-    const int32_t *rho = a.rho + lnode * S;
-    for (int q = threadIdx.x; q < S; q += kThreads) { sa[q] = a.am[bl + q]; sc[q] = a.ae[bl + q] + rho[q]; }
+    const int32_t *rho = a.rho + lnode * S, *rmx = a.rmax + lnode * S;
+    // R: the exponent of the largest term any row can give (row maxima as bit patterns)
+    int w = FA_INT_NONE;
+    for (int q = threadIdx.x; q < S; q += kThreads) {
+        const float x = a.am[bl + q];
+        const int e = a.ae[bl + q] + rho[q], rb = rmx[q];
+        sa[q] = x;
+        sc[q] = e;
+        if (x > 0.0f && rb > 0) w = max(w, e + fa_exponent(x) + max(-126, fa_exponent(__int_as_float(rb))));
+    }
+    if (threadIdx.x == 0) need_exact = 0;
+    const int R = fa_block_max_int(w, red);
+    for (int q = threadIdx.x; q < S; q += kThreads) {
+        sf[q] = (sa[q] > 0.0f && R != FA_INT_NONE) ? fa_mul_pow2(sa[q], sc[q] - R) : 0.0f;
+        sz[q] = sa[q] > 0.0f ? 1.0f : 0.0f;
+    }
     __syncthreads();
     const int c = threadIdx.x % CB, qs = threadIdx.x / CB;
     const int col = cbk * CB + c;
     const float *A = a.mant + lnode * (size_t)S * S;
     constexpr int U = 16;  // loads issued together
+    float sum = 0.0f, sum1 = 0.0f;
+    if (col < S)
+        for (int q0 = qs; q0 < S; q0 += U * QS) {
+            float v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + u * QS;
+                v[u] = q < S ? __ldg(A + (size_t)q * S + col) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = min(q0 + u * QS, S - 1);
+                sum = fmaf(sf[q], v[u], sum);
+                sum1 = fmaf(sz[q], v[u], sum1);
+            }
+        }
+    ps[qs * CB + c] = sum;
+    reinterpret_cast<float *>(pe)[qs * CB + c] = sum1;
+    __syncthreads();
+    bool exact_col = false;
+    if (qs == 0 && col < S) {
+        float tot = 0.0f, tot1 = 0.0f;
+        for (int t = 0; t < QS; ++t) { tot += ps[t * CB + c]; tot1 += reinterpret_cast<float *>(pe)[t * CB + c]; }
+        if (!(tot1 > 0.0f)) {
+            a.am[bmid + col] = 0.0f;
+            a.ae[bmid + col] = 0;
+        } else if (tot >= kMsgFastMin && tot <= 3.0e38f) {
+            float mo;
+            int eo;
+            fa_split(tot, mo, eo);
+            a.am[bmid + col] = mo;
+            a.ae[bmid + col] = eo + R;
+        } else {
+            exact_col = true;
+            need_exact = 1;
+        }
+    }
+    __syncthreads();
+    if (!need_exact) return;
+    // the exact form for the block's columns (written only where the fast pass gave up)
     int e = FA_INT_NONE;
     if (col < S)
         for (int q0 = qs; q0 < S; q0 += U * QS) {
@@ -945,14 +1025,14 @@ __device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int q = q0 + u * QS;
-                if (v[u] > 0.0f && sa[q] > 0.0f) e = max(e, sc[q] + fa_exponent(v[u]));
+                if (v[u] > 0.0f && q < S && sa[q] > 0.0f) e = max(e, sc[q] + fa_exponent(v[u]));
             }
         }
     pe[qs * CB + c] = e;
     __syncthreads();
     int E = FA_INT_NONE;
     for (int t = 0; t < QS; ++t) E = max(E, pe[t * CB + c]);
-    float sum = 0.0f;
+    float esum = 0.0f;
     if (col < S && E != FA_INT_NONE)
         for (int q0 = qs; q0 < S; q0 += U * QS) {
             float v[U];
@@ -964,17 +1044,17 @@ __device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int q = q0 + u * QS;
-                if (v[u] > 0.0f && sa[q] > 0.0f) {
+                if (v[u] > 0.0f && q < S && sa[q] > 0.0f) {
                     float mv;
                     int ev;
                     fa_split(v[u], mv, ev);
-                    sum += sa[q] * mv * fa_pow2(sc[q] + ev - E);
+                    esum += sa[q] * mv * fa_pow2(sc[q] + ev - E);
                 }
             }
         }
-    ps[qs * CB + c] = sum;
+    ps[qs * CB + c] = esum;
     __syncthreads();
-    if (qs == 0 && col < S) {
+    if (exact_col) {
         float tot = 0.0f;
         for (int t = 0; t < QS; ++t) tot += ps[t * CB + c];
         float mo = 0.0f;
@@ -994,22 +1074,76 @@ __device__ void topdown_beta(const TopdownArgs &a, int blk, float *sm) {
     const int l = j << (k + 1), m = l + (1 << k);
     if (m >= L) return;
     const int r = min(l + (1 << (k + 1)), L);
-    float *sb = sm;
-    int *se = (int *)(sb + S);
+    float *sb = sm;                  // [S] mantissas of beta_r
+    int *se = (int *)(sb + S);       // [S] their exponents
+    float *sg = (float *)(se + S);   // [S] fast-pass factors beta_r(q) 2^-R
+    float *sz = sg + S;              // [S] 1 where beta_r(q) > 0
+    __shared__ int red[kWarps];
     const size_t br = ((size_t)b * (L + 1) + r) * S, bmid = ((size_t)b * (L + 1) + m) * S;
-    for (int q = threadIdx.x; q < S; q += kThreads) { sb[q] = a.bm[br + q]; se[q] = a.be[br + q]; }
+    int w = FA_INT_NONE;
+    for (int q = threadIdx.x; q < S; q += kThreads) {
+        const float x = a.bm[br + q];
+        const int e = a.be[br + q];
+        sb[q] = x;
+        se[q] = e;
+        if (x > 0.0f) w = max(w, e + fa_exponent(x));
+    }
+    const int R = fa_block_max_int(w, red);
+    for (int q = threadIdx.x; q < S; q += kThreads) {
+        sg[q] = (sb[q] > 0.0f && R != FA_INT_NONE) ? fa_mul_pow2(sb[q], se[q] - R) : 0.0f;
+        sz[q] = sb[q] > 0.0f ? 1.0f : 0.0f;
+    }
     __syncthreads();
     const int row = rbk * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= S) return;
     const size_t rnode = (size_t)b * a.nc + 2 * j + 1;
     const float *Rrow = a.mant + rnode * (size_t)S * S + (size_t)row * S;
+    // the row's entries scaled by its largest (their exponents then stay near 0)
+    const int rb = a.rmax[rnode * S + row];
+    const int er = min(126, max(-126, fa_exponent(__int_as_float(rb))));
+    const float rs = __int_as_float((127 - er) << 23);   // 2^-er
+    float sum = 0.0f, sum1 = 0.0f;
+    if (rb > 0) {
+        constexpr int U = 8;
+        for (int q0 = lane; q0 < S; q0 += 32 * U) {
+            float v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + 32 * u;
+                v[u] = q < S ? __ldg(Rrow + q) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = min(q0 + 32 * u, S - 1);
+                sum = fmaf(v[u] * rs, sg[q], sum);
+                sum1 = fmaf(v[u], sz[q], sum1);
+            }
+        }
+    }
+    sum = fa_warp_sum(sum);
+    sum1 = fa_warp_sum(sum1);
+    if (!(sum1 > 0.0f)) {
+        if (lane == 0) { a.bm[bmid + row] = 0.0f; a.be[bmid + row] = 0; }
+        return;
+    }
+    if (sum >= kMsgFastMin && sum <= 3.0e38f) {
+        if (lane == 0) {
+            float mo;
+            int eo;
+            fa_split(sum, mo, eo);
+            a.bm[bmid + row] = mo;
+            a.be[bmid + row] = eo + R + er + a.rho[rnode * S + row];
+        }
+        return;
+    }
+    // the exact form for this row
     int e = FA_INT_NONE;
     for (int q = lane; q < S; q += 32) {
         const float v = Rrow[q];
         if (v > 0.0f && sb[q] > 0.0f) e = max(e, se[q] + fa_exponent(v));
     }
     e = fa_warp_max_int(e);
-    float sum = 0.0f;
+    float esum = 0.0f;
     if (e != FA_INT_NONE)
         for (int q = lane; q < S; q += 32) {
             const float v = Rrow[q];
@@ -1017,14 +1151,14 @@ __device__ void topdown_beta(const TopdownArgs &a, int blk, float *sm) {
                 float mv;
                 int ev;
                 fa_split(v, mv, ev);
-                sum += sb[q] * mv * fa_pow2(se[q] + ev - e);
+                esum += sb[q] * mv * fa_pow2(se[q] + ev - e);
             }
         }
-    sum = fa_warp_sum(sum);
+    esum = fa_warp_sum(esum);
     if (lane == 0) {
         float mo = 0.0f;
         int eo = 0;
-        if (sum > 0.0f) { fa_split(sum, mo, eo); eo += e + a.rho[rnode * S + row]; }
+        if (esum > 0.0f) { fa_split(esum, mo, eo); eo += e + a.rho[rnode * S + row]; }
         a.bm[bmid + row] = mo;
         a.be[bmid + row] = eo;
     }
@@ -2191,11 +2325,15 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
         ta.nA = B * ta.np * ((S + ta.CB - 1) / ta.CB);
         ta.nB = B * ta.np * ((S + kWarps - 1) / kWarps);
         const int nM = (B * ta.np + kWarps - 1) / kWarps;
-        ta.mant = F(p.mant[kk]); ta.rho = I(p.rho[kk]);
+        ta.mant = F(p.mant[kk]); ta.rho = I(p.rho[kk]); ta.rmax = I(p.rmax[kk]);
         ta.seed = philox_seed; ta.offset = philox_offset;
         ta.z = I(p.z); ta.status = row_status;
         ta.am = F(p.am); ta.ae = I(p.ae); ta.bm = F(p.bm); ta.be = I(p.be);
-        const size_t smem = (size_t)S * 8 + (size_t)kThreads * 8;
+        const size_t smem = (size_t)S * 16 + (size_t)kThreads * 8;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(k_topdown, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) { fa_set_error(std::string("top-down smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+        }
         k_topdown<<<(unsigned)(ta.nA + ta.nB + nM), kThreads, smem, s>>>(ta);
         if ((st = launch_check("top-down level")) != FA_OK) return st;
     }
