@@ -413,3 +413,43 @@ def test_sequence_results_do_not_depend_on_the_batch(native):
     o = oracle.OracleFA(fa)
     check_against_oracle(fa, o, probs[:16], committed[:16], part, 5, rows=[0, 7, 15])
     check_against_oracle(fa, o, probs, committed, whole, 5, rows=[16])
+
+
+def rare_start_rare_end_fa(n_states: int):
+    """State 0 starts; token 0 leads to state 1 and tokens 1-6 to state 2; states 1 and 2 loop
+    on every token; state 1 accepts, and state 2 reaches the accepting state 3 only by token 7.
+    States 4.. have no edges (they only widen the matrices to the SIMT and tensor-core
+    span paths)."""
+    from constrained_decoding_diffusion_gb300.synth import _from_edge_lists
+    V = 8
+    edges = [(0, 1, np.array([0])), (0, 2, np.arange(1, 7)), (1, 1, np.arange(V)), (2, 2, np.arange(V)),
+             (2, 3, np.array([7]))]
+    return _from_edge_lists(n_states, 0, [1, 3], edges, V)
+
+
+@pytest.mark.parametrize("S", [4, 100, 200])
+def test_messages_keep_states_far_below_the_largest(native, S):
+    """p(token 0) = 1e-30 at the first position and p(token 7) = 1e-30 at the last: the two
+    accepting paths (a rare start into state 1, a rare end out of state 2) weigh about the
+    same, while state 1's forward message and state 2's backward message lie about 2^-100
+    below the largest entries of theirs, and state 2's forward weight is the dead end's only
+    rival.  Such entries need the exact form of the message products: the step matches the
+    oracle on logZ and the marginals, and 64 draws take the rare start at the oracle's rate."""
+    fa = rare_start_rare_end_fa(S)
+    o = oracle.OracleFA(fa)
+    aut = native.fa_compile(fa)
+    B, L, V = 64, 24, 8
+    rng = np.random.default_rng(S)
+    row = synth.gaussian_probs(rng, 1, L, V, 1.0)[0]
+    row[0, 0] = 1e-30
+    row[L - 1, 7] = 1e-30
+    probs = np.ascontiguousarray(np.broadcast_to(row, (B, L, V)), dtype=np.float32)
+    committed = np.full((B, L), -1, np.int32)
+    res = run_step(aut, probs, committed, seed=11, offset=0, k=4)
+    assert (res["status"] == 0).all()
+    check_against_oracle(fa, o, probs, committed, res, 4, rows=range(8))
+    tok0 = np.zeros(L, np.int32)
+    p_a = float(o.posterior(row, committed[0], tokens=tok0)["marg_tokens"][0])  # P(x_0 = token 0)
+    assert 0.2 < p_a < 0.8, p_a
+    n_a = int((res["tokens"][:, 0] == 0).sum())
+    assert abs(n_a - B * p_a) <= 4.5 * math.sqrt(B * p_a * (1 - p_a)), (n_a, B * p_a)
