@@ -865,6 +865,7 @@ struct TopdownArgs {
     int CB, QS;           // alpha: columns per block, row splits
     const float *mant;    // level-k spans
     const int32_t *rho, *rmax;
+    int vec4;             // |S| % 4 == 0: 16-byte loads in the message passes
     uint64_t seed, offset;
     int32_t *z, *status;
     float *am, *bm;
@@ -946,8 +947,9 @@ __device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
     int *sc = (int *)(sa + S);               // [S] alpha exponent + row exponent of A[l, m)
     float *sf = (float *)(sc + S);           // [S] fast-pass row factors alpha_l(q) 2^(rho(q) - R)
     float *sz = sf + S;                      // [S] 1 where alpha_l(q) > 0
-    int *pe = (int *)(sz + S);               // [QS * CB] partial max exponents
-    float *ps = (float *)(pe + QS * CB);     // [QS * CB] partial sums
+    int *pe = (int *)(sz + S);               // [QS * CB] partial max exponents (exact form)
+    float *ps = (float *)(pe + QS * CB);     // [QS * CB] partial sums (exact form)
+    // (the fast pass uses [pe, pe + 8 kThreads) for its partial sums first)
     __shared__ int red[kWarps];
     __shared__ int need_exact;
     const size_t lnode = (size_t)b * a.nc + 2 * j;
@@ -973,29 +975,60 @@ __device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
     const int col = cbk * CB + c;
     const float *A = a.mant + lnode * (size_t)S * S;
     constexpr int U = 16;  // loads issued together
-    float sum = 0.0f, sum1 = 0.0f;
-    if (col < S)
-        for (int q0 = qs; q0 < S; q0 += U * QS) {
-            float v[U];
+    // fast pass partial sums: [nsplit][CB] each (sums, then the exact-zero sums)
+    float *fs = reinterpret_cast<float *>(pe), *fz = fs + kThreads * 4;
+    int nsplit = QS;
+    if (a.vec4 && CB == 64) {
+        // |S| % 4 == 0: 16 four-column groups x 16 row splits, 16-byte loads
+        nsplit = kThreads / 16;
+        const int c4 = threadIdx.x & 15, rs = threadIdx.x >> 4, col4 = cbk * CB + 4 * c4;
+        float4 sm4 = make_float4(0.f, 0.f, 0.f, 0.f), sz4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        constexpr int U4 = 8;
+        if (col4 < S)
+            for (int q0 = rs; q0 < S; q0 += U4 * 16) {
+                float4 v[U4];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int q = q0 + u * QS;
-                v[u] = q < S ? __ldg(A + (size_t)q * S + col) : 0.0f;
-            }
+                for (int u = 0; u < U4; ++u) {
+                    const int q = q0 + 16 * u;
+                    v[u] = q < S ? __ldg(reinterpret_cast<const float4 *>(A + (size_t)q * S + col4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int q = min(q0 + u * QS, S - 1);
-                sum = fmaf(sf[q], v[u], sum);
-                sum1 = fmaf(sz[q], v[u], sum1);
+                for (int u = 0; u < U4; ++u) {
+                    const int q = min(q0 + 16 * u, S - 1);
+                    const float f = sf[q], z = sz[q];
+                    sm4.x = fmaf(f, v[u].x, sm4.x); sm4.y = fmaf(f, v[u].y, sm4.y);
+                    sm4.z = fmaf(f, v[u].z, sm4.z); sm4.w = fmaf(f, v[u].w, sm4.w);
+                    sz4.x = fmaf(z, v[u].x, sz4.x); sz4.y = fmaf(z, v[u].y, sz4.y);
+                    sz4.z = fmaf(z, v[u].z, sz4.z); sz4.w = fmaf(z, v[u].w, sz4.w);
+                }
             }
-        }
-    ps[qs * CB + c] = sum;
-    reinterpret_cast<float *>(pe)[qs * CB + c] = sum1;
+        *reinterpret_cast<float4 *>(fs + rs * CB + 4 * c4) = sm4;
+        *reinterpret_cast<float4 *>(fz + rs * CB + 4 * c4) = sz4;
+    } else {
+        float sum = 0.0f, sum1 = 0.0f;
+        if (col < S)
+            for (int q0 = qs; q0 < S; q0 += U * QS) {
+                float v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int q = q0 + u * QS;
+                    v[u] = q < S ? __ldg(A + (size_t)q * S + col) : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int q = min(q0 + u * QS, S - 1);
+                    sum = fmaf(sf[q], v[u], sum);
+                    sum1 = fmaf(sz[q], v[u], sum1);
+                }
+            }
+        fs[qs * CB + c] = sum;
+        fz[qs * CB + c] = sum1;
+    }
     __syncthreads();
     bool exact_col = false;
     if (qs == 0 && col < S) {
         float tot = 0.0f, tot1 = 0.0f;
-        for (int t = 0; t < QS; ++t) { tot += ps[t * CB + c]; tot1 += reinterpret_cast<float *>(pe)[t * CB + c]; }
+        for (int t = 0; t < nsplit; ++t) { tot += fs[t * CB + c]; tot1 += fz[t * CB + c]; }
         if (!(tot1 > 0.0f)) {
             a.am[bmid + col] = 0.0f;
             a.ae[bmid + col] = 0;
@@ -1103,7 +1136,26 @@ __device__ void topdown_beta(const TopdownArgs &a, int blk, float *sm) {
     const int er = min(126, max(-126, fa_exponent(__int_as_float(rb))));
     const float rs = __int_as_float((127 - er) << 23);   // 2^-er
     float sum = 0.0f, sum1 = 0.0f;
-    if (rb > 0) {
+    if (rb > 0 && a.vec4) {
+        constexpr int U4 = 4;  // 16-byte loads issued together
+        for (int q0 = 4 * lane; q0 < S; q0 += 128 * U4) {
+            float4 v[U4];
+#pragma unroll
+            for (int u = 0; u < U4; ++u) {
+                const int q = q0 + 128 * u;
+                v[u] = q < S ? __ldg(reinterpret_cast<const float4 *>(Rrow + q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U4; ++u) {
+                const int q = min(q0 + 128 * u, S - 4);
+                const float4 g = *reinterpret_cast<const float4 *>(sg + q), z = *reinterpret_cast<const float4 *>(sz + q);
+                sum = fmaf(v[u].x * rs, g.x, sum); sum = fmaf(v[u].y * rs, g.y, sum);
+                sum = fmaf(v[u].z * rs, g.z, sum); sum = fmaf(v[u].w * rs, g.w, sum);
+                sum1 = fmaf(v[u].x, z.x, sum1); sum1 = fmaf(v[u].y, z.y, sum1);
+                sum1 = fmaf(v[u].z, z.z, sum1); sum1 = fmaf(v[u].w, z.w, sum1);
+            }
+        }
+    } else if (rb > 0) {
         constexpr int U = 8;
         for (int q0 = lane; q0 < S; q0 += 32 * U) {
             float v[U];
@@ -2289,18 +2341,19 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
             if ((st = launch_check("span product (small)")) != FA_OK) return st;
             continue;
         }
-        dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
-        k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
-                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
-        if ((st = launch_check("rowshift")) != FA_OK) return st;
         if (fa_span_tc_supported(S)) {
-            g_launches.fetch_add(2, std::memory_order_relaxed);
+            // the row shift is computed by the left operand images (three launches per level)
+            g_launches.fetch_add(3, std::memory_order_relaxed);
             st = fa_span_tc_level(S, B, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
                                   I(p.rminc[kk - 1]), p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]),
                                   I(p.rmax[kk]), I(p.rminc[kk]), I(p.tc_err), I(p.range_lost), ws + p.img, s);
             if (st != FA_OK) return st;
             continue;
         }
+        dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
+        k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
+                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
+        if ((st = launch_check("rowshift")) != FA_OK) return st;
         const long tiles = (S + GBN - 1) / GBN;
         const long g2 = (long)B * p.nk[kk] * tiles * tiles;
         k_gemm_simt<false><<<(unsigned)g2, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
@@ -2326,10 +2379,11 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
         ta.nB = B * ta.np * ((S + kWarps - 1) / kWarps);
         const int nM = (B * ta.np + kWarps - 1) / kWarps;
         ta.mant = F(p.mant[kk]); ta.rho = I(p.rho[kk]); ta.rmax = I(p.rmax[kk]);
+        ta.vec4 = (S & 3) == 0;
         ta.seed = philox_seed; ta.offset = philox_offset;
         ta.z = I(p.z); ta.status = row_status;
         ta.am = F(p.am); ta.ae = I(p.ae); ta.bm = F(p.bm); ta.be = I(p.be);
-        const size_t smem = (size_t)S * 16 + (size_t)kThreads * 8;
+        const size_t smem = (size_t)S * 16 + (size_t)kThreads * 32;
         if (smem > 48 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(k_topdown, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) { fa_set_error(std::string("top-down smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
