@@ -1247,6 +1247,7 @@ struct LeafShared {
     float wsum[kLeafWarps];
     float xm;
     int xe;
+    int ra, rb;   // the scales of the normaliser's fast pass
     int cell, pick_thread, last_thread, v, ok;
     int last;
 };
@@ -1316,11 +1317,37 @@ __device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float 
     // the cell z_{t-1} -> z_t (one pass over the source's cells) and the two messages
     const float *a_m = am + ba, *b_m = bm + bb;
     const int32_t *a_e = ae + ba, *b_e = be + bb;
+    // staged: the messages, and for the normaliser's fast pass the messages scaled by one
+    // power of two each (alpha_{t-1}(s) 2^-Ra, beta_t(d) 2^-Rb, at most 2)
+    float *sa2 = nullptr, *sb2 = nullptr;
     if (stage) {
         float *sam = stage, *sbm = stage + S;
         int32_t *sae = (int32_t *)(stage + 2 * S), *sbe = (int32_t *)(stage + 3 * S);
+        sa2 = stage + 4 * S;
+        sb2 = stage + 5 * S;
+        int ra = FA_INT_NONE, rb = FA_INT_NONE;
         for (int s = tid; s < S; s += kLeafThreads) {
-            sam[s] = a_m[s]; sae[s] = a_e[s]; sbm[s] = b_m[s]; sbe[s] = b_e[s];
+            const float x = a_m[s], y = b_m[s];
+            const int ex = a_e[s], ey = b_e[s];
+            sam[s] = x; sae[s] = ex; sbm[s] = y; sbe[s] = ey;
+            if (x > 0.0f) ra = max(ra, ex + fa_exponent(x));
+            if (y > 0.0f) rb = max(rb, ey + fa_exponent(y));
+        }
+        ra = fa_warp_max_int(ra);
+        rb = fa_warp_max_int(rb);
+        if ((tid & 31) == 0) { sh.we[tid >> 5] = ra; reinterpret_cast<int *>(sh.wsum)[tid >> 5] = rb; }
+        __syncthreads();
+        if (tid == 0) {
+            int A = FA_INT_NONE, Bv = FA_INT_NONE;
+            for (int i = 0; i < kLeafWarps; ++i) { A = max(A, sh.we[i]); Bv = max(Bv, reinterpret_cast<int *>(sh.wsum)[i]); }
+            sh.ra = A;
+            sh.rb = Bv;
+        }
+        __syncthreads();
+        const int RA = sh.ra, RB = sh.rb;
+        for (int s = tid; s < S; s += kLeafThreads) {
+            sa2[s] = (sam[s] > 0.0f && RA != FA_INT_NONE) ? fa_mul_pow2(sam[s], sae[s] - RA) : 0.0f;
+            sb2[s] = (sbm[s] > 0.0f && RB != FA_INT_NONE) ? fa_mul_pow2(sbm[s], sbe[s] - RB) : 0.0f;
         }
         a_m = sam; b_m = sbm; a_e = sae; b_e = sbe;
     }
@@ -1355,7 +1382,43 @@ __device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float 
             dx.add(a * bv * mm, ea + b_e[d] + em);
         }
     };
-    if ((long)fa.n_cells * 4 >= (long)S * S && (S & 3) == 0 && (reinterpret_cast<uintptr_t>(Mt) & 15) == 0) {
+    const bool dense = (long)fa.n_cells * 4 >= (long)S * S && (S & 3) == 0 && (reinterpret_cast<uintptr_t>(Mt) & 15) == 0;
+    // fast pass of a dense normaliser: plain fp32 sum of sa2(s) M_t(s, d) sb2(d) (terms at most
+    // 4), kept when it is at least 2^-60 (the terms lost below the fp32 normal range then add
+    // under 2^-57 of it); otherwise the exact form below
+    bool exact_den = true;
+    float den_m = 0.0f;
+    int den_e = 0;
+    if (dense && sa2) {
+        const int S4 = S >> 2, n4 = S * S4;
+        const int dr = kLeafThreads / S4, dc = kLeafThreads % S4;
+        int r = tid / S4, c4 = tid % S4;
+        const float4 *M4 = reinterpret_cast<const float4 *>(Mt);
+        float fsum = 0.0f;
+#pragma unroll 8
+        for (int i = tid; i < n4; i += kLeafThreads) {
+            const float4 mv = __ldg(M4 + i);
+            const float4 bv = *reinterpret_cast<const float4 *>(sb2 + 4 * c4);
+            fsum = fmaf(sa2[r], mv.x * bv.x + mv.y * bv.y + mv.z * bv.z + mv.w * bv.w, fsum);
+            r += dr;
+            c4 += dc;
+            if (c4 >= S4) { c4 -= S4; ++r; }
+        }
+        fsum = fa_warp_sum(fsum);
+        __syncthreads();   // the scale reductions above are read
+        if ((tid & 31) == 0) sh.wsum[tid >> 5] = fsum;
+        __syncthreads();
+        float D = 0.0f;
+        for (int i = 0; i < kLeafWarps; ++i) D += sh.wsum[i];
+        __syncthreads();
+        if (D >= 8.6736174e-19f && D <= 3.0e38f) {
+            exact_den = false;
+            fa_split(D, den_m, den_e);
+            den_e += sh.ra + sh.rb;
+        }
+    }
+    if (!exact_den) {
+    } else if (dense) {
         const int S4 = S >> 2, n4 = S * S4;
         const int dr = kLeafThreads / S4, dc = kLeafThreads % S4;
         int r = tid / S4, c4 = tid % S4;
@@ -1391,9 +1454,11 @@ __device__ bool leaf_position(const DevFA &fa, int b, int t, int L, const float 
 
     float total;
     const float incl = block_scan(own, sh, &total);
-    block_xacc(dx, sh);
-    const float den_m = sh.xm;
-    const int den_e = sh.xe;
+    if (exact_den) {
+        block_xacc(dx, sh);
+        den_m = sh.xm;
+        den_e = sh.xe;
+    }
     if (!(total > 0.0f)) {
         if (tid == 0) { status[b] = FA_ROW_UNDERFLOW; tokens[pos] = -1; marg[pos] = 0.0f; }
         return false;
@@ -2396,7 +2461,11 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
     //    the entropy of every position's full constrained distribution
     stage_mark(3, s);
     const bool entropies = confidence == FA_CONF_NEG_ENTROPY || entropy;
-    const size_t leaf_smem = S <= kLeafStageStates ? (size_t)S * 16 : 0;
+    const size_t leaf_smem = S <= kLeafStageStates ? (size_t)S * 24 : 0;
+    if (leaf_smem + sizeof(LeafShared) > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_leaf_commit, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)leaf_smem);
+        if (e != cudaSuccess) { fa_set_error(std::string("leaf smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    }
     k_leaf_commit<<<(unsigned)((long)B * L), kLeafThreads, leaf_smem, s>>>(
         dev_view(aut), B, L, probs, committed, philox_seed, philox_offset, I(p.z), F(p.am), I(p.ae), F(p.bm), I(p.be),
         tokens, marg, row_status, k, commit_lo, commit_hi, commit_idx, (unsigned long long *)(ws + p.keys),
