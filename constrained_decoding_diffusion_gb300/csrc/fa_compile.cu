@@ -536,7 +536,8 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
             cnt = std::max(cnt, tok_off[tok_perm[i] + 1] - tok_off[tok_perm[i]]);
         tok_goff[g + 1] = tok_goff[g] + cnt;
     }
-    std::vector<uint32_t> tok_sd((size_t)tok_goff[n_tg] * 32, FA_SD_NONE);
+    // padding (src, dst) = (S, S): the all-token pass keeps a zero message entry at index S
+    std::vector<uint32_t> tok_sd((size_t)tok_goff[n_tg] * 32, ((uint32_t)S << 16) | (uint32_t)S);
     for (int64_t i = 0; i < V; ++i) {
         const int64_t g = i / 32, lane = i % 32, v = tok_perm[i];
         for (int64_t k = 0; k < tok_off[v + 1] - tok_off[v]; ++k) {

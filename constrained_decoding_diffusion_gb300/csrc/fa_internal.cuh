@@ -33,7 +33,7 @@ struct fa_automaton {
     // (src << 16) | dst of every incidence, token-major: tokens in the order tok_perm (by
     // incidence count, ties by id), interleaved by groups of 32: row k of group g (rows
     // tok_goff[g] .. tok_goff[g + 1]) holds incidence k of token tok_perm[32 g + lane] at
-    // tok_sd[32 * row + lane], FA_SD_NONE past a token's count, so a warp reading one row
+    // tok_sd[32 * row + lane], (|S|, |S|) past a token's count, so a warp reading one row
     // reads 128 contiguous bytes
     uint32_t *tok_sd = nullptr;
     int64_t *tok_goff = nullptr;     // [ceil(V / 32) + 1]
@@ -84,7 +84,6 @@ void fa_set_error(const std::string &msg);
 #ifndef FA_REWEIGHT_MAX_CHUNK
 #define FA_REWEIGHT_MAX_CHUNK 24576  // tokens per staged vocabulary chunk
 #endif
-#define FA_SD_NONE 0xFFFFFFFFu       // tok_sd padding
 #define FA_RUN_END 0x8000u           // flag on a group's first entry: the group ends the lane's run
 #define FA_GROUP_ENTRIES 4           // entries per 8-byte group; runs end only at group ends
 #define FA_PAD_SLOTS 32              // zero slots after a staged chunk, one per shared-memory bank

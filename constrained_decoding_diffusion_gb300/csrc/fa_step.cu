@@ -1575,8 +1575,11 @@ __global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int 
                                                           const float *__restrict__ den_m,
                                                           const int32_t *__restrict__ den_e, float *marg_all,
                                                           double *part) {
-    extern __shared__ float2 tm_s[];  // [2 S]: (mantissa, exponent bits) of alpha, then of beta
+    // shared memory: fast form [S + 1] alpha', [S + 1] beta' (fp32, scaled, zero at index S);
+    // exact form [S + 1] + [S + 1] (mantissa, exponent bits) pairs
+    extern __shared__ float2 tm_s[];
     __shared__ double red[kTmWarps];
+    __shared__ int ired[2 * kTmWarps];
     const int S = fa.S, V = fa.V;
     const size_t pos = blockIdx.x / (unsigned)n_chunks;
     const int chunk = (int)(blockIdx.x % (unsigned)n_chunks);
@@ -1594,13 +1597,40 @@ __global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int 
     }
     const int E = den_e[pos];
     const float inv = 1.0f / dm;
-    float2 *sa = tm_s, *sb = tm_s + S;
     const size_t ba = ((size_t)b * (L + 1) + t) * S, bb = ba + S;
+    // the fast form scales alpha and beta by one power of two each (at most 2 after it), and a
+    // token's sum by 2^X, X = Ea + Eb - E; it is taken when X <= 60, so the products lost
+    // below the fp32 normal range weigh under |S| 2^-66 in a marginal
+    int ea = FA_INT_NONE, eb = FA_INT_NONE;
     for (int s = tid; s < S; s += kTmThreads) {
-        sa[s] = make_float2(am[ba + s], __int_as_float(ae[ba + s]));
-        sb[s] = make_float2(bm[bb + s], __int_as_float(be[bb + s]));
+        const float x = am[ba + s], y = bm[bb + s];
+        if (x > 0.0f) ea = max(ea, ae[ba + s] + fa_exponent(x));
+        if (y > 0.0f) eb = max(eb, be[bb + s] + fa_exponent(y));
+    }
+    ea = fa_warp_max_int(ea);
+    eb = fa_warp_max_int(eb);
+    if (lane == 0) { ired[warp] = ea; ired[kTmWarps + warp] = eb; }
+    __syncthreads();
+    int Ea = FA_INT_NONE, Eb = FA_INT_NONE;
+    for (int w = 0; w < kTmWarps; ++w) { Ea = max(Ea, ired[w]); Eb = max(Eb, ired[kTmWarps + w]); }
+    const bool fast = Ea != FA_INT_NONE && Eb != FA_INT_NONE && Ea + Eb - E <= 60;
+    const int X = fast ? Ea + Eb - E : 0;
+    float *fa1 = reinterpret_cast<float *>(tm_s), *fb1 = fa1 + S + 1;
+    float2 *sa = tm_s, *sb = tm_s + S + 1;
+    if (fast) {
+        for (int s = tid; s <= S; s += kTmThreads) {
+            const float x = s < S ? am[ba + s] : 0.0f, y = s < S ? bm[bb + s] : 0.0f;
+            fa1[s] = x > 0.0f ? fa_mul_pow2(x, ae[ba + s] - Ea) : 0.0f;
+            fb1[s] = y > 0.0f ? fa_mul_pow2(y, be[bb + s] - Eb) : 0.0f;
+        }
+    } else {
+        for (int s = tid; s <= S; s += kTmThreads) {
+            sa[s] = s < S ? make_float2(am[ba + s], __int_as_float(ae[ba + s])) : make_float2(0.0f, 0.0f);
+            sb[s] = s < S ? make_float2(bm[bb + s], __int_as_float(be[bb + s])) : make_float2(0.0f, 0.0f);
+        }
     }
     __syncthreads();
+    const uint32_t pad = ((uint32_t)S << 16) | (uint32_t)S;   // the streams' padding: index S (zero)
     const float *prow = probs + pos * (size_t)V;
     float sl = 0.0f, cl = 0.0f;  // compensated sum of p ln p
     // the block's range [v0, v1) is in the tok_perm order; warp w takes the token groups
@@ -1616,18 +1646,21 @@ __global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int 
         for (int64_t k0 = 0; k0 < nr; k0 += 8) {
             uint32_t sdv[8];  // eight rows' loads in flight before any is used
 #pragma unroll
-            for (int u = 0; u < 8; ++u) sdv[u] = k0 + u < nr ? __ldg(col + (size_t)(k0 + u) * 32) : FA_SD_NONE;
+            for (int u = 0; u < 8; ++u) sdv[u] = k0 + u < nr ? __ldg(col + (size_t)(k0 + u) * 32) : pad;
+            if (fast) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t sd = sdv[u];
-                if (sd != FA_SD_NONE) {
+                for (int u = 0; u < 8; ++u) acc = fmaf(fa1[sdv[u] >> 16], fb1[sdv[u] & 0xffffu], acc);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t sd = sdv[u];
                     const float2 a = sa[sd >> 16], bq = sb[sd & 0xffffu];
                     if (a.x > 0.0f && bq.x > 0.0f) acc += a.x * bq.x * fa_pow2(__float_as_int(a.y) + __float_as_int(bq.y) - E);
                 }
             }
         }
         if (i >= v1) continue;
-        const float pv = w > 0.0f ? w * acc * inv : 0.0f;
+        const float pv = w > 0.0f ? w * fa_mul_pow2(acc, X) * inv : 0.0f;
         if (out) out[v] = pv;
         if (pv > 0.0f) {
             const float y = pv * logf(pv) - cl, tt = sl + y;
@@ -2160,8 +2193,8 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
 fa_status launch_token_marginals(const fa_automaton *aut, int B, int L, const float *probs, const int32_t *committed,
                                  const Plan &p, const char *ws, const int32_t *row_status, float *marg_all,
                                  float *entropy, float *conf, cudaStream_t st) {
-    const size_t smem = (size_t)aut->S * 16;
-    if (smem > 48 * 1024) {
+    const size_t smem = ((size_t)aut->S + 1) * 16;
+    if (smem > 44 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k_tm_partial, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) { fa_set_error(std::string("token marginals smem: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     }
