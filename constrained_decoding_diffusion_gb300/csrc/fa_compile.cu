@@ -185,6 +185,78 @@ size_t schedule_unit_chunk(int CH, const std::vector<std::vector<std::vector<uin
     return (size_t)gmax;
 }
 
+// Token-major incidence streams of the all-token marginals: the (src, dst) pair of every
+// token-edge incidence (|S| <= 4096 fits 16 bits), the tokens ordered by incidence count
+// (ties by id) and interleaved by groups of 32, each group as many rows as its longest
+// token (tokens of nearly equal counts share a group, so the padding stays near one row per
+// incidence however skewed the counts are), padding (S, S).  A token's incidences may come
+// in any order, so each row is filled greedily to keep the 32 lanes' gathers of alpha(src)
+// (shared-memory word src) and of beta(dst) (word S + 1 + dst) in distinct banks, or on a
+// shared address: a lane takes the first of its next incidences (a window of 48) that adds
+// no conflict, else the one adding fewest.
+void build_token_streams(int S, int V, const std::vector<int64_t> &tok_off, const std::vector<int32_t> &tok_edges,
+                         const int32_t *edge_src, const int32_t *edge_dst, std::vector<int32_t> &tok_perm,
+                         std::vector<int64_t> &tok_goff, std::vector<uint32_t> &tok_sd) {
+    const int64_t n_tg = ((int64_t)V + 31) / 32;
+    tok_perm.resize(V);
+    std::iota(tok_perm.begin(), tok_perm.end(), 0);
+    std::stable_sort(tok_perm.begin(), tok_perm.end(), [&](int32_t x, int32_t y) {
+        return tok_off[x + 1] - tok_off[x] < tok_off[y + 1] - tok_off[y];
+    });
+    tok_goff.assign(n_tg + 1, 0);
+    for (int64_t g = 0; g < n_tg; ++g) {
+        int64_t cnt = 0;
+        for (int64_t i = 32 * g; i < std::min<int64_t>(32 * g + 32, V); ++i)
+            cnt = std::max(cnt, tok_off[tok_perm[i] + 1] - tok_off[tok_perm[i]]);
+        tok_goff[g + 1] = tok_goff[g] + cnt;
+    }
+    const uint32_t pad = ((uint32_t)S << 16) | (uint32_t)S;
+    tok_sd.assign((size_t)tok_goff[n_tg] * 32, pad);
+    const int kWin = 48;
+    std::vector<uint32_t> rem[32];
+    for (int64_t g = 0; g < n_tg; ++g) {
+        for (int l = 0; l < 32; ++l) {
+            rem[l].clear();
+            const int64_t i = 32 * g + l;
+            if (i >= V) continue;
+            const int v = tok_perm[i];
+            for (int64_t k = tok_off[v]; k < tok_off[v + 1]; ++k) {
+                const int e = tok_edges[k];
+                rem[l].push_back(((uint32_t)edge_src[e] << 16) | (uint32_t)edge_dst[e]);
+            }
+        }
+        for (int64_t row = tok_goff[g]; row < tok_goff[g + 1]; ++row) {
+            int a_addr[32], b_addr[32];   // the address a bank holds (-1: free, -2: several)
+            for (int q = 0; q < 32; ++q) a_addr[q] = b_addr[q] = -1;
+            auto cost = [&](uint32_t sd) {
+                const int a = (int)(sd >> 16), bw = S + 1 + (int)(sd & 0xffffu);
+                const int qa = a & 31, qb = bw & 31;
+                return (int)(a_addr[qa] != -1 && a_addr[qa] != a) + (int)(b_addr[qb] != -1 && b_addr[qb] != bw);
+            };
+            bool padded = false;   // the lanes past their token's count read the padding
+            for (int l = 0; l < 32; ++l) padded |= rem[l].empty();
+            if (padded) { a_addr[S & 31] = S; b_addr[(2 * S + 1) & 31] = 2 * S + 1; }
+            for (int l = 0; l < 32; ++l) {
+                if (rem[l].empty()) continue;
+                const int n = (int)std::min<size_t>(rem[l].size(), kWin);
+                int best = 0, bc = 3;
+                for (int x = 0; x < n && bc > 0; ++x) {
+                    const int c = cost(rem[l][rem[l].size() - 1 - x]);
+                    if (c < bc) { bc = c; best = x; }
+                }
+                const size_t at = rem[l].size() - 1 - best;
+                const uint32_t sd = rem[l][at];
+                rem[l][at] = rem[l].back();
+                rem[l].pop_back();
+                const int a = (int)(sd >> 16), bw = S + 1 + (int)(sd & 0xffffu);
+                a_addr[a & 31] = a_addr[a & 31] == -1 || a_addr[a & 31] == a ? a : -2;
+                b_addr[bw & 31] = b_addr[bw & 31] == -1 || b_addr[bw & 31] == bw ? bw : -2;
+                tok_sd[(size_t)row * 32 + l] = sd;
+            }
+        }
+    }
+}
+
 std::string build_run_layout(int S, int V, int n_cells, const std::vector<int32_t> &row_cell_off,
                              const std::vector<int64_t> &cell_off, const std::vector<int32_t> &cell_tok,
                              RunLayout &out) {
@@ -519,32 +591,10 @@ extern "C" fa_status fa_compile(int32_t n_states, int32_t start, const int32_t *
     }
 
     std::vector<int32_t> esrc(edge_src, edge_src + E), edst(edge_dst, edge_dst + E);
-    // the (src, dst) pair of every token-edge incidence (|S| <= 4096 fits 16 bits), the tokens
-    // ordered by incidence count (ties by id) and interleaved by groups of 32, each group as
-    // many rows as its longest token: tokens of nearly equal counts share a group, so the
-    // padding stays near one row per incidence however skewed the counts are
-    const int64_t n_tg = ((int64_t)V + 31) / 32;
-    std::vector<int32_t> tok_perm(V);
-    std::iota(tok_perm.begin(), tok_perm.end(), 0);
-    std::stable_sort(tok_perm.begin(), tok_perm.end(), [&](int32_t x, int32_t y) {
-        return tok_off[x + 1] - tok_off[x] < tok_off[y + 1] - tok_off[y];
-    });
-    std::vector<int64_t> tok_goff(n_tg + 1, 0);
-    for (int64_t g = 0; g < n_tg; ++g) {
-        int64_t cnt = 0;
-        for (int64_t i = 32 * g; i < std::min<int64_t>(32 * g + 32, V); ++i)
-            cnt = std::max(cnt, tok_off[tok_perm[i] + 1] - tok_off[tok_perm[i]]);
-        tok_goff[g + 1] = tok_goff[g] + cnt;
-    }
-    // padding (src, dst) = (S, S): the all-token pass keeps a zero message entry at index S
-    std::vector<uint32_t> tok_sd((size_t)tok_goff[n_tg] * 32, ((uint32_t)S << 16) | (uint32_t)S);
-    for (int64_t i = 0; i < V; ++i) {
-        const int64_t g = i / 32, lane = i % 32, v = tok_perm[i];
-        for (int64_t k = 0; k < tok_off[v + 1] - tok_off[v]; ++k) {
-            const int e = tok_edges[tok_off[v] + k];
-            tok_sd[(size_t)(tok_goff[g] + k) * 32 + lane] = ((uint32_t)edge_src[e] << 16) | (uint32_t)edge_dst[e];
-        }
-    }
+    std::vector<int32_t> tok_perm;
+    std::vector<int64_t> tok_goff;
+    std::vector<uint32_t> tok_sd;
+    build_token_streams(S, V, tok_off, tok_edges, edge_src, edge_dst, tok_perm, tok_goff, tok_sd);
 
     BlobBuilder bb;
     bb.add(&a->lab_off, lab_off);
