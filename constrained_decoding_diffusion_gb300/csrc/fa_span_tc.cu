@@ -9,11 +9,11 @@
 // truncated to TF32, so hi*hi + hi*lo + lo*hi on the TF32 tensor cores (fp32 accumulation)
 // keeps fp32 accuracy ("3xTF32"); lo*lo is below fp32 rounding.
 //
-// Three kernels per tree level.  k_tc_prep_left computes each row's shift mu and writes the
-// left child, row prescaled, and k_tc_prep_right the right child, both split into hi/lo, as
-// the exact images of the shared-memory tiles the MMAs read (canonical K-major no-swizzle
-// layout: 8-row x 16-byte core matrices, K-direction core stride 128 B, row-group stride
-// 512 B; 128x16 left tiles, 256x16 right tiles).  k_span_tc then runs a warp-specialised pipeline per 128x256 output
+// Two kernels per tree level.  k_tc_prep converts every operand once: the left child, row
+// prescaled, and the right child are split into hi/lo and written as the exact images of the
+// shared-memory tiles the MMAs read (canonical K-major no-swizzle layout: 8-row x 16-byte
+// core matrices, K-direction core stride 128 B, row-group stride 512 B; 128x16 left tiles,
+// 256x16 right tiles).  k_span_tc then runs a warp-specialised pipeline per 128x256 output
 // tile: one producer thread streams the tile images of each K step (48 KB) into one of four
 // shared-memory stages, tracked by the stage's "full" mbarrier; one thread issues the MMAs
 // (M=128, N=256, K=8; hi*hi, hi*lo, lo*hi) and commits them to the stage's "empty" mbarrier,
@@ -152,136 +152,88 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
     lo = x - hi;
 }
 
-// Right operand images for one level.  Blocks: (product, 256-column tile, chunk of PREP_KT K
-// steps); the right child is split into hi/lo and transposed to K-major tiles.  The left
-// images come first in img (n_prod_slots products), written by k_tc_prep_left.
-__global__ void __launch_bounds__(NTHR) k_tc_prep_right(int S, int L, int k, int nk, const float *__restrict__ mant_c,
-                                                      int nc, long n_prod_slots, unsigned char *img) {
+// Operand images for one level.  Blocks: (product, side, tile, chunk of PREP_KT K steps);
+// side 0 = left operand (prescaled by 2^(rhoR[m] - mu[row]), 128-row tiles), side 1 = right
+// operand (256-column tiles, transposed to K-major).
+__global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, const float *__restrict__ mant_c,
+                                                const int32_t *__restrict__ rho_c,
+                                                const int32_t *__restrict__ rmax_c,
+                                                const int32_t *__restrict__ rminc_c, int nc,
+                                                const int32_t *__restrict__ mu, unsigned char *img,
+                                                int32_t *range_lost) {
     const int tid = threadIdx.x;
     const int tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN, nkt = (S + TK - 1) / TK;
+    const int per = tiles_m + tiles_n;
     const int kch = (nkt + PREP_KT - 1) / PREP_KT;                 // K-step chunks per tile
     const int kc = blockIdx.x % kch;
     const long flat = blockIdx.x / kch;
-    const int tn = (int)(flat % tiles_n);
-    const long bn = flat / tiles_n;
+    const int w = (int)(flat % per);
+    const long bn = flat / per;
     const int kt0 = kc * PREP_KT, kt1 = min(nkt, kt0 + PREP_KT);
-    const int node = (int)(bn % nk), b = (int)(bn / nk);
-    if (((2 * node + 1) << (k - 1)) >= L) return;     // a copy, no product
-    const size_t SS = (size_t)S * S;
-    const size_t rnode = (size_t)b * nc + 2 * node + 1;
-    const size_t per_prod_a = (size_t)tiles_m * nkt * A_IMG, per_prod_b = (size_t)tiles_n * nkt * B_IMG;
-    const size_t total_a = (size_t)n_prod_slots * per_prod_a;
-    const int n = tid, gj = tn * TN + n;
-    const float *Bm = mant_c + rnode * SS;
-    unsigned char *base = img + total_a + (size_t)bn * per_prod_b + (size_t)tn * nkt * B_IMG;
-    for (int kt = kt0; kt < kt1; ++kt) {
-        unsigned char *t = base + (size_t)kt * B_IMG;
-#pragma unroll
-        for (int g = 0; g < TK / 4; ++g) {
-            float x[4], hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = kt * TK + 4 * g + e;
-                x[e] = (gj < S && m < S) ? __ldg(Bm + (size_t)m * S + gj) : 0.0f;
-                split_tf32(x[e], hi[e], lo[e]);
-            }
-            const uint32_t off = kmaj_off(n, 4 * g);
-            *reinterpret_cast<float4 *>(t + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<float4 *>(t + B_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-        }
-    }
-}
-
-// Left operand images with the row shift fused in: one block per 128-row tile of a product,
-// in groups of 16 rows.  For each row i, mu[i] = max over m with a nonzero right row m and
-// A_L[i, m] > 0 of rhoR[m] + e(rmaxR[m]) + e(A_L[i, m]) (a warp per row), then the row is
-// prescaled by 2^(rhoR[m] - mu[i]), split into hi/lo and written as the K-major tile images
-// of every K step.  The group's rows are read twice, the second time from cache.  Also clears
-// the product's row maxima (rmax_p, rminc_p), which the product kernel accumulates with
-// atomicMax.
-constexpr int PREP_ROWS = 16;
-
-__global__ void __launch_bounds__(NTHR) k_tc_prep_left(int S, int L, int k, int nk, const float *__restrict__ mant_c,
-                                                     const int32_t *__restrict__ rho_c,
-                                                     const int32_t *__restrict__ rmax_c,
-                                                     const int32_t *__restrict__ rminc_c, int nc, int32_t *mu,
-                                                     int32_t *rmax_p, int32_t *rminc_p, unsigned char *img,
-                                                     int32_t *range_lost) {
-    extern __shared__ int prep_sm[];
-    int *srho = prep_sm;            // [S] rhoR[m], FA_INT_NONE for an all-zero right row m
-    int *stop = srho + S;           // [S] rhoR[m] + e(rmaxR[m])
-    int *smin = stop + S;           // [S] min(0, e(smallest nonzero entry of right row m))
-    int *smu = smin + S;            // [PREP_ROWS] row shifts of the current group
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int tiles_m = (S + TM - 1) / TM, nkt = (S + TK - 1) / TK;
-    const int tm = (int)(blockIdx.x % tiles_m);
-    const long bn = blockIdx.x / tiles_m;
     const int node = (int)(bn % nk), b = (int)(bn / nk);
     if (((2 * node + 1) << (k - 1)) >= L) return;     // a copy, no product
     const size_t SS = (size_t)S * S;
     const size_t pnode = (size_t)b * nk + node;
     const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
-    const float *A = mant_c + lnode * SS;
-    for (int m = tid; m < S; m += NTHR) {
-        const int rr = rmax_c[rnode * S + m], rn = rminc_c[rnode * S + m], rh = rho_c[rnode * S + m];
-        srho[m] = rr > 0 ? rh : FA_INT_NONE;
-        stop[m] = rr > 0 ? rh + fa_exponent(__int_as_float(rr)) : FA_INT_NONE;
-        smin[m] = rn > 0 ? min(0, fa_exponent(__int_as_float(0x7fffffff - rn))) : 0;
-    }
-    unsigned char *base = img + (size_t)bn * tiles_m * nkt * A_IMG + (size_t)tm * nkt * A_IMG;
-    int lost = 0;
-    for (int g0 = 0; g0 < TM; g0 += PREP_ROWS) {
-        __syncthreads();   // the staged right-row data, and the previous group's shifts are used up
-        // the group's row shifts: warp w takes rows g0 + w and g0 + w + 8
-        for (int r = warp; r < PREP_ROWS; r += NTHR / 32) {
-            const int gi = tm * TM + g0 + r;
-            int best = FA_INT_NONE;
-            if (gi < S) {
-                const float *row = A + (size_t)gi * S;
-                for (int m = lane; m < S; m += 32) {
-                    const float x = __ldg(row + m);
-                    const int t = stop[m];
-                    if (x > 0.0f && t != FA_INT_NONE) best = max(best, t + fa_exponent(x));
-                }
-                best = fa_warp_max_int(best);
-                if (lane == 0) {
-                    mu[pnode * S + gi] = best;
-                    rmax_p[pnode * S + gi] = 0;
-                    rminc_p[pnode * S + gi] = 0;
-                }
-            }
-            if (lane == 0) smu[r] = best;
-        }
-        __syncthreads();
-        // prescale and split: 16 threads per row, each a 4-column group at a time
-        const int r = tid >> 4, c4 = tid & 15;
-        const int row = g0 + r, gi = tm * TM + row;
-        const int mrow = smu[r];
-        for (int m0 = 4 * c4; m0 < nkt * TK; m0 += 64) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (gi < S && m0 < S) v = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gi * S + m0));
-            const float x[4] = {v.x, v.y, v.z, v.w};
-            float hi[4], lo[4];
+    const size_t per_prod_a = (size_t)tiles_m * nkt * A_IMG, per_prod_b = (size_t)tiles_n * nkt * B_IMG;
+    const size_t total_a = (size_t)gridDim.x / ((size_t)per * kch) * per_prod_a;  // left images come first
+    if (w < tiles_m) {
+        const int tm = w, row = tid >> 1, gi = tm * TM + row;
+        const float *A = mant_c + lnode * SS;
+        const int32_t *rhoR = rho_c + rnode * S, *rmaxR = rmax_c + rnode * S, *rmincR = rminc_c + rnode * S;
+        const int mrow = gi < S ? mu[pnode * S + gi] : FA_INT_NONE;
+        unsigned char *base = img + (size_t)bn * per_prod_a + (size_t)tm * nkt * A_IMG;
+        int lost = 0;
+        for (int kt = kt0; kt < kt1; ++kt) {
+            unsigned char *t = base + (size_t)kt * A_IMG;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = m0 + e;
-                float y = 0.0f;
-                if (x[e] > 0.0f && mrow != FA_INT_NONE && m < S && srho[m] != FA_INT_NONE) {
-                    const int d = srho[m] - mrow;
-                    // below the normal range after the prescale, alone or times the right
-                    // row's smallest entry: mass may be lost
-                    if (fa_exponent(x[e]) + d + smin[m] < -126) lost = 1;
-                    y = fa_mul_pow2(x[e], d);
+            for (int q = 0; q < TK / 8; ++q) {
+                const int kk = (tid & 1) * (TK / 2) + 4 * q, m0 = kt * TK + kk;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gi < S && m0 < S) v = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gi * S + m0));
+                float x[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = m0 + e;
+                    float y = 0.0f;
+                    if (x[e] > 0.0f && mrow != FA_INT_NONE && m < S && __ldg(rmaxR + m) > 0) {
+                        const int d = __ldg(rhoR + m) - mrow;
+                        // below the normal range after the prescale, alone or times the right
+                        // row's smallest entry: mass may be lost
+                        const int rn = __ldg(rmincR + m);
+                        const int emin = rn > 0 ? min(0, fa_exponent(__int_as_float(0x7fffffff - rn))) : 0;
+                        if (fa_exponent(x[e]) + d + emin < -126) lost = 1;
+                        y = fa_mul_pow2(x[e], d);
+                    }
+                    split_tf32(y, hi[e], lo[e]);
                 }
-                split_tf32(y, hi[e], lo[e]);
+                const uint32_t off = kmaj_off(row, kk);
+                *reinterpret_cast<float4 *>(t + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4 *>(t + A_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
-            unsigned char *t = base + (size_t)(m0 / TK) * A_IMG;
-            const uint32_t off = kmaj_off(row, m0 % TK);
-            *reinterpret_cast<float4 *>(t + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<float4 *>(t + A_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        if (__any_sync(0xffffffffu, lost) && (tid & 31) == 0) atomicOr(range_lost + b, 1);
+    } else {
+        const int tn = w - tiles_m, n = tid, gj = tn * TN + n;
+        const float *Bm = mant_c + rnode * SS;
+        unsigned char *base = img + total_a + (size_t)bn * per_prod_b + (size_t)tn * nkt * B_IMG;
+        for (int kt = kt0; kt < kt1; ++kt) {
+            unsigned char *t = base + (size_t)kt * B_IMG;
+#pragma unroll
+            for (int g = 0; g < TK / 4; ++g) {
+                float x[4], hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = kt * TK + 4 * g + e;
+                    x[e] = (gj < S && m < S) ? __ldg(Bm + (size_t)m * S + gj) : 0.0f;
+                    split_tf32(x[e], hi[e], lo[e]);
+                }
+                const uint32_t off = kmaj_off(n, 4 * g);
+                *reinterpret_cast<float4 *>(t + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4 *>(t + B_BYTES + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            }
         }
     }
-    if (__any_sync(0xffffffffu, lost) && lane == 0) atomicOr(range_lost + b, 1);
 }
 
 __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk, const float *__restrict__ mant_c,
@@ -467,7 +419,7 @@ size_t fa_span_tc_image_bytes(int S, long products) {
 }
 
 fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant_c, const int32_t *rho_c,
-                           const int32_t *rmax_c, const int32_t *rminc_c, int nc, int32_t *mu, float *mant_p,
+                           const int32_t *rmax_c, const int32_t *rminc_c, int nc, const int32_t *mu, float *mant_p,
                            int32_t *rho_p, int32_t *rmax_p, int32_t *rminc_p, int32_t *err, int32_t *range_lost,
                            void *img, cudaStream_t stream) {
     const size_t smem = fa_span_tc_smem(S);
@@ -475,17 +427,8 @@ fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant
     if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     const long tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN;
     const long kch = ((S + TK - 1) / TK + PREP_KT - 1) / PREP_KT;
-    const size_t left_smem = (3 * (size_t)S + PREP_ROWS) * sizeof(int);
-    if (left_smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(k_tc_prep_left, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)left_smem);
-        if (e != cudaSuccess) { fa_set_error(std::string("operand images (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
-    }
-    k_tc_prep_left<<<(unsigned)((long)B * nk * tiles_m), NTHR, left_smem, stream>>>(
-        S, L, k, nk, mant_c, rho_c, rmax_c, rminc_c, nc, mu, rmax_p, rminc_p, (unsigned char *)img, range_lost);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) { fa_set_error(std::string("operand images (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
-    k_tc_prep_right<<<(unsigned)((long)B * nk * tiles_n * kch), NTHR, 0, stream>>>(S, L, k, nk, mant_c, nc, (long)B * nk,
-                                                                                (unsigned char *)img);
+    k_tc_prep<<<(unsigned)((long)B * nk * (tiles_m + tiles_n) * kch), NTHR, 0, stream>>>(
+        S, L, k, nk, mant_c, rho_c, rmax_c, rminc_c, nc, mu, (unsigned char *)img, range_lost);
     e = cudaGetLastError();
     if (e != cudaSuccess) { fa_set_error(std::string("operand images (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     const long grid = (long)B * nk * tiles_m * tiles_n;

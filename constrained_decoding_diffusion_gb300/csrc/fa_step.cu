@@ -2439,19 +2439,18 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
             if ((st = launch_check("span product (small)")) != FA_OK) return st;
             continue;
         }
+        dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
+        k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
+                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
+        if ((st = launch_check("rowshift")) != FA_OK) return st;
         if (fa_span_tc_supported(S)) {
-            // the row shift is computed by the left operand images (three launches per level)
-            g_launches.fetch_add(3, std::memory_order_relaxed);
+            g_launches.fetch_add(2, std::memory_order_relaxed);
             st = fa_span_tc_level(S, B, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
                                   I(p.rminc[kk - 1]), p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]),
                                   I(p.rmax[kk]), I(p.rminc[kk]), I(p.tc_err), I(p.range_lost), ws + p.img, s);
             if (st != FA_OK) return st;
             continue;
         }
-        dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
-        k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
-                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
-        if ((st = launch_check("rowshift")) != FA_OK) return st;
         const long tiles = (S + GBN - 1) / GBN;
         const long g2 = (long)B * p.nk[kk] * tiles * tiles;
         k_gemm_simt<false><<<(unsigned)g2, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
