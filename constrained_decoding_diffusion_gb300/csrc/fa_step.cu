@@ -1643,14 +1643,26 @@ __global__ void __launch_bounds__(kTmThreads) k_tm_partial(DevFA fa, int L, int 
         const int64_t r0 = fa.tok_goff[g], nr = fa.tok_goff[g + 1] - r0;
         const uint32_t *col = fa.tok_sd + (size_t)r0 * 32 + lane;
         float acc = 0.0f;
-        for (int64_t k0 = 0; k0 < nr; k0 += 8) {
-            uint32_t sdv[8];  // eight rows' loads in flight before any is used
+        if (fast) {
+            // whole steps of eight rows (their loads in flight before any is used), then the rest
+            const uint32_t *p = col;
+            int64_t k0 = 0;
+            for (; k0 + 8 <= nr; k0 += 8, p += 256) {
+                uint32_t sdv[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) sdv[u] = k0 + u < nr ? __ldg(col + (size_t)(k0 + u) * 32) : pad;
-            if (fast) {
+                for (int u = 0; u < 8; ++u) sdv[u] = __ldg(p + 32 * u);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) acc = fmaf(fa1[sdv[u] >> 16], fb1[sdv[u] & 0xffffu], acc);
-            } else {
+            }
+            for (; k0 < nr; ++k0, p += 32) {
+                const uint32_t sd = __ldg(p);
+                acc = fmaf(fa1[sd >> 16], fb1[sd & 0xffffu], acc);
+            }
+        } else {
+            for (int64_t k0 = 0; k0 < nr; k0 += 8) {
+                uint32_t sdv[8];  // eight rows' loads in flight before any is used
+#pragma unroll
+                for (int u = 0; u < 8; ++u) sdv[u] = k0 + u < nr ? __ldg(col + (size_t)(k0 + u) * 32) : pad;
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const uint32_t sd = sdv[u];
