@@ -99,9 +99,23 @@ def test_entropy_closed_form_real_number(native):
     np.testing.assert_allclose(res["entropy"][0], [math.log(11), math.log(10)], rtol=0, atol=1e-5)
 
 
-@pytest.mark.parametrize("case", ["real", "tiny_nfa", "dup_dfa", "random_dfa", "tensor_core", "unconstrained"])
+@pytest.mark.parametrize("case", ["real", "tiny_nfa", "dup_dfa", "random_dfa", "tensor_core", "unconstrained",
+                                  "rare_start_rare_end"])
 def test_full_marginals_match_oracle(native, case):
+    """rare_start_rare_end (a rare first and a rare last token carry the only two accepting
+    paths) puts the normaliser about 2^-100 below the largest message products, so the
+    all-token pass takes its exact form there."""
     rng = np.random.default_rng(11)
+    if case == "rare_start_rare_end":
+        from test_gpu_parity import rare_start_rare_end_fa
+        fa, B, L, V = rare_start_rare_end_fa(4), 2, 12, 8
+        probs = synth.gaussian_probs(rng, B, L, V, 1.0)
+        probs[:, 0, 0] = 1e-30
+        probs[:, L - 1, 7] = 1e-30
+        committed = np.full((B, L), -1, np.int32)
+        res = run(native, fa, probs, committed, 17, 3)
+        check_full(fa, probs, committed, res)
+        return
     if case == "real":
         fa, B, L, sigma = synth.real_number_dfa(), 3, 6, 2.0
     elif case == "tiny_nfa":
