@@ -24,6 +24,7 @@
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kHostChunks = 8;  // sequence chunks of fa_constrained_step_host's input copies
 constexpr int kTmChunkMax = 4096, kTmChunkMin = 1024;  // tokens per block of the all-token marginals
 constexpr int kWarps = kThreads / 32;
 
@@ -2352,10 +2353,18 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
 }
 
 namespace {
+// Inputs still in host memory (fa_constrained_step_host): copied into the device buffers
+// probs / committed in sequence chunks, each chunk's reweighting started once it has landed.
+struct HostInput {
+    const float *probs;
+    const int32_t *committed;
+};
+
 fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *probs, const int32_t *committed,
                     uint64_t philox_seed, uint64_t philox_offset, int32_t k, int32_t commit_lo, int32_t commit_hi,
                     int32_t confidence, void *workspace, size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
-                    float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream, bool chain);
+                    float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream, bool chain,
+                    const HostInput *hin = nullptr);
 }
 
 extern "C" fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
@@ -2366,6 +2375,22 @@ extern "C" fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, 
                                             fa_stream stream) {
     return step_impl(aut, B, L, probs, committed, philox_seed, philox_offset, k, commit_lo, commit_hi, confidence,
                      workspace, ws_bytes, tokens, logZ, marg, entropy, commit_idx, row_status, stream, false);
+}
+
+extern "C" fa_status fa_constrained_step_host(const fa_automaton *aut, int32_t B, int32_t L, const float *h_probs,
+                                              const int32_t *h_committed, float *d_probs, int32_t *d_committed,
+                                              uint64_t philox_seed, uint64_t philox_offset, int32_t k,
+                                              int32_t commit_lo, int32_t commit_hi, void *workspace, size_t ws_bytes,
+                                              int32_t *tokens, double *logZ, float *marg, int32_t *commit_idx,
+                                              int32_t *row_status, fa_stream stream) {
+    if (B > 0 && L > 0 && (!h_probs || !h_committed || !d_probs || !d_committed)) {
+        fa_set_error("fa_constrained_step_host: NULL input buffer");
+        return FA_ERR_INVALID_ARG;
+    }
+    const HostInput hin{h_probs, h_committed};
+    return step_impl(aut, B, L, d_probs, d_committed, philox_seed, philox_offset, k, commit_lo, commit_hi,
+                     FA_CONF_MARGINAL, workspace, ws_bytes, tokens, logZ, marg, nullptr, commit_idx, row_status, stream,
+                     false, &hin);
 }
 
 extern "C" fa_status fa_constrained_step_chain(const fa_automaton *aut, int32_t B, int32_t L, const float *probs,
@@ -2380,10 +2405,76 @@ extern "C" fa_status fa_constrained_step_chain(const fa_automaton *aut, int32_t 
 }
 
 namespace {
+// The copy stream and events of fa_constrained_step_host, per host thread and device.
+struct CopyContext {
+    cudaStream_t cs = nullptr;
+    cudaEvent_t start = nullptr, com = nullptr;
+    cudaEvent_t chunk[kHostChunks] = {};
+};
+
+fa_status copy_context(CopyContext *&out) {
+    static thread_local std::vector<CopyContext> ctx;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { fa_set_error(std::string("host inputs: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    if ((int)ctx.size() <= dev) ctx.resize(dev + 1);
+    CopyContext &c = ctx[dev];
+    if (!c.cs) {
+        e = cudaStreamCreateWithFlags(&c.cs, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.start, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.com, cudaEventDisableTiming);
+        for (int i = 0; i < kHostChunks && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&c.chunk[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) { c.cs = nullptr; fa_set_error(std::string("host inputs: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    }
+    out = &c;
+    return FA_OK;
+}
+
+// Emission reweighting from host inputs: the committed tokens and then the probabilities of
+// up to kHostChunks chunks of sequences are copied on the copy stream (after the work already
+// on `s`), and the reweighting of each chunk runs on `s` once its rows are in, so the copies
+// of later chunks overlap the reweighting of earlier ones.
+fa_status reweight_from_host(const fa_automaton *a, int B, int L, const HostInput &hin, float *d_probs,
+                             int32_t *d_committed, float *mant, int32_t *rho, int32_t *rmax, int32_t *rminc,
+                             cudaStream_t s, int32_t *zero, long n_zero) {
+    CopyContext *c = nullptr;
+    fa_status st = copy_context(c);
+    if (st != FA_OK) return st;
+    const size_t S = (size_t)a->S, V = (size_t)a->V, Ls = (size_t)L;
+    const int nch = std::min(B, kHostChunks), per = (B + nch - 1) / nch;
+    cudaError_t e = cudaEventRecord(c->start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->cs, c->start, 0);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d_committed, hin.committed, (size_t)B * Ls * sizeof(int32_t), cudaMemcpyHostToDevice, c->cs);
+    if (e == cudaSuccess) e = cudaEventRecord(c->com, c->cs);
+    for (int i = 0; i < nch && e == cudaSuccess; ++i) {
+        const size_t b0 = (size_t)i * per, b1 = std::min((size_t)B, b0 + per);
+        if (b0 >= b1) break;
+        e = cudaMemcpyAsync(d_probs + b0 * Ls * V, hin.probs + b0 * Ls * V, (b1 - b0) * Ls * V * sizeof(float),
+                            cudaMemcpyHostToDevice, c->cs);
+        if (e == cudaSuccess) e = cudaEventRecord(c->chunk[i], c->cs);
+    }
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->com, 0);
+    if (e != cudaSuccess) { fa_set_error(std::string("host inputs: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+    for (int i = 0; i < nch; ++i) {
+        const size_t b0 = (size_t)i * per, b1 = std::min((size_t)B, b0 + per);
+        if (b0 >= b1) break;
+        e = cudaStreamWaitEvent(s, c->chunk[i], 0);
+        if (e != cudaSuccess) { fa_set_error(std::string("host inputs: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
+        const size_t pos0 = b0 * Ls;
+        st = launch_reweight(a, (int)(b1 - b0), L, d_probs + pos0 * V, d_committed + pos0, mant + pos0 * S * S,
+                             rho + pos0 * S, rmax + pos0 * S, rminc + pos0 * S, s, i == 0 ? zero : nullptr,
+                             i == 0 ? n_zero : 0);
+        if (st != FA_OK) return st;
+    }
+    return FA_OK;
+}
+
 fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *probs, const int32_t *committed,
                     uint64_t philox_seed, uint64_t philox_offset, int32_t k, int32_t commit_lo, int32_t commit_hi,
                     int32_t confidence, void *workspace, size_t ws_bytes, int32_t *tokens, double *logZ, float *marg,
-                    float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream, bool chain) {
+                    float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream, bool chain,
+                    const HostInput *hin) {
     if (!aut) { fa_set_error("fa_constrained_step: NULL automaton"); return FA_ERR_INVALID_ARG; }
     if (confidence != FA_CONF_MARGINAL && confidence != FA_CONF_NEG_ENTROPY && confidence != FA_CONF_UNCONSTRAINED) {
         fa_set_error("fa_constrained_step: unknown confidence"); return FA_ERR_INVALID_ARG;
@@ -2417,8 +2508,13 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
 
     // 1. emission reweighting -> level-0 spans (also clears the row maxima of levels >= 1)
     stage_mark(0, s);
-    st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), I(p.rminc[0]), s,
-                         I(p.rmax_hi), (long)(p.rmax_hi_bytes / sizeof(int32_t)));
+    if (hin)
+        st = reweight_from_host(aut, B, L, *hin, const_cast<float *>(probs), const_cast<int32_t *>(committed),
+                                F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), I(p.rminc[0]), s, I(p.rmax_hi),
+                                (long)(p.rmax_hi_bytes / sizeof(int32_t)));
+    else
+        st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), I(p.rminc[0]), s,
+                             I(p.rmax_hi), (long)(p.rmax_hi_bytes / sizeof(int32_t)));
     if (st != FA_OK) return st;
 
     if (chain) {

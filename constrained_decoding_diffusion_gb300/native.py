@@ -30,7 +30,7 @@ CONFIDENCE = {"marginal": FA_CONF_MARGINAL, "neg_entropy": FA_CONF_NEG_ENTROPY,
 # every entry point include/fa.h declares
 EXPORTS = ("fa_compile", "fa_destroy", "fa_query", "fa_export_csr", "fa_step_workspace_bytes",
            "fa_transition_matrices", "fa_constrained_step", "fa_constrained_step_ex", "fa_constrained_step_chain",
-           "fa_token_marginals", "fa_map_step",
+           "fa_token_marginals", "fa_map_step", "fa_constrained_step_host",
            "fa_apply_commits", "fa_constrained_step_noalloc", "fa_debug_inject_wait_timeouts",
            "fa_profile_enable", "fa_profile_read",
            "fa_launch_count", "fa_last_error")
@@ -81,6 +81,8 @@ def load(path: str = LIB_PATH):
     lib.fa_token_marginals.restype = st
     lib.fa_apply_commits.argtypes = [i32, i32, i32, P, P, P, P]
     lib.fa_apply_commits.restype = st
+    lib.fa_constrained_step_host.argtypes = [P, i32, i32, P, P, P, P, u64, u64, i32, i32, i32, P, sz, P, P, P, P, P, P]
+    lib.fa_constrained_step_host.restype = st
     lib.fa_constrained_step_noalloc.argtypes = [P, i32, i32, P, P, u64, u64, i32, i32, i32, P, P, P, P, P, P]
     lib.fa_constrained_step_noalloc.restype = st
     lib.fa_debug_inject_wait_timeouts.argtypes = [i32]
@@ -204,6 +206,34 @@ def fa_constrained_step(aut: CompiledAutomaton, probs, committed, philox_seed: i
     _check(_lib.fa_constrained_step(
         aut.handle, B, L, _dev(probs, torch.float32, "probs", (B, L, aut.vocab)),
         _dev(committed, torch.int32, "committed", (B, L)), ctypes.c_uint64(philox_seed & (2 ** 64 - 1)),
+        ctypes.c_uint64(philox_offset & (2 ** 64 - 1)), int(k), int(commit_lo), int(commit_hi),
+        _dev(workspace, workspace.dtype, "workspace"), ws_bytes, _dev(tokens, torch.int32, "tokens", (B, L)),
+        _dev(logZ, torch.float64, "logZ", (B,)), _dev(marg, torch.float32, "marg", (B, L)),
+        _dev(commit_idx, torch.int32, "commit_idx", (B, k)) if k > 0 else None,
+        _dev(row_status, torch.int32, "row_status", (B,)), _stream_ptr(stream)))
+
+
+def _host(t, dtype, name, shape):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("%s must be a host tensor" % name)
+    if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must be a contiguous %s tensor of shape %s" % (name, dtype, tuple(shape)))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def fa_constrained_step_host(aut: CompiledAutomaton, h_probs, h_committed, d_probs, d_committed, philox_seed: int,
+                             philox_offset: int, k: int, commit_lo: int, commit_hi: int, workspace, tokens, logZ,
+                             marg, commit_idx, row_status, stream=None):
+    """fa_constrained_step with the inputs in (page-locked) host tensors: copied into d_probs
+    and d_committed in chunks of sequences, overlapped with the emission reweighting."""
+    import torch
+    B, L, V = h_probs.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.fa_constrained_step_host(
+        aut.handle, B, L, _host(h_probs, torch.float32, "h_probs", (B, L, aut.vocab)),
+        _host(h_committed, torch.int32, "h_committed", (B, L)), _dev(d_probs, torch.float32, "d_probs", (B, L, aut.vocab)),
+        _dev(d_committed, torch.int32, "d_committed", (B, L)), ctypes.c_uint64(philox_seed & (2 ** 64 - 1)),
         ctypes.c_uint64(philox_offset & (2 ** 64 - 1)), int(k), int(commit_lo), int(commit_hi),
         _dev(workspace, workspace.dtype, "workspace"), ws_bytes, _dev(tokens, torch.int32, "tokens", (B, L)),
         _dev(logZ, torch.float64, "logZ", (B,)), _dev(marg, torch.float32, "marg", (B, L)),

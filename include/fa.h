@@ -229,6 +229,35 @@ fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, int32_t L, 
                                  float *entropy, int32_t *commit_idx, int32_t *row_status, fa_stream stream);
 
 /*
+ * fa_constrained_step_host -- fa_constrained_step with the per-position inputs in host
+ * memory (the step a caller runs when the model's probabilities are still on the host).
+ * The method is the one of fa_constrained_step (paperfeed.app summary, "The scan trick";
+ * papernotes.org notes, key designs 1-3); this call only moves the inputs.
+ *
+ *   h_probs      [B, L, V] fp32 host, page-locked (cudaHostAlloc or cudaHostRegister) for
+ *                the copies to run asynchronously; read-only
+ *   h_committed  [B, L] int32 host, page-locked; read-only
+ *   d_probs      [B, L, V] fp32 device, caller-owned: receives the copy of h_probs
+ *   d_committed  [B, L] int32 device, caller-owned: receives the copy of h_committed
+ *   every other argument and output as for fa_constrained_step (outputs in device memory)
+ *
+ * The committed tokens and then the probabilities, in up to eight chunks of sequences, are
+ * copied on a copy stream the library keeps per host thread and device, after the work
+ * already queued on `stream`; the emission reweighting of each chunk starts on `stream` as
+ * soon as its rows have landed, so the copy of later chunks overlaps the reweighting of
+ * earlier ones.  The results are those of fa_constrained_step on the copied inputs, bit for
+ * bit.  The host buffers must stay unchanged until `stream` has passed the call.
+ * Errors: as fa_constrained_step; FA_ERR_INVALID_ARG for a NULL input buffer; FA_ERR_CUDA
+ * when the copy stream or its events cannot be created.
+ */
+fa_status fa_constrained_step_host(const fa_automaton *aut, int32_t B, int32_t L, const float *h_probs,
+                                   const int32_t *h_committed, float *d_probs, int32_t *d_committed,
+                                   uint64_t philox_seed, uint64_t philox_offset, int32_t k, int32_t commit_lo,
+                                   int32_t commit_hi, void *workspace, size_t ws_bytes, int32_t *tokens,
+                                   double *logZ, float *marg, int32_t *commit_idx, int32_t *row_status,
+                                   fa_stream stream);
+
+/*
  * fa_constrained_step_chain -- the same step computed in chain form: forward messages
  * alpha_t = alpha_{t-1} M_t for t = 1..L, then backward messages beta_{t-1} = M_t beta_t with
  * forward-filtering backward-sampling of the states (z_L ~ alpha_L restricted to F,
