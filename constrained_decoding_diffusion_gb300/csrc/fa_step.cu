@@ -867,6 +867,8 @@ struct TopdownArgs {
     const float *mant;    // level-k spans
     const int32_t *rho, *rmax;
     int vec4;             // |S| % 4 == 0: 16-byte loads in the message passes
+    int beta_rows;        // rows per beta block: a multiple of the warps, more for large |S| so
+                          // that the staging of beta_r is shared by more rows
     uint64_t seed, offset;
     int32_t *z, *status;
     float *am, *bm;
@@ -1101,7 +1103,8 @@ __device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
 
 __device__ void topdown_beta(const TopdownArgs &a, int blk, float *sm) {
     const int S = a.S, L = a.L, k = a.k;
-    const int nrbk = (S + kWarps - 1) / kWarps;
+    const int RB = a.beta_rows;
+    const int nrbk = (S + RB - 1) / RB;
     const int rbk = blk % nrbk;
     const long bj = blk / nrbk;
     const int j = (int)(bj % a.np), b = (int)(bj / a.np);
@@ -1128,92 +1131,94 @@ __device__ void topdown_beta(const TopdownArgs &a, int blk, float *sm) {
         sz[q] = sb[q] > 0.0f ? 1.0f : 0.0f;
     }
     __syncthreads();
-    const int row = rbk * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (row >= S) return;
-    const size_t rnode = (size_t)b * a.nc + 2 * j + 1;
-    const float *Rrow = a.mant + rnode * (size_t)S * S + (size_t)row * S;
-    // the row's entries scaled by its largest (their exponents then stay near 0)
-    const int rb = a.rmax[rnode * S + row];
-    const int er = min(126, max(-126, fa_exponent(__int_as_float(rb))));
-    const float rs = __int_as_float((127 - er) << 23);   // 2^-er
-    float sum = 0.0f, sum1 = 0.0f;
-    if (rb > 0 && a.vec4) {
-        constexpr int U4 = 4;  // 16-byte loads issued together
-        for (int q0 = 4 * lane; q0 < S; q0 += 128 * U4) {
-            float4 v[U4];
-#pragma unroll
-            for (int u = 0; u < U4; ++u) {
-                const int q = q0 + 128 * u;
-                v[u] = q < S ? __ldg(reinterpret_cast<const float4 *>(Rrow + q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int lane = threadIdx.x & 31;
+    // warp w takes rows rbk * RB + w, + kWarps, ... of the block's RB rows
+    for (int row = rbk * RB + (threadIdx.x >> 5); row < min(S, (rbk + 1) * RB); row += kWarps) {
+        const size_t rnode = (size_t)b * a.nc + 2 * j + 1;
+        const float *Rrow = a.mant + rnode * (size_t)S * S + (size_t)row * S;
+        // the row's entries scaled by its largest (their exponents then stay near 0)
+        const int rb = a.rmax[rnode * S + row];
+        const int er = min(126, max(-126, fa_exponent(__int_as_float(rb))));
+        const float rs = __int_as_float((127 - er) << 23);   // 2^-er
+        float sum = 0.0f, sum1 = 0.0f;
+        if (rb > 0 && a.vec4) {
+            constexpr int U4 = 4;  // 16-byte loads issued together
+            for (int q0 = 4 * lane; q0 < S; q0 += 128 * U4) {
+                float4 v[U4];
+    #pragma unroll
+                for (int u = 0; u < U4; ++u) {
+                    const int q = q0 + 128 * u;
+                    v[u] = q < S ? __ldg(reinterpret_cast<const float4 *>(Rrow + q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+    #pragma unroll
+                for (int u = 0; u < U4; ++u) {
+                    const int q = min(q0 + 128 * u, S - 4);
+                    const float4 g = *reinterpret_cast<const float4 *>(sg + q), z = *reinterpret_cast<const float4 *>(sz + q);
+                    sum = fmaf(v[u].x * rs, g.x, sum); sum = fmaf(v[u].y * rs, g.y, sum);
+                    sum = fmaf(v[u].z * rs, g.z, sum); sum = fmaf(v[u].w * rs, g.w, sum);
+                    sum1 = fmaf(v[u].x, z.x, sum1); sum1 = fmaf(v[u].y, z.y, sum1);
+                    sum1 = fmaf(v[u].z, z.z, sum1); sum1 = fmaf(v[u].w, z.w, sum1);
+                }
             }
-#pragma unroll
-            for (int u = 0; u < U4; ++u) {
-                const int q = min(q0 + 128 * u, S - 4);
-                const float4 g = *reinterpret_cast<const float4 *>(sg + q), z = *reinterpret_cast<const float4 *>(sz + q);
-                sum = fmaf(v[u].x * rs, g.x, sum); sum = fmaf(v[u].y * rs, g.y, sum);
-                sum = fmaf(v[u].z * rs, g.z, sum); sum = fmaf(v[u].w * rs, g.w, sum);
-                sum1 = fmaf(v[u].x, z.x, sum1); sum1 = fmaf(v[u].y, z.y, sum1);
-                sum1 = fmaf(v[u].z, z.z, sum1); sum1 = fmaf(v[u].w, z.w, sum1);
+        } else if (rb > 0) {
+            constexpr int U = 8;
+            for (int q0 = lane; q0 < S; q0 += 32 * U) {
+                float v[U];
+    #pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int q = q0 + 32 * u;
+                    v[u] = q < S ? __ldg(Rrow + q) : 0.0f;
+                }
+    #pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int q = min(q0 + 32 * u, S - 1);
+                    sum = fmaf(v[u] * rs, sg[q], sum);
+                    sum1 = fmaf(v[u], sz[q], sum1);
+                }
             }
         }
-    } else if (rb > 0) {
-        constexpr int U = 8;
-        for (int q0 = lane; q0 < S; q0 += 32 * U) {
-            float v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int q = q0 + 32 * u;
-                v[u] = q < S ? __ldg(Rrow + q) : 0.0f;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int q = min(q0 + 32 * u, S - 1);
-                sum = fmaf(v[u] * rs, sg[q], sum);
-                sum1 = fmaf(v[u], sz[q], sum1);
-            }
+        sum = fa_warp_sum(sum);
+        sum1 = fa_warp_sum(sum1);
+        if (!(sum1 > 0.0f)) {
+            if (lane == 0) { a.bm[bmid + row] = 0.0f; a.be[bmid + row] = 0; }
+            continue;
         }
-    }
-    sum = fa_warp_sum(sum);
-    sum1 = fa_warp_sum(sum1);
-    if (!(sum1 > 0.0f)) {
-        if (lane == 0) { a.bm[bmid + row] = 0.0f; a.be[bmid + row] = 0; }
-        return;
-    }
-    if (sum >= kMsgFastMin && sum <= 3.0e38f) {
-        if (lane == 0) {
-            float mo;
-            int eo;
-            fa_split(sum, mo, eo);
-            a.bm[bmid + row] = mo;
-            a.be[bmid + row] = eo + R + er + a.rho[rnode * S + row];
+        if (sum >= kMsgFastMin && sum <= 3.0e38f) {
+            if (lane == 0) {
+                float mo;
+                int eo;
+                fa_split(sum, mo, eo);
+                a.bm[bmid + row] = mo;
+                a.be[bmid + row] = eo + R + er + a.rho[rnode * S + row];
+            }
+            continue;
         }
-        return;
-    }
-    // the exact form for this row
-    int e = FA_INT_NONE;
-    for (int q = lane; q < S; q += 32) {
-        const float v = Rrow[q];
-        if (v > 0.0f && sb[q] > 0.0f) e = max(e, se[q] + fa_exponent(v));
-    }
-    e = fa_warp_max_int(e);
-    float esum = 0.0f;
-    if (e != FA_INT_NONE)
+        // the exact form for this row
+        int e = FA_INT_NONE;
         for (int q = lane; q < S; q += 32) {
             const float v = Rrow[q];
-            if (v > 0.0f && sb[q] > 0.0f) {
-                float mv;
-                int ev;
-                fa_split(v, mv, ev);
-                esum += sb[q] * mv * fa_pow2(se[q] + ev - e);
-            }
+            if (v > 0.0f && sb[q] > 0.0f) e = max(e, se[q] + fa_exponent(v));
         }
-    esum = fa_warp_sum(esum);
-    if (lane == 0) {
-        float mo = 0.0f;
-        int eo = 0;
-        if (esum > 0.0f) { fa_split(esum, mo, eo); eo += e + a.rho[rnode * S + row]; }
-        a.bm[bmid + row] = mo;
-        a.be[bmid + row] = eo;
+        e = fa_warp_max_int(e);
+        float esum = 0.0f;
+        if (e != FA_INT_NONE)
+            for (int q = lane; q < S; q += 32) {
+                const float v = Rrow[q];
+                if (v > 0.0f && sb[q] > 0.0f) {
+                    float mv;
+                    int ev;
+                    fa_split(v, mv, ev);
+                    esum += sb[q] * mv * fa_pow2(se[q] + ev - e);
+                }
+            }
+        esum = fa_warp_sum(esum);
+        if (lane == 0) {
+            float mo = 0.0f;
+            int eo = 0;
+            if (esum > 0.0f) { fa_split(esum, mo, eo); eo += e + a.rho[rnode * S + row]; }
+            a.bm[bmid + row] = mo;
+            a.be[bmid + row] = eo;
+        }
     }
 }
 
@@ -2581,7 +2586,8 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
         ta.CB = S >= 64 ? 64 : ((S + 31) / 32) * 32;
         ta.QS = kThreads / ta.CB;
         ta.nA = B * ta.np * ((S + ta.CB - 1) / ta.CB);
-        ta.nB = B * ta.np * ((S + kWarps - 1) / kWarps);
+        ta.beta_rows = S >= 256 ? 4 * kWarps : kWarps;
+        ta.nB = B * ta.np * ((S + ta.beta_rows - 1) / ta.beta_rows);
         const int nM = (B * ta.np + kWarps - 1) / kWarps;
         ta.mant = F(p.mant[kk]); ta.rho = I(p.rho[kk]); ta.rmax = I(p.rmax[kk]);
         ta.vec4 = (S & 3) == 0;
