@@ -559,6 +559,14 @@ def run_native(args, rank, world, local):
     # in chunks of sequences that overlap the emission reweighting; for inputs of a few MB the
     # copies are short and a graph replay of the step after them launches faster
     use_host = args.method == "tree" and args.confidence == "marginal" and probs.numel() * 4 > (64 << 20)
+    # the host-to-device copy rate of this machine for the same bytes, for context
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        c0.record(stream)
+        probs.copy_(h_probs, non_blocking=True)
+        c1.record(stream)
+    torch.cuda.synchronize()
+    h2d_gbs = probs.numel() * 4 / (c0.elapsed_time(c1) * 1e6)
     with torch.cuda.stream(stream):
         for i in range(n_e2e):
             flush.zero_()
@@ -614,7 +622,8 @@ def run_native(args, rank, world, local):
             "stage_ms": per_stage,
             "e2e": {"value": replica_value(w.B * w.L, world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "call": "fa_constrained_step_host" if use_host else "host copies + the step"},
+                    "call": "fa_constrained_step_host" if use_host else "host copies + the step",
+                    "h2d_copy_gbs": h2d_gbs},
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
             "wall_s": wall, "row_status_ok": bool((status == 0).all()),
             "clocks": clock_summary}
