@@ -503,10 +503,33 @@ __global__ void __launch_bounds__(kThreads) k_rowshift(int S, int L, int k, int 
     const int32_t *rhoR = rho_c + rnode * S;
     const int32_t *rmaxR = rmax_c + rnode * S;
     int best = FA_INT_NONE;
-    for (int m = lane; m < S; m += 32) {
-        const float x = Lrow[m];
-        const int rr = rmaxR[m];
-        if (x > 0.0f && rr > 0) best = max(best, rhoR[m] + fa_exponent(__int_as_float(rr)) + fa_exponent(x));
+    if ((S & 3) == 0) {
+        // 16-byte loads, four in flight per lane
+        for (int m0 = 4 * lane; m0 < S; m0 += 512) {
+            float4 x[4];
+            int4 rr[4], rh[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int m = m0 + 128 * u;
+                x[u] = m < S ? __ldg(reinterpret_cast<const float4 *>(Lrow + m)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                rr[u] = m < S ? __ldg(reinterpret_cast<const int4 *>(rmaxR + m)) : make_int4(0, 0, 0, 0);
+                rh[u] = m < S ? __ldg(reinterpret_cast<const int4 *>(rhoR + m)) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                const int rs[4] = {rr[u].x, rr[u].y, rr[u].z, rr[u].w}, hs[4] = {rh[u].x, rh[u].y, rh[u].z, rh[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (xs[e] > 0.0f && rs[e] > 0) best = max(best, hs[e] + fa_exponent(__int_as_float(rs[e])) + fa_exponent(xs[e]));
+            }
+        }
+    } else {
+        for (int m = lane; m < S; m += 32) {
+            const float x = Lrow[m];
+            const int rr = rmaxR[m];
+            if (x > 0.0f && rr > 0) best = max(best, rhoR[m] + fa_exponent(__int_as_float(rr)) + fa_exponent(x));
+        }
     }
     best = fa_warp_max_int(best);
     if (lane == 0) mu[pnode * S + i] = best;
