@@ -7,6 +7,7 @@
 // indices inside their chunk or its zero pad slots.  Prints one line "bad=N ..." and exits non-zero when N > 0.
 #include "../constrained_decoding_diffusion_gb300/csrc/fa_compile.cu"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <map>
@@ -128,6 +129,28 @@ int main(int argc, char **argv) {
         bad += prev_r1 != S;
         for (int c = 0; c < nc; ++c) bad += seen[c] != 1;
     }
+    // shared-memory wavefronts per warp gather: distinct addresses in the busiest bank, over
+    // every step of every unit's stream (the zero pad slots count as addresses too)
+    long steps = 0, waves = 0;
+    for (int u = 0; u < rl.n_units; ++u)
+        for (int ch = 0; ch < nch; ++ch) {
+            const size_t ui = (size_t)u * nch + ch;
+            const int gb = rl.ru_goff[ui], ng = (rl.ru_goff[ui + 1] - gb) / 32;
+            for (int k = 0; k < ng; ++k)
+                for (int h = 0; h < G; ++h) {
+                    std::map<int, std::vector<int>> bank;
+                    int w = 1;
+                    for (int l = 0; l < 32; ++l) {
+                        const int idx = rl.ru_tok[((size_t)gb + (size_t)k * 32 + l) * G + h] & 0x7fff;
+                        auto &v = bank[idx & 31];
+                        if (std::find(v.begin(), v.end(), idx) == v.end()) v.push_back(idx);
+                        w = std::max(w, (int)v.size());
+                    }
+                    ++steps;
+                    waves += w;
+                }
+        }
+    printf("wavefronts_per_gather=%.3f ", steps ? (double)waves / steps : 1.0);
     printf("bad=%ld S=%d V=%d cells=%d incidences=%zu units=%d chunks=%d partitions=%zu entries_per_incidence=%.3f "
            "worst_rel=%.2e\n",
            bad, S, V, nc, cell_tok.size(), rl.n_units, nch, rl.part_count.size(),

@@ -52,3 +52,7 @@ def test_run_layout(harness, tmp_path, name):
     dump(CASES[name](), path)
     r = subprocess.run([harness, str(path)], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and "bad=0" in r.stdout, r.stdout + r.stderr
+    # the bank matching keeps a warp gather near one shared-memory wavefront (32 random
+    # addresses would need about 3.5; these small automata give 1.0-1.62, the workloads 1.09-1.22)
+    waves = float(r.stdout.split("wavefronts_per_gather=")[1].split()[0])
+    assert waves <= 1.75, r.stdout
