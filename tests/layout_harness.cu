@@ -151,6 +151,55 @@ int main(int argc, char **argv) {
                 }
         }
     printf("wavefronts_per_gather=%.3f ", steps ? (double)waves / steps : 1.0);
+    // token-major streams of the all-token marginals (build_token_streams): every token's
+    // incidences exactly once, padding (S, S) past its count, and the alpha / beta gathers'
+    // wavefronts after the bank ordering
+    {
+        std::vector<int64_t> tok_off(V + 1, 0);
+        for (int e = 0; e < E; ++e) for (int64_t q = lo[e]; q < lo[e + 1]; ++q) tok_off[lt[q] + 1]++;
+        for (int v = 0; v < V; ++v) tok_off[v + 1] += tok_off[v];
+        std::vector<int32_t> tok_edges(tok_off[V]);
+        std::vector<int64_t> fill(tok_off.begin(), tok_off.end() - 1);
+        for (int e = 0; e < E; ++e) for (int64_t q = lo[e]; q < lo[e + 1]; ++q) tok_edges[fill[lt[q]]++] = e;
+        std::vector<int32_t> perm;
+        std::vector<int64_t> goff;
+        std::vector<uint32_t> sd;
+        build_token_streams(S, V, tok_off, tok_edges, es.data(), ed.data(), perm, goff, sd);
+        const uint32_t pad = ((uint32_t)S << 16) | (uint32_t)S;
+        long wa = 0, wb = 0, rows = 0;
+        for (int64_t g = 0; g * 32 < V; ++g) {
+            for (int l = 0; l < 32 && g * 32 + l < V; ++l) {
+                const int v = perm[g * 32 + l];
+                std::vector<uint32_t> want, got;
+                for (int64_t q = tok_off[v]; q < tok_off[v + 1]; ++q)
+                    want.push_back(((uint32_t)es[tok_edges[q]] << 16) | (uint32_t)ed[tok_edges[q]]);
+                for (int64_t r = goff[g]; r < goff[g + 1]; ++r) {
+                    const uint32_t x = sd[(size_t)r * 32 + l];
+                    if (r - goff[g] < (int64_t)want.size()) got.push_back(x);
+                    else bad += x != pad;
+                }
+                std::sort(want.begin(), want.end());
+                std::sort(got.begin(), got.end());
+                bad += want != got;
+            }
+            for (int64_t r = goff[g]; r < goff[g + 1]; ++r) {
+                for (int which = 0; which < 2; ++which) {
+                    std::map<int, std::vector<int>> bank;
+                    int w = 1;
+                    for (int l = 0; l < 32; ++l) {
+                        const uint32_t x = sd[(size_t)r * 32 + l];
+                        const int a = which == 0 ? (int)(x >> 16) : S + 1 + (int)(x & 0xffffu);
+                        auto &vv = bank[a & 31];
+                        if (std::find(vv.begin(), vv.end(), a) == vv.end()) vv.push_back(a);
+                        w = std::max(w, (int)vv.size());
+                    }
+                    (which == 0 ? wa : wb) += w;
+                }
+                ++rows;
+            }
+        }
+        printf("token_rows_wavefronts=%.3f/%.3f ", rows ? (double)wa / rows : 1.0, rows ? (double)wb / rows : 1.0);
+    }
     printf("bad=%ld S=%d V=%d cells=%d incidences=%zu units=%d chunks=%d partitions=%zu entries_per_incidence=%.3f "
            "worst_rel=%.2e\n",
            bad, S, V, nc, cell_tok.size(), rl.n_units, nch, rl.part_count.size(),

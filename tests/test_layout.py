@@ -1,6 +1,8 @@
-"""The reweight's run layout, checked on the host (no GPU): tests/layout_harness.cu builds
-the layout with the library's own build_run_layout, replays the kernel's walk over the
-entry streams and compares every cell sum with float64, on automata covering one and
+"""The reweight's run layout and the all-token pass's token streams, checked on the host (no
+GPU): tests/layout_harness.cu builds the layout with the library's own build_run_layout,
+replays the kernel's walk over the entry streams and compares every cell sum with float64,
+and builds the token-major incidence streams with build_token_streams and checks that every
+token's incidences appear once (padding past its count), on automata covering one and
 several vocabulary chunks, small and large rows, parallel edges and many states."""
 import os
 import shutil
