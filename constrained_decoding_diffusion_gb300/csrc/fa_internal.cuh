@@ -217,4 +217,5 @@ size_t fa_span_tc_image_bytes(int S, long products);
 fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant_c, const int32_t *rho_c,
                            const int32_t *rmax_c, const int32_t *rminc_c, int nc, const int32_t *mu, float *mant_p,
                            int32_t *rho_p, int32_t *rmax_p, int32_t *rminc_p, int32_t *err, int32_t *range_lost,
-                           void *img, cudaStream_t stream);
+                           void *img, cudaStream_t stream, const int32_t *fflag_p = nullptr,
+                           const int32_t *fmap_p = nullptr);

@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
                                                 const int32_t *__restrict__ rmax_c,
                                                 const int32_t *__restrict__ rminc_c, int nc,
                                                 const int32_t *__restrict__ mu, unsigned char *img,
-                                                int32_t *range_lost) {
+                                                int32_t *range_lost, const int32_t *__restrict__ fflag_p) {
     const int tid = threadIdx.x;
     const int tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN, nkt = (S + TK - 1) / TK;
     const int per = tiles_m + tiles_n;
@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(NTHR) k_tc_prep(int S, int L, int k, int nk, c
     const int kt0 = kc * PREP_KT, kt1 = min(nkt, kt0 + PREP_KT);
     const int node = (int)(bn % nk), b = (int)(bn / nk);
     if (((2 * node + 1) << (k - 1)) >= L) return;     // a copy, no product
+    if (fflag_p && fflag_p[bn]) return;               // a functional span: no product either
     const size_t SS = (size_t)S * S;
     const size_t pnode = (size_t)b * nk + node;
     const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
@@ -242,7 +243,9 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
                                                     const int32_t *__restrict__ rminc_c, int nc,
                                                     const int32_t *__restrict__ mu, const unsigned char *__restrict__ img,
                                                     float *mant_p, int32_t *rho_p, int32_t *rmax_p, int32_t *rminc_p,
-                                                    int32_t *err, int inject_timeout) {
+                                                    int32_t *err, int inject_timeout,
+                                                    const int32_t *__restrict__ fflag_p,
+                                                    const int32_t *__restrict__ fmap_p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ uint64_t full[NSTAGE], empty[NSTAGE], done, never;
     __shared__ uint32_t tmem_base_s;
@@ -269,6 +272,23 @@ __global__ void __launch_bounds__(NTHR, 1) k_span_tc(int S, int L, int k, int nk
                 rho_p[pnode * S + r] = rho_c[lnode * S + r];
                 rmax_p[pnode * S + r] = rmax_c[lnode * S + r];
                 rminc_p[pnode * S + r] = rminc_c[lnode * S + r];
+            }
+        return;
+    }
+    if (fflag_p && fflag_p[pnode]) {
+        // a functional span: the 0/1 matrix of its partial function, row exponents 0 -- what
+        // the product of the two 0/1 matrices gives -- written without the MMAs
+        const int32_t *fm = fmap_p + pnode * S;
+        for (int q = tid; q < TM * TN; q += NTHR) {
+            const int r = i0 + q / TN, c = j0 + q % TN;
+            if (r < S && c < S) C[(size_t)r * S + c] = fm[r] == c ? 1.0f : 0.0f;
+        }
+        if (tn == 0)
+            for (int r = i0 + tid; r < min(i0 + TM, S); r += NTHR) {
+                const bool one = fm[r] >= 0;
+                rho_p[pnode * S + r] = 0;
+                rmax_p[pnode * S + r] = one ? __float_as_int(1.0f) : 0;
+                rminc_p[pnode * S + r] = one ? 0x7fffffff - __float_as_int(1.0f) : 0;
             }
         return;
     }
@@ -421,14 +441,14 @@ size_t fa_span_tc_image_bytes(int S, long products) {
 fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant_c, const int32_t *rho_c,
                            const int32_t *rmax_c, const int32_t *rminc_c, int nc, const int32_t *mu, float *mant_p,
                            int32_t *rho_p, int32_t *rmax_p, int32_t *rminc_p, int32_t *err, int32_t *range_lost,
-                           void *img, cudaStream_t stream) {
+                           void *img, cudaStream_t stream, const int32_t *fflag_p, const int32_t *fmap_p) {
     const size_t smem = fa_span_tc_smem(S);
     cudaError_t e = cudaFuncSetAttribute(k_span_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     const long tiles_m = (S + TM - 1) / TM, tiles_n = (S + TN - 1) / TN;
     const long kch = ((S + TK - 1) / TK + PREP_KT - 1) / PREP_KT;
     k_tc_prep<<<(unsigned)((long)B * nk * (tiles_m + tiles_n) * kch), NTHR, 0, stream>>>(
-        S, L, k, nk, mant_c, rho_c, rmax_c, rminc_c, nc, mu, (unsigned char *)img, range_lost);
+        S, L, k, nk, mant_c, rho_c, rmax_c, rminc_c, nc, mu, (unsigned char *)img, range_lost, fflag_p);
     e = cudaGetLastError();
     if (e != cudaSuccess) { fa_set_error(std::string("operand images (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     const long grid = (long)B * nk * tiles_m * tiles_n;
@@ -437,7 +457,7 @@ fa_status fa_span_tc_level(int S, int B, int L, int k, int nk, const float *mant
         if (g_inject_timeouts.compare_exchange_weak(n, n - 1)) inject = 1;
     k_span_tc<<<(unsigned)grid, NTHR, smem, stream>>>(S, L, k, nk, mant_c, rho_c, rmax_c, rminc_c, nc, mu,
                                                       (const unsigned char *)img, mant_p, rho_p, rmax_p, rminc_p, err,
-                                                      inject);
+                                                      inject, fflag_p, fmap_p);
     e = cudaGetLastError();
     if (e != cudaSuccess) { fa_set_error(std::string("span product (tensor cores): ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     return FA_OK;

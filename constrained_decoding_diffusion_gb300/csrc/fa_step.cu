@@ -37,6 +37,10 @@ struct Plan {
     size_t z = 0, am = 0, ae = 0, bm = 0, be = 0, keys = 0, conf = 0, den_m = 0, den_e = 0, tm_part = 0, zsum = 0, zexp = 0;
     int tm_chunks = 1, tm_chunk = kTmChunkMax;
     size_t rmax_hi = 0, rmax_hi_bytes = 0, leaf_done = 0, tc_err = 0, range_lost = 0, img = 0;
+    // functional spans (a DFA on the tensor-core path): per tree level, one flag per node and,
+    // for flagged nodes, the partial function s -> the one state its row reaches (-1: none)
+    bool functional = false;
+    size_t fflag[18] = {0}, fmap[18] = {0};
     size_t total = 0;
 };
 
@@ -97,6 +101,13 @@ Plan make_plan(const fa_automaton *a, int B, int L) {
     if (fa_span_tc_supported(a->S) && p.K >= 1) p.img = take(fa_span_tc_image_bytes(a->S, (long)B * p.nk[1]));
     p.zsum = take((size_t)B * sizeof(float));
     p.zexp = take((size_t)B * sizeof(int32_t));
+    p.functional = a->is_dfa && fa_span_tc_supported(a->S) && p.K >= 1;
+    if (p.functional)
+        for (int k = 0; k <= p.K; ++k) {
+            const size_t nodes = (size_t)B * (size_t)p.nk[k];
+            p.fflag[k] = take(nodes * sizeof(int32_t));
+            p.fmap[k] = take(nodes * S * sizeof(int32_t));
+        }
     p.total = off;
     return p;
 }
@@ -232,7 +243,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
                                                                 const int4 *__restrict__ rbm, int nrb, int tot_floats,
                                                                     float *mant, int32_t *rho, int32_t *rmax,
                                                                     int32_t *rminc, int32_t *zero, long n_zero,
-                                                                    int tile) {
+                                                                    int tile, int32_t *fflag, int32_t *fmap) {
     extern __shared__ float smem_f[];
     const int nthr = blockDim.x;
     // clear the row maxima of the higher tree levels (their products accumulate with atomicMax)
@@ -264,6 +275,9 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
     // (s, s') pair of the rows
     if (c >= 0 || (!tile && c1 - c0 < (r1 - r0) * S))
         for (size_t i = (size_t)r0 * S + tid; i < (size_t)r1 * S; i += nthr) M[i] = 0.0f;
+    // functional spans (DFA): a committed position's M_t is the partial function s -> the
+    // target of the edge from s carrying its token; a masked position's is not functional
+    if (fflag && r == 0 && tid == 0) fflag[pos] = c >= 0 ? 1 : 0;
     if (c < 0) {
         const float *prow = probs + pos * (size_t)fa.V;
         const bool aligned = (reinterpret_cast<uintptr_t>(prow) & 15) == 0 && (CH & 3) == 0;
@@ -445,7 +459,11 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
             return;
         }
     } else {
-        for (int i = tid; i < r1 - r0; i += nthr) { smax[i] = 0; smin[i] = 0; }
+        for (int i = tid; i < r1 - r0; i += nthr) {
+            smax[i] = 0;
+            smin[i] = 0;
+            if (fmap) fmap[pos * S + r0 + i] = -1;
+        }
         __syncthreads();
         if (c < fa.V) {
             const int64_t a0 = fa.tok_off[c], a1 = fa.tok_off[c + 1];
@@ -455,6 +473,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
                 if (s >= r0 && s < r1) {
                     if constexpr (MAX) M[(size_t)s * S + fa.edge_dst[e]] = 1.0f;
                     else atomicAdd(&M[(size_t)s * S + fa.edge_dst[e]], 1.0f);
+                    if (fmap) fmap[pos * S + s] = fa.edge_dst[e];   // one edge per (s, token) in a DFA
                 }
             }
             __syncthreads();
@@ -489,7 +508,7 @@ __global__ void __launch_bounds__(32 * FA_RW_WARPS, 2) k_reweight(DevFA fa, int 
 __global__ void __launch_bounds__(kThreads) k_rowshift(int S, int L, int k, int nk, const float *__restrict__ mant_c,
                                                      const int32_t *__restrict__ rho_c,
                                                      const int32_t *__restrict__ rmax_c, int nc, int32_t *mu,
-                                                     int32_t *rmax_p) {
+                                                     int32_t *rmax_p, const int32_t *__restrict__ fflag_p) {
     const int b = blockIdx.z, j = blockIdx.y;
     const int i = blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -497,7 +516,7 @@ __global__ void __launch_bounds__(kThreads) k_rowshift(int S, int L, int k, int 
     const size_t pnode = (size_t)b * nk + j;
     if (lane == 0) rmax_p[pnode * S + i] = 0;
     const bool has_right = ((2 * j + 1) << (k - 1)) < L;
-    if (!has_right) return;
+    if (!has_right || (fflag_p && fflag_p[pnode])) return;   // a copy, or a functional span
     const size_t lnode = (size_t)b * nc + 2 * j, rnode = lnode + 1;
     const float *Lrow = mant_c + lnode * (size_t)S * S + (size_t)i * S;
     const int32_t *rhoR = rho_c + rnode * S;
@@ -533,6 +552,30 @@ __global__ void __launch_bounds__(kThreads) k_rowshift(int S, int L, int k, int 
     }
     best = fa_warp_max_int(best);
     if (lane == 0) mu[pnode * S + i] = best;
+}
+
+// Functional spans of tree level k (a DFA, tensor-core path): a node is functional when its
+// children are (a copy node, whose right child is padding, when its left child is), and its
+// partial function composes theirs, f(s) = f_R(f_L(s)).  Such a span is the 0/1 matrix of
+// that function with row exponents 0 -- exactly what the product of the two 0/1 matrices
+// gives -- so the level's products skip it and write the matrix from the function.  One block
+// per node.
+__global__ void __launch_bounds__(kThreads) k_func_level(int S, int L, int k, int nk, int nc,
+                                                       const int32_t *__restrict__ fflag_c,
+                                                       const int32_t *__restrict__ fmap_c, int32_t *fflag_p,
+                                                       int32_t *fmap_p) {
+    const long pn = blockIdx.x;                    // b * nk + node
+    const int node = (int)(pn % nk), b = (int)(pn / nk);
+    const size_t lnode = (size_t)b * nc + 2 * node, rnode = lnode + 1;
+    const bool has_right = ((2 * node + 1) << (k - 1)) < L;
+    const int f = fflag_c[lnode] && (!has_right || fflag_c[rnode]);
+    if (threadIdx.x == 0) fflag_p[pn] = f;
+    if (!f) return;
+    const int32_t *fl = fmap_c + lnode * S, *fr = fmap_c + rnode * S;
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+        const int m = fl[i];
+        fmap_p[(size_t)pn * S + i] = m < 0 ? -1 : (has_right ? fr[m] : m);
+    }
 }
 
 // |S| <= 64: a product C = A_L A_R of one node is split into 32x32 output tiles, one block
@@ -2194,7 +2237,8 @@ fa_status check_device(const fa_automaton *a, const char *fn) {
 
 fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *probs, const int32_t *committed,
                           float *mant, int32_t *rho, int32_t *rmax, int32_t *rminc, cudaStream_t st,
-                          int32_t *zero = nullptr, long n_zero = 0, bool use_max = false) {
+                          int32_t *zero = nullptr, long n_zero = 0, bool use_max = false,
+                          int32_t *fflag = nullptr, int32_t *fmap = nullptr) {
     const int p = pick_partition(a, (long)B * L);
     const int nrb = a->part_count[p];
     const int4 *rbm = reinterpret_cast<const int4 *>(a->rb_meta) + 2 * a->part_first[p];
@@ -2217,7 +2261,7 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     // units per warp: the register totals of a third unit cost the smaller layouts ~10%
     const int upw = (max_units + FA_RW_WARPS - 1) / FA_RW_WARPS;
     using K = void (*)(DevFA, int, const float *, const int32_t *, const int4 *, int, int, float *, int32_t *, int32_t *,
-                       int32_t *, int32_t *, long, int);
+                       int32_t *, int32_t *, long, int, int32_t *, int32_t *);
     K kern = upw <= 1 ? (use_max ? (K)k_reweight<true, 1> : (K)k_reweight<false, 1>)
              : upw == 2 ? (use_max ? (K)k_reweight<true, 2> : (K)k_reweight<false, 2>)
                         : (use_max ? (K)k_reweight<true, 3> : (K)k_reweight<false, 3>);
@@ -2227,7 +2271,7 @@ fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *prob
     }
     dim3 grid((unsigned)((long)L * nrb), (unsigned)B);
     kern<<<grid, threads, smem, st>>>(dev_view(a), L, probs, committed, rbm, nrb, tot_floats, mant, rho, rmax, rminc,
-                                      zero, n_zero, tile);
+                                      zero, n_zero, tile, fflag, fmap);
     return launch_check("reweight");
 }
 
@@ -2323,7 +2367,7 @@ extern "C" fa_status fa_map_step(const fa_automaton *aut, int32_t B, int32_t L, 
         }
         dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
         k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
-                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
+                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]), nullptr);
         if ((st = launch_check("rowshift")) != FA_OK) return st;
         const long tiles = (S + GBN - 1) / GBN;
         k_gemm_simt<true><<<(unsigned)((long)B * p.nk[kk] * tiles * tiles), kThreads, 0, s>>>(
@@ -2464,7 +2508,7 @@ fa_status copy_context(CopyContext *&out) {
 // of later chunks overlap the reweighting of earlier ones.
 fa_status reweight_from_host(const fa_automaton *a, int B, int L, const HostInput &hin, float *d_probs,
                              int32_t *d_committed, float *mant, int32_t *rho, int32_t *rmax, int32_t *rminc,
-                             cudaStream_t s, int32_t *zero, long n_zero) {
+                             cudaStream_t s, int32_t *zero, long n_zero, int32_t *fflag, int32_t *fmap) {
     CopyContext *c = nullptr;
     fa_status st = copy_context(c);
     if (st != FA_OK) return st;
@@ -2492,7 +2536,8 @@ fa_status reweight_from_host(const fa_automaton *a, int B, int L, const HostInpu
         const size_t pos0 = b0 * Ls;
         st = launch_reweight(a, (int)(b1 - b0), L, d_probs + pos0 * V, d_committed + pos0, mant + pos0 * S * S,
                              rho + pos0 * S, rmax + pos0 * S, rminc + pos0 * S, s, i == 0 ? zero : nullptr,
-                             i == 0 ? n_zero : 0);
+                             i == 0 ? n_zero : 0, false, fflag ? fflag + pos0 : nullptr,
+                             fmap ? fmap + pos0 * S : nullptr);
         if (st != FA_OK) return st;
     }
     return FA_OK;
@@ -2539,10 +2584,12 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
     if (hin)
         st = reweight_from_host(aut, B, L, *hin, const_cast<float *>(probs), const_cast<int32_t *>(committed),
                                 F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), I(p.rminc[0]), s, I(p.rmax_hi),
-                                (long)(p.rmax_hi_bytes / sizeof(int32_t)));
+                                (long)(p.rmax_hi_bytes / sizeof(int32_t)), p.functional ? I(p.fflag[0]) : nullptr,
+                                p.functional ? I(p.fmap[0]) : nullptr);
     else
         st = launch_reweight(aut, B, L, probs, committed, F(p.mant[0]), I(p.rho[0]), I(p.rmax[0]), I(p.rminc[0]), s,
-                             I(p.rmax_hi), (long)(p.rmax_hi_bytes / sizeof(int32_t)));
+                             I(p.rmax_hi), (long)(p.rmax_hi_bytes / sizeof(int32_t)), false,
+                             p.functional ? I(p.fflag[0]) : nullptr, p.functional ? I(p.fmap[0]) : nullptr);
     if (st != FA_OK) return st;
 
     if (chain) {
@@ -2575,15 +2622,26 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
             if ((st = launch_check("span product (small)")) != FA_OK) return st;
             continue;
         }
+        // functional spans of this level (a DFA on the tensor-core path), before its products
+        int32_t *fflag_k = nullptr, *fmap_k = nullptr;
+        if (p.functional) {
+            fflag_k = I(p.fflag[kk]);
+            fmap_k = I(p.fmap[kk]);
+            k_func_level<<<(unsigned)((long)B * p.nk[kk]), kThreads, 0, s>>>(S, L, kk, p.nk[kk], p.nk[kk - 1],
+                                                                             I(p.fflag[kk - 1]), I(p.fmap[kk - 1]),
+                                                                             fflag_k, fmap_k);
+            if ((st = launch_check("functional spans")) != FA_OK) return st;
+        }
         dim3 g1((S + kWarps - 1) / kWarps, p.nk[kk], B);
         k_rowshift<<<g1, kThreads, 0, s>>>(S, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
-                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]));
+                                           p.nk[kk - 1], I(p.mu[kk]), I(p.rmax[kk]), fflag_k);
         if ((st = launch_check("rowshift")) != FA_OK) return st;
         if (fa_span_tc_supported(S)) {
             g_launches.fetch_add(2, std::memory_order_relaxed);
             st = fa_span_tc_level(S, B, L, kk, p.nk[kk], F(p.mant[kk - 1]), I(p.rho[kk - 1]), I(p.rmax[kk - 1]),
                                   I(p.rminc[kk - 1]), p.nk[kk - 1], I(p.mu[kk]), F(p.mant[kk]), I(p.rho[kk]),
-                                  I(p.rmax[kk]), I(p.rminc[kk]), I(p.tc_err), I(p.range_lost), ws + p.img, s);
+                                  I(p.rmax[kk]), I(p.rminc[kk]), I(p.tc_err), I(p.range_lost), ws + p.img, s, fflag_k,
+                                  fmap_k);
             if (st != FA_OK) return st;
             continue;
         }

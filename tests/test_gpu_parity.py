@@ -453,3 +453,33 @@ def test_messages_keep_states_far_below_the_largest(native, S):
     assert 0.2 < p_a < 0.8, p_a
     n_a = int((res["tokens"][:, 0] == 0).sum())
     assert abs(n_a - B * p_a) <= 4.5 * math.sqrt(B * p_a * (1 - p_a)), (n_a, B * p_a)
+
+
+@pytest.mark.parametrize("S", [128, 256])
+def test_committed_ranges_functional_spans(native, S):
+    """A DFA on the tensor-core path with long committed ranges, as in the later steps of a
+    block-wise schedule: spans over committed positions are 0/1 partial functions, composed
+    instead of multiplied (level 1 up to the root for an all-committed sequence).  Every row
+    matches the oracle: all masked, a committed prefix, a committed suffix with a few holes,
+    committed except one position, and all committed."""
+    rng = np.random.default_rng(40 + S)
+    fa = synth.random_dfa(S, 2000, 0.8, 16, seed=S + 3)
+    o = oracle.OracleFA(fa)
+    aut = native.fa_compile(fa)
+    B, L = 5, 64
+    probs = synth.gaussian_probs(rng, B, L, 2000, 3.0)
+    committed = np.full((B, L), -1, np.int32)
+    for b in range(1, B):
+        x = synth.random_accepted_string(fa, L, rng)
+        if b == 1:
+            committed[b, :40] = x[:40]
+        elif b == 2:
+            committed[b, 8:] = x[8:]
+            committed[b, [20, 33, 50]] = -1
+        elif b == 3:
+            committed[b] = x
+            committed[b, 31] = -1
+        else:
+            committed[b] = x
+    res = run_step(aut, probs, committed, seed=6, offset=2, k=4)
+    check_against_oracle(fa, o, probs, committed, res, 4)
