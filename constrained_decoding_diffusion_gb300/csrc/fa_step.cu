@@ -935,6 +935,7 @@ struct TopdownArgs {
     int vec4;             // |S| % 4 == 0: 16-byte loads in the message passes
     int beta_rows;        // rows per beta block: a multiple of the warps, more for large |S| so
                           // that the staging of beta_r is shared by more rows
+    const int32_t *fflag, *fmap;   // functional spans of the level (nullptr: none)
     uint64_t seed, offset;
     int32_t *z, *status;
     float *am, *bm;
@@ -1035,6 +1036,32 @@ __device__ void topdown_alpha(const TopdownArgs &a, int blk, float *sm) {
     }
     if (threadIdx.x == 0) need_exact = 0;
     const int R = fa_block_max_int(w, red);
+    if (a.fflag && a.fflag[lnode]) {
+        // a functional span (committed positions of a DFA): alpha_m(d) is the sum of alpha_l(s)
+        // over the states s its function maps to d, each term with its own exponent -- the
+        // largest exponent first, then the sum scaled by it; the span is not read
+        int *fm = reinterpret_cast<int *>(sf);
+        for (int q = threadIdx.x; q < S; q += kThreads) fm[q] = a.fmap[lnode * S + q];
+        __syncthreads();
+        if (threadIdx.x < CB) {
+            const int d = cbk * CB + threadIdx.x;
+            if (d < S) {
+                int E = FA_INT_NONE;
+                for (int q = 0; q < S; ++q)
+                    if (fm[q] == d && sa[q] > 0.0f) E = max(E, sc[q] + fa_exponent(sa[q]));
+                float sum = 0.0f;
+                if (E != FA_INT_NONE)
+                    for (int q = 0; q < S; ++q)
+                        if (fm[q] == d && sa[q] > 0.0f) sum += fa_mul_pow2(sa[q], sc[q] - E);
+                float mo = 0.0f;
+                int eo = 0;
+                if (sum > 0.0f) { fa_split(sum, mo, eo); eo += E; }
+                a.am[bmid + d] = mo;
+                a.ae[bmid + d] = eo;
+            }
+        }
+        return;
+    }
     for (int q = threadIdx.x; q < S; q += kThreads) {
         sf[q] = (sa[q] > 0.0f && R != FA_INT_NONE) ? fa_mul_pow2(sa[q], sc[q] - R) : 0.0f;
         sz[q] = sa[q] > 0.0f ? 1.0f : 0.0f;
@@ -1198,6 +1225,16 @@ __device__ void topdown_beta(const TopdownArgs &a, int blk, float *sm) {
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
+    const size_t rnode_f = (size_t)b * a.nc + 2 * j + 1;
+    if (a.fflag && a.fflag[rnode_f]) {
+        // a functional span: beta_m(s) = beta_r(f(s)) (row exponents 0); the span is not read
+        for (int row = rbk * RB + threadIdx.x; row < min(S, (rbk + 1) * RB); row += kThreads) {
+            const int t = a.fmap[rnode_f * S + row];
+            a.bm[bmid + row] = t >= 0 ? sb[t] : 0.0f;
+            a.be[bmid + row] = t >= 0 ? se[t] : 0;
+        }
+        return;
+    }
     // warp w takes rows rbk * RB + w, + kWarps, ... of the block's RB rows
     for (int row = rbk * RB + (threadIdx.x >> 5); row < min(S, (rbk + 1) * RB); row += kWarps) {
         const size_t rnode = (size_t)b * a.nc + 2 * j + 1;
@@ -2668,6 +2705,8 @@ fa_status step_impl(const fa_automaton *aut, int32_t B, int32_t L, const float *
         ta.QS = kThreads / ta.CB;
         ta.nA = B * ta.np * ((S + ta.CB - 1) / ta.CB);
         ta.beta_rows = S >= 256 ? 4 * kWarps : kWarps;
+        ta.fflag = p.functional ? I(p.fflag[kk]) : nullptr;
+        ta.fmap = p.functional ? I(p.fmap[kk]) : nullptr;
         ta.nB = B * ta.np * ((S + ta.beta_rows - 1) / ta.beta_rows);
         const int nM = (B * ta.np + kWarps - 1) / kWarps;
         ta.mant = F(p.mant[kk]); ta.rho = I(p.rho[kk]); ta.rmax = I(p.rmax[kk]);
