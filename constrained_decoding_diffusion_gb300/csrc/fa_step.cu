@@ -234,7 +234,11 @@ __device__ __forceinline__ void rw_group_end(float s, uint32_t x, uint32_t dummy
 // adds the staged probabilities of its entries and, at each run end, stores the run's chunk
 // sum into its slot; after each walk the lane folds those slots into the unit's register
 // totals, in chunk order.  After the last chunk the totals go to the freed chunk buffer and
-// every cell adds its runs' totals in a fixed order, so the result is deterministic.
+// every cell adds its runs' totals in a fixed order, so the result is deterministic; with
+// tile != 0 the block's rows are assembled in shared memory and written whole, each with its
+// maximum and smallest nonzero entry.  fflag / fmap (non-null for a DFA on the tensor-core
+// path): whether the position's M_t is a partial function (a committed position) and that
+// function, s -> the target of the edge from s carrying the token (-1: none).
 // MAX = true: the max-product variant for greedy decoding, M_t(s, s') = max over the tokens of
 // the edges s -> s' of w_t(v) (a committed position: 1 where an edge carries its token).
 template <bool MAX, int UPW>
