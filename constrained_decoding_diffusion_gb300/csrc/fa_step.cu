@@ -24,7 +24,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kHostChunks = 8;  // sequence chunks of fa_constrained_step_host's input copies
+constexpr int kHostChunks = 8;  // pieces of fa_constrained_step_host's input copies
 constexpr int kTmChunkMax = 4096, kTmChunkMin = 1024;  // tokens per block of the all-token marginals
 constexpr int kWarps = kThreads / 32;
 
@@ -2279,8 +2279,10 @@ fa_status check_device(const fa_automaton *a, const char *fn) {
 fa_status launch_reweight(const fa_automaton *a, int B, int L, const float *probs, const int32_t *committed,
                           float *mant, int32_t *rho, int32_t *rmax, int32_t *rminc, cudaStream_t st,
                           int32_t *zero = nullptr, long n_zero = 0, bool use_max = false,
-                          int32_t *fflag = nullptr, int32_t *fmap = nullptr) {
-    const int p = pick_partition(a, (long)B * L);
+                          int32_t *fflag = nullptr, int32_t *fmap = nullptr, long layout_positions = -1) {
+    // the row-block layout is chosen by the whole batch's positions (layout_positions when a
+    // batch is reweighted in pieces, so every piece sums its cells exactly as the whole would)
+    const int p = pick_partition(a, layout_positions >= 0 ? layout_positions : (long)B * L);
     const int nrb = a->part_count[p];
     const int4 *rbm = reinterpret_cast<const int4 *>(a->rb_meta) + 2 * a->part_first[p];
     const int max_units = a->part_max_units[p];
@@ -2467,7 +2469,8 @@ extern "C" fa_status fa_constrained_step(const fa_automaton *aut, int32_t B, int
 
 namespace {
 // Inputs still in host memory (fa_constrained_step_host): copied into the device buffers
-// probs / committed in sequence chunks, each chunk's reweighting started once it has landed.
+// probs / committed in pieces of positions, each piece's reweighting started once it has
+// landed.
 struct HostInput {
     const float *probs;
     const int32_t *committed;
@@ -2543,42 +2546,49 @@ fa_status copy_context(CopyContext *&out) {
     return FA_OK;
 }
 
-// Emission reweighting from host inputs: the committed tokens and then the probabilities of
-// up to kHostChunks chunks of sequences are copied on the copy stream (after the work already
-// on `s`), and the reweighting of each chunk runs on `s` once its rows are in, so the copies
-// of later chunks overlap the reweighting of earlier ones.
+// Emission reweighting from host inputs: the committed tokens and then the probabilities are
+// copied on the copy stream (after the work already on `s`) in up to kHostChunks pieces of
+// consecutive positions, and the reweighting of each piece runs on `s` once its rows are in,
+// so the copies of later pieces overlap the reweighting of earlier ones.
 fa_status reweight_from_host(const fa_automaton *a, int B, int L, const HostInput &hin, float *d_probs,
                              int32_t *d_committed, float *mant, int32_t *rho, int32_t *rmax, int32_t *rminc,
                              cudaStream_t s, int32_t *zero, long n_zero, int32_t *fflag, int32_t *fmap) {
     CopyContext *c = nullptr;
     fa_status st = copy_context(c);
     if (st != FA_OK) return st;
-    const size_t S = (size_t)a->S, V = (size_t)a->V, Ls = (size_t)L;
-    const int nch = std::min(B, kHostChunks), per = (B + nch - 1) / nch;
+    const size_t S = (size_t)a->S, V = (size_t)a->V, P = (size_t)B * (size_t)L;
+    // piece bounds in positions: a first piece of P / 32, each next one 1.4 times the last
+    // (so that its copy lands while the previous piece is reweighted, for a copy up to 1.4
+    // times slower per position than the reweighting), the last piece the rest
+    size_t bound[kHostChunks + 1];
+    int nch = 0;
+    bound[0] = 0;
+    double len = (double)std::max<size_t>(1, P / 32);
+    while (bound[nch] < P) {
+        bound[nch + 1] = nch == kHostChunks - 1 ? P : std::min(P, bound[nch] + (size_t)len);
+        ++nch;
+        len *= 1.4;
+    }
     cudaError_t e = cudaEventRecord(c->start, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->cs, c->start, 0);
     if (e == cudaSuccess)
-        e = cudaMemcpyAsync(d_committed, hin.committed, (size_t)B * Ls * sizeof(int32_t), cudaMemcpyHostToDevice, c->cs);
+        e = cudaMemcpyAsync(d_committed, hin.committed, P * sizeof(int32_t), cudaMemcpyHostToDevice, c->cs);
     if (e == cudaSuccess) e = cudaEventRecord(c->com, c->cs);
     for (int i = 0; i < nch && e == cudaSuccess; ++i) {
-        const size_t b0 = (size_t)i * per, b1 = std::min((size_t)B, b0 + per);
-        if (b0 >= b1) break;
-        e = cudaMemcpyAsync(d_probs + b0 * Ls * V, hin.probs + b0 * Ls * V, (b1 - b0) * Ls * V * sizeof(float),
-                            cudaMemcpyHostToDevice, c->cs);
+        e = cudaMemcpyAsync(d_probs + bound[i] * V, hin.probs + bound[i] * V,
+                            (bound[i + 1] - bound[i]) * V * sizeof(float), cudaMemcpyHostToDevice, c->cs);
         if (e == cudaSuccess) e = cudaEventRecord(c->chunk[i], c->cs);
     }
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->com, 0);
     if (e != cudaSuccess) { fa_set_error(std::string("host inputs: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
     for (int i = 0; i < nch; ++i) {
-        const size_t b0 = (size_t)i * per, b1 = std::min((size_t)B, b0 + per);
-        if (b0 >= b1) break;
         e = cudaStreamWaitEvent(s, c->chunk[i], 0);
         if (e != cudaSuccess) { fa_set_error(std::string("host inputs: ") + cudaGetErrorString(e)); return FA_ERR_CUDA; }
-        const size_t pos0 = b0 * Ls;
-        st = launch_reweight(a, (int)(b1 - b0), L, d_probs + pos0 * V, d_committed + pos0, mant + pos0 * S * S,
-                             rho + pos0 * S, rmax + pos0 * S, rminc + pos0 * S, s, i == 0 ? zero : nullptr,
-                             i == 0 ? n_zero : 0, false, fflag ? fflag + pos0 : nullptr,
-                             fmap ? fmap + pos0 * S : nullptr);
+        const size_t p0 = bound[i];
+        st = launch_reweight(a, 1, (int)(bound[i + 1] - p0), d_probs + p0 * V, d_committed + p0, mant + p0 * S * S,
+                             rho + p0 * S, rmax + p0 * S, rminc + p0 * S, s, i == 0 ? zero : nullptr,
+                             i == 0 ? n_zero : 0, false, fflag ? fflag + p0 : nullptr, fmap ? fmap + p0 * S : nullptr,
+                             (long)P);
         if (st != FA_OK) return st;
     }
     return FA_OK;

@@ -226,7 +226,7 @@ def fa_constrained_step_host(aut: CompiledAutomaton, h_probs, h_committed, d_pro
                              philox_offset: int, k: int, commit_lo: int, commit_hi: int, workspace, tokens, logZ,
                              marg, commit_idx, row_status, stream=None):
     """fa_constrained_step with the inputs in (page-locked) host tensors: copied into d_probs
-    and d_committed in chunks of sequences, overlapped with the emission reweighting."""
+    and d_committed in pieces of positions, overlapped with the emission reweighting."""
     import torch
     B, L, V = h_probs.shape
     ws_bytes = workspace.numel() * workspace.element_size()

@@ -241,10 +241,11 @@ fa_status fa_constrained_step_ex(const fa_automaton *aut, int32_t B, int32_t L, 
  *   d_committed  [B, L] int32 device, caller-owned: receives the copy of h_committed
  *   every other argument and output as for fa_constrained_step (outputs in device memory)
  *
- * The committed tokens and then the probabilities, in up to eight chunks of sequences, are
+ * The committed tokens and then the probabilities, in up to eight pieces of consecutive
+ * positions (the first a thirty-second of the batch, each next one 1.4 times larger), are
  * copied on a copy stream the library keeps per host thread and device, after the work
- * already queued on `stream`; the emission reweighting of each chunk starts on `stream` as
- * soon as its rows have landed, so the copy of later chunks overlaps the reweighting of
+ * already queued on `stream`; the emission reweighting of each piece starts on `stream` as
+ * soon as its rows have landed, so the copy of later pieces overlaps the reweighting of
  * earlier ones.  The results are those of fa_constrained_step on the copied inputs, bit for
  * bit.  The host buffers must stay unchanged until `stream` has passed the call.
  * Errors: as fa_constrained_step; FA_ERR_INVALID_ARG for a NULL input buffer; FA_ERR_CUDA

@@ -1,8 +1,9 @@
 """fa_constrained_step_host: the step with the probabilities and committed tokens in host
-memory, copied in chunks of sequences that overlap the emission reweighting.  Its outputs
-must equal those of fa_constrained_step on the same inputs already on the device, bit for
-bit (the same kernels over the same values), for batches split into several chunks, on the
-shared-memory-row reweight (random DFA) and the cell-store one (layered chain)."""
+memory, copied in up to eight pieces of consecutive positions (the first a thirty-second
+of the batch, each next one 1.4 times larger) that overlap the emission reweighting.  Its outputs must equal those of fa_constrained_step
+on the same inputs already on the device, bit for bit (the same kernels and row-block layout
+over the same values), for batches split into pieces that start and end inside sequences, on
+the shared-memory-row reweight (random DFA) and the cell-store one (layered chain)."""
 import numpy as np
 import pytest
 
