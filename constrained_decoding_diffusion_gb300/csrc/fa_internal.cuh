@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstring>
 #include <string>
 #include <vector>
 
@@ -130,6 +131,33 @@ __device__ __forceinline__ void fa_split(float x, float &m, int &e) {
     }
     e = ex - 127;
     m = __int_as_float((bits & 0x807fffff) | 0x3f800000);
+}
+
+// The bit pattern of a float and back (host and device).
+__host__ __device__ __forceinline__ uint32_t fa_f32_bits(float x) {
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    return u;
+}
+__host__ __device__ __forceinline__ float fa_bits_f32(uint32_t u) {
+    float x;
+    memcpy(&x, &u, sizeof x);
+    return x;
+}
+
+// The operand split of the tensor-core span products: x = p1 + p2 + p3 with bf16 parts (each
+// the upper 16 bits of a float).  p1 keeps x's leading 8 significant bits, p2 the leading 8 of
+// the remainder r = x - p1 and p3 = r - p2, which has at most 8 significant bits left; both
+// subtractions are exact in fp32, so the parts sum to x exactly (a subnormal p3 keeps its top
+// bits only, a loss below 2^-133).  Returns the three bf16 bit patterns in the low halves.
+__host__ __device__ __forceinline__ void fa_split_bf16x3(float x, uint32_t &b1, uint32_t &b2, uint32_t &b3) {
+    const uint32_t u = fa_f32_bits(x);
+    const float r = x - fa_bits_f32(u & 0xFFFF0000u);
+    const uint32_t ur = fa_f32_bits(r);
+    const float r2 = r - fa_bits_f32(ur & 0xFFFF0000u);
+    b1 = u >> 16;
+    b2 = ur >> 16;
+    b3 = fa_f32_bits(r2) >> 16;
 }
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): a counter-based generator; one call

@@ -177,27 +177,14 @@ __device__ __forceinline__ uint32_t kmaj_off(int row, int k) {
     return (uint32_t)((row >> 3) * KGRP + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
 }
 
-// x = p1 + p2 + p3 with bf16 parts (the upper 16 bits of each float): p1 keeps x's leading 8
-// significant bits, p2 the next 8 of the remainder and p3 the rest, each subtraction exact;
-// returns the three bf16 bit patterns in the low halves
-__device__ __forceinline__ void split_bf16x3(float x, uint32_t &b1, uint32_t &b2, uint32_t &b3) {
-    const uint32_t u = __float_as_uint(x);
-    const float r = x - __uint_as_float(u & 0xFFFF0000u);
-    const uint32_t ur = __float_as_uint(r);
-    const float r2 = r - __uint_as_float(ur & 0xFFFF0000u);
-    b1 = u >> 16;
-    b2 = ur >> 16;
-    b3 = __float_as_uint(r2) >> 16;
-}
-
 // the three bf16 parts of eight consecutive K-columns as one 16-byte core-matrix row per part
 __device__ __forceinline__ void pack_bf16x3(const float (&x)[8], uint4 &q1, uint4 &q2, uint4 &q3) {
     uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         uint32_t a1, a2, a3, c1, c2, c3;
-        split_bf16x3(x[2 * j], a1, a2, a3);
-        split_bf16x3(x[2 * j + 1], c1, c2, c3);
+        fa_split_bf16x3(x[2 * j], a1, a2, a3);
+        fa_split_bf16x3(x[2 * j + 1], c1, c2, c3);
         w1[j] = a1 | (c1 << 16);
         w2[j] = a2 | (c2 << 16);
         w3[j] = a3 | (c3 << 16);
