@@ -375,8 +375,8 @@ def test_step_long_sequence_global_topk(native):
 @pytest.mark.parametrize("S", [128, 200, 300, 400, 512])
 def test_step_tensor_core_span_products(native, S):
     """|S| >= 128 takes the tcgen05 span products (three bf16 parts per operand, six MMAs per
-    16 K-columns), one CTA per 128x256 output tile; 200, 300 and 400 leave ragged tiles in
-    both directions and a ragged last K step."""
+    16 K-columns) in 128x256 output tiles, walked by the persistent product kernel; 200, 300
+    and 400 leave ragged tiles in both directions and a ragged last K step."""
     rng = np.random.default_rng(S)
     fa = synth.random_dfa(S, 3000, 0.8, 12, seed=S)
     o = oracle.OracleFA(fa)
