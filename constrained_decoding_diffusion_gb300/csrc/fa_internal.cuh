@@ -160,6 +160,25 @@ __host__ __device__ __forceinline__ void fa_split_bf16x3(float x, uint32_t &b1, 
     b3 = fa_f32_bits(r2) >> 16;
 }
 
+// Pieces of the host-input copies of fa_constrained_step_host: bounds bound[0] = 0 <
+// bound[1] < ... < bound[n] = P over the batch's P positions, n <= FA_HOST_PIECES (n = 0 for
+// P = 0).  The first piece is P / 32 positions (at least one), each next one 1.4 times the
+// last, so that a piece's copy lands while the previous piece is reweighted (for a copy up
+// to 1.4 times slower per position than the reweighting), and the last piece is the rest.
+#define FA_HOST_PIECES 8
+inline int fa_host_pieces(size_t P, size_t (&bound)[FA_HOST_PIECES + 1]) {
+    int n = 0;
+    bound[0] = 0;
+    double len = (double)(P / 32 > 0 ? P / 32 : 1);
+    while (bound[n] < P) {
+        const size_t next = bound[n] + (size_t)len;
+        bound[n + 1] = (n == FA_HOST_PIECES - 1 || next > P) ? P : next;
+        ++n;
+        len *= 1.4;
+    }
+    return n;
+}
+
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): a counter-based generator; one call
 // maps (counter, key) to four independent 32-bit words.
 struct fa_u4 { uint32_t x, y, z, w; };

@@ -24,7 +24,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kHostChunks = 8;  // pieces of fa_constrained_step_host's input copies
+constexpr int kHostChunks = FA_HOST_PIECES;  // pieces of fa_constrained_step_host's input copies
 constexpr int kTmChunkMax = 4096, kTmChunkMin = 1024;  // tokens per block of the all-token marginals
 constexpr int kWarps = kThreads / 32;
 
@@ -2557,18 +2557,8 @@ fa_status reweight_from_host(const fa_automaton *a, int B, int L, const HostInpu
     fa_status st = copy_context(c);
     if (st != FA_OK) return st;
     const size_t S = (size_t)a->S, V = (size_t)a->V, P = (size_t)B * (size_t)L;
-    // piece bounds in positions: a first piece of P / 32, each next one 1.4 times the last
-    // (so that its copy lands while the previous piece is reweighted, for a copy up to 1.4
-    // times slower per position than the reweighting), the last piece the rest
     size_t bound[kHostChunks + 1];
-    int nch = 0;
-    bound[0] = 0;
-    double len = (double)std::max<size_t>(1, P / 32);
-    while (bound[nch] < P) {
-        bound[nch + 1] = nch == kHostChunks - 1 ? P : std::min(P, bound[nch] + (size_t)len);
-        ++nch;
-        len *= 1.4;
-    }
+    const int nch = fa_host_pieces(P, bound);
     cudaError_t e = cudaEventRecord(c->start, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->cs, c->start, 0);
     if (e == cudaSuccess)
